@@ -1,0 +1,156 @@
+"""CPU oracle for token-tree verification (ctypes wrapper over ``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by ``__graft_entry__.smoke``
+and by the benchmark's CPU-baseline leg.  The product library never imports,
+links or calls anything here, and this package never imports the product.
+
+All arithmetic lives in ``oracle.c`` (plain single-threaded C, IEEE double);
+this module only marshals numpy arrays.  Inputs are taken as float32 (bf16
+values widen to float32 exactly), so the oracle reads the same numbers as the
+GPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` with plain gcc (-O2, no
+    OpenMP, no BLAS, no -march flags: the same source builds on x86 and Arm)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+             "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    P = ctypes.c_void_p
+    i32, i64, u64 = ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
+    lib.oracle_philox4x64_10.argtypes = [P, P, P]
+    lib.oracle_philox4x64_10.restype = None
+    lib.oracle_uniform.argtypes = [u64, i64, i64, i64]
+    lib.oracle_uniform.restype = ctypes.c_double
+    lib.oracle_build_mask.argtypes = [P, P, i32, i32, P, P, P]
+    lib.oracle_build_mask.restype = i32
+    lib.oracle_tree_attn.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                     P, P, P, ctypes.c_double, P, i64]
+    lib.oracle_tree_attn.restype = i32
+    lib.oracle_tree_verify.argtypes = [P, P, P, P, P, i32, i32, i32, ctypes.c_float,
+                                       u64, P, P, P, P, i32, P]
+    lib.oracle_tree_verify.restype = i32
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def philox4x64_10(counter, key) -> np.ndarray:
+    """One Philox4x64-10 block: counter = 4 uint64 words, key = 2 uint64 words."""
+    ctr = _c(counter, np.uint64)
+    k = _c(key, np.uint64)
+    out = np.zeros(4, dtype=np.uint64)
+    _load().oracle_philox4x64_10(_ptr(ctr), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, node: int, request: int, kind: int) -> float:
+    """The method's uniform for (request, node, kind), in [0, 1)."""
+    return float(_load().oracle_uniform(seed & (2**64 - 1), node, request, kind))
+
+
+def build_mask(parents, offsets):
+    """Ancestor-or-self bitmask [T, 4] uint32, depth [T] int32, status [B]."""
+    par = _c(parents, np.int32)
+    off = _c(offsets, np.int32)
+    B, T = off.size - 1, par.size
+    mask = np.zeros((T, 4), dtype=np.uint32)
+    depth = np.full(T, -1, dtype=np.int32)
+    status = np.zeros(B, dtype=np.int32)
+    rc = _load().oracle_build_mask(_ptr(par), _ptr(off), B, T, _ptr(mask), _ptr(depth), _ptr(status))
+    if rc != 0:
+        raise ValueError(f"oracle_build_mask: status {rc}")
+    return mask, depth, status
+
+
+def tree_attn(q, k, v, prefix_lens, offsets, parents, scale: float = 0.0, rows=None):
+    """Dense masked attention per (node, head) in float64.
+
+    q [T, Hq, D]; k, v [B, Hkv, S_cap, D] (float32 or anything that widens to
+    it exactly).  Returns [T, Hq, D] float64, or [len(rows), D] when ``rows``
+    (flat node*Hq + head indices) is given."""
+    qa = _c(q, np.float32)
+    ka = _c(k, np.float32)
+    va = _c(v, np.float32)
+    T, Hq, D = qa.shape
+    B, Hkv, S_cap, D2 = ka.shape
+    assert D2 == D and va.shape == ka.shape
+    pl = _c(prefix_lens, np.int32)
+    off = _c(offsets, np.int32)
+    par = _c(parents, np.int32)
+    if rows is None:
+        out = np.zeros((T, Hq, D), dtype=np.float64)
+        rows_a, nrows = None, T * Hq
+    else:
+        rows_a = _c(rows, np.int64)
+        nrows = rows_a.size
+        out = np.zeros((nrows, D), dtype=np.float64)
+    rc = _load().oracle_tree_attn(_ptr(qa), _ptr(ka), _ptr(va), _ptr(out), B, T, Hq, Hkv, D,
+                                  S_cap, _ptr(pl), _ptr(off), _ptr(par), float(scale),
+                                  _ptr(rows_a), nrows)
+    if rc != 0:
+        raise ValueError(f"oracle_tree_attn: status {rc}")
+    return out
+
+
+def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperature: float,
+                seed: int, max_depth_plus1: int):
+    """Sequential root-to-leaf verification walk per request.
+
+    Returns a dict of numpy arrays: accept_len [B], path_nodes [B, W],
+    out_tokens [B, W], near_ties [B], status [B]."""
+    tl = _c(target_logits, np.float32)
+    T, V = tl.shape
+    dl = None if draft_logits is None else _c(draft_logits, np.float32)
+    tok = _c(tokens, np.int32)
+    par = _c(parents, np.int32)
+    off = _c(offsets, np.int32)
+    B = off.size - 1
+    W = int(max_depth_plus1)
+    res = dict(
+        accept_len=np.full(B, -1, dtype=np.int32),
+        path_nodes=np.full((B, W), -1, dtype=np.int32),
+        out_tokens=np.full((B, W), -1, dtype=np.int32),
+        near_ties=np.zeros(B, dtype=np.int32),
+        status=np.zeros(B, dtype=np.int32),
+    )
+    rc = _load().oracle_tree_verify(
+        _ptr(tl), _ptr(dl), _ptr(tok), _ptr(par), _ptr(off), B, T, V,
+        ctypes.c_float(temperature), seed & (2**64 - 1),
+        _ptr(res["accept_len"]), _ptr(res["path_nodes"]), _ptr(res["out_tokens"]),
+        _ptr(res["near_ties"]), W, _ptr(res["status"]))
+    if rc != 0:
+        raise ValueError(f"oracle_tree_verify: status {rc}")
+    return res
