@@ -1,0 +1,479 @@
+"""Benchmark: verified tree tokens/s for one tree-verification step on GB300.
+
+One step = the whole hot path over one batch: ancestor mask, tree attention
+(one attention layer over the request's KV prefix + tree), and verification
+(vocab softmax, acceptance walk, bonus token).  The workload is the
+LLaMA-7B-shaped tree-verify case: 1 request, 32 heads (MHA), head dim 128,
+bf16 KV prefix 2048, a width-5 depth-3 draft tree pruned to 64 nodes, vocab
+32000, stochastic verification at temperature 0.7.  Inputs are synthetic and
+seeded; the step's inputs rotate over enough device copies (> 4x L2) that
+every step reads them from HBM.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+Multi-GPU (torchrun, one rank per GPU) runs independent replicas: the path has
+no exchange step, so there is no data-path collective (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified tree tokens/s; tree-attn + verify HBM GB/s as % of GB300 peak"
+UNIT = "tree tokens/s"
+WORKLOAD = "llama7b"
+WORKLOAD_DESC = ("LLaMA-7B-shaped tree verify: B1, Hq=Hkv=32, D128, bf16 KV prefix 2048, "
+                 "w5 d3 draft tree pruned to 64 nodes, V32000 fp32 logits, T=0.7 stochastic")
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes
+# --------------------------------------------------------------------------
+def attn_bytes(w) -> int:
+    """KV of every prefix + tree slot read once per KV head, Q read once, O
+    written once (bf16)."""
+    el = 2
+    kv = sum(int(w.prefix_lens[b] + w.offsets[b + 1] - w.offsets[b]) for b in range(w.B)) * w.Hkv * w.D * el * 2
+    return kv + 2 * w.T * w.Hq * w.D * el
+
+
+def verify_bytes(w) -> int:
+    """Every node's target row; internal nodes' draft rows when stochastic."""
+    rows = w.T
+    if w.temperature > 0:
+        internal = 0
+        for b in range(w.B):
+            lo, hi = w.offsets[b], w.offsets[b + 1]
+            internal += len(set(w.parents[lo + 1:hi].tolist()))
+        rows += internal
+    return rows * w.V * 4
+
+
+def mask_bytes(w) -> int:
+    return w.T * (4 + 16 + 4)
+
+
+# --------------------------------------------------------------------------
+# environment helpers
+# --------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, only while the
+    kernel's source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    srcs = [os.path.join(ROOT, s) for s in d["sources"]]
+    if not all(os.path.exists(s) for s in srcs) or source_hash(srcs) != d["source_hash"]:
+        return None
+    return d["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = [l.split(",") for l in open(self.path).read().strip().splitlines() if l.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# the CUDA path
+# --------------------------------------------------------------------------
+class Step:
+    """Device buffers for one workload and R rotating input copies."""
+
+    def __init__(self, w, copies: int, seed: int):
+        import torch
+        import token_tree_verification_gb300 as ttv
+        self.ttv, self.torch, self.w = ttv, torch, w
+        dev = "cuda"
+        self.par = torch.as_tensor(w.parents).to(dev)
+        self.off = torch.as_tensor(w.offsets).to(dev)
+        self.tok = torch.as_tensor(w.tokens).to(dev)
+        self.pl = torch.as_tensor(w.prefix_lens).to(dev)
+        self.status = torch.zeros(w.B, dtype=torch.int32, device=dev)
+        self.mask = torch.empty((w.T, 4), dtype=torch.int32, device=dev)
+        self.depth = torch.empty(w.T, dtype=torch.int32, device=dev)
+        self.o = torch.empty((w.T, w.Hq, w.D), dtype=w.q.dtype, device=dev)
+        self.W = w.max_depth + 1
+        self.ws = ttv.make_verify_workspace(w.B, w.T, w.V)
+        self.outs = dict(
+            accept_len=torch.empty(w.B, dtype=torch.int32, device=dev),
+            path_nodes=torch.empty((w.B, self.W), dtype=torch.int32, device=dev),
+            out_tokens=torch.empty((w.B, self.W), dtype=torch.int32, device=dev),
+            near_ties=torch.empty(w.B, dtype=torch.int32, device=dev))
+        tl = torch.as_tensor(w.target_logits).to(dev)
+        dl = torch.as_tensor(w.draft_logits).to(dev) if w.draft_logits is not None else None
+        self.copies = []
+        for _ in range(copies):
+            self.copies.append(dict(q=w.q.to(dev).clone(), k=w.k_cache.to(dev).clone(),
+                                    v=w.v_cache.to(dev).clone(), tl=tl.clone(),
+                                    dl=None if dl is None else dl.clone()))
+        self.max_prefix = int(w.prefix_lens.max())
+        self.seed = seed
+
+    def run(self, i: int, stream=None, ev=None):
+        """Enqueue step i: mask, attention, verification.  ``ev`` (optional)
+        holds three (start, end) event pairs recorded around the kernels."""
+        ttv, w, c = self.ttv, self.w, self.copies[i % len(self.copies)]
+        if ev is not None:
+            ev[0].record()
+        ttv.build_tree_mask(self.par, self.off, self.status, mask=self.mask, depth=self.depth, stream=stream)
+        if ev is not None:
+            ev[1].record()
+            ev[2].record()
+        ttv.tree_attn(c["q"], c["k"], c["v"], self.pl, self.off, self.mask, self.max_prefix,
+                      self.status, o=self.o, stream=stream)
+        if ev is not None:
+            ev[3].record()
+            ev[4].record()
+        ttv.tree_verify(c["tl"], c["dl"], self.tok, self.par, self.off, w.temperature,
+                        self.seed + i, self.W, self.status, self.ws, outputs=self.outs, stream=stream)
+        if ev is not None:
+            ev[5].record()
+
+
+def run_native(args, rank, world, local_rank):
+    import torch
+    from token_tree_verification_gb300 import synthetic
+    torch.cuda.set_device(local_rank)
+    import token_tree_verification_gb300 as ttv
+    ttv.load()
+    w = synthetic.make_workload(WORKLOAD, seed=0, device="cuda", pad=0.0)
+    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    per_copy = (w.q.numel() + w.k_cache.numel() + w.v_cache.numel()) * w.q.element_size() \
+        + w.target_logits.nbytes + (w.draft_logits.nbytes if w.draft_logits is not None else 0)
+    copies = max(2, math.ceil(4 * l2 / per_copy) + 1)
+    st = Step(w, copies, seed=1000 * rank)
+    stream = torch.cuda.Stream()
+    K, Wm = args.steps, args.warmup
+
+    # eager warm-up configures the kernels before any capture
+    with torch.cuda.stream(stream):
+        for i in range(max(1, Wm)):
+            st.run(i)
+    torch.cuda.synchronize()
+
+    # capture: a warm-up graph of W steps and the timed graph(s) of K steps
+    chunk = min(K, args.graph_steps)
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)] for _ in range(chunk)]
+
+    def capture(n, with_events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                st.run(i, ev=evs[i] if with_events else None)
+        return g
+
+    g_warm = capture(max(1, Wm), False)
+    g_main = capture(chunk, True)
+    reps, rem = divmod(K, chunk)
+    g_rem = capture(rem, False) if rem else None
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0.record(stream)
+    for _ in range(reps):
+        g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    # If the timed region was shorter than a few clock samples, keep the same
+    # work running briefly so the clock record covers this load.
+    soak = False
+    if elapsed_ms < 1500:
+        soak = True
+        tend = time.time() + 1.0
+        while time.time() < tend:
+            g_main.replay()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    status = st.status.cpu().numpy()
+    if (status != 0).any():
+        raise RuntimeError(f"device status {status.tolist()}")
+
+    # per-kernel durations from the events of the last timed replay of g_main
+    d_mask = np.array([e[0].elapsed_time(e[1]) for e in evs[:chunk]])
+    d_attn = np.array([e[2].elapsed_time(e[3]) for e in evs[:chunk]])
+    d_ver = np.array([e[4].elapsed_time(e[5]) for e in evs[:chunk]])
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    ms_per_step = elapsed_ms / K
+    value = world * w.T * K / (elapsed_ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    ab, vb, mb = attn_bytes(w), verify_bytes(w), mask_bytes(w)
+    attn_ms = float(d_attn.mean())
+    ver_ms = float(d_ver.mean())
+    mask_ms = float(d_mask.mean())
+    achieved = ab / (attn_ms * 1e-3) / 1e9
+    traffic = profiled_traffic("tree_attn_llama7b")
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; no datasets or weights)",
+        "config": {"workload": WORKLOAD_DESC, "T": w.T, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "prefix": int(w.prefix_lens[0]), "V": w.V, "temperature": w.temperature,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs rotate over {copies} device copies ({copies * per_copy / 1e6:.0f} MB > 4x L2)",
+                   "launch": f"CUDA graph of {chunk} steps, replayed"},
+        "roofline": {"bound": "hbm", "kernel": "tree_attn_mma_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": ab, "launch_ms": attn_ms, "peak_kind": peak_kind},
+        "kernels": {
+            "mask": {"ms": mask_ms, "bytes": mb},
+            "attn": {"ms": attn_ms, "bytes": ab, "gbs": achieved},
+            "verify": {"ms": ver_ms, "bytes": vb, "gbs": vb / (ver_ms * 1e-3) / 1e9},
+            "step_gbs": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9,
+            "step_frac": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9 / peak,
+        },
+        "gpu_launches": 3 * K,
+        "clocks": clocks, "clock_window": "timed region + 1 s soak of the same graph" if soak else "timed region",
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(st, w, stream, args.e2e_steps)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    return result
+
+
+def run_e2e(st, w, stream, steps):
+    """Same metric through the public API with host buffers: each step copies
+    its inputs from pinned host memory and reads the verified tokens back."""
+    import torch
+    c = st.copies[0]
+    host = {k: v.cpu().pin_memory() for k, v in c.items() if v is not None}
+    tree_host = {"par": st.par.cpu().pin_memory(), "off": st.off.cpu().pin_memory(),
+                 "tok": st.tok.cpu().pin_memory(), "pl": st.pl.cpu().pin_memory()}
+    out_host = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in st.outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values()) + \
+        sum(v.numel() * v.element_size() for v in tree_host.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def one(i):
+        with torch.cuda.stream(stream):
+            for k, v in host.items():
+                c[k].copy_(v, non_blocking=True)
+            st.par.copy_(tree_host["par"], non_blocking=True)
+            st.off.copy_(tree_host["off"], non_blocking=True)
+            st.tok.copy_(tree_host["tok"], non_blocking=True)
+            st.pl.copy_(tree_host["pl"], non_blocking=True)
+            st.run(0)
+            for k, v in st.outs.items():
+                out_host[k].copy_(v, non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": w.T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# --------------------------------------------------------------------------
+# the oracle as CPU baseline / reference arm
+# --------------------------------------------------------------------------
+class OracleInputs:
+    def __init__(self, w):
+        self.w = w
+        self.q = w.q.float().cpu().numpy()
+        self.k = w.k_cache.float().cpu().numpy()
+        self.v = w.v_cache.float().cpu().numpy()
+
+
+def oracle_step_time(oi, nsel: int, seed: int):
+    """Wall time of one oracle step on a bounded sample: the full mask, the
+    full verification walk, and attention for ``nsel`` seeded (node, head)
+    rows, scaled to all rows."""
+    import oracle
+    w, q, k, v = oi.w, oi.q, oi.k, oi.v
+    n_rows = w.T * w.Hq
+    rng = np.random.default_rng(seed)
+    nsel = max(1, min(n_rows, nsel))
+    rows = np.sort(rng.choice(n_rows, size=nsel, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.build_mask(w.parents, w.offsets)
+    t1 = time.perf_counter()
+    oracle.tree_attn(q, k, v, w.prefix_lens, w.offsets, w.parents, rows=rows)
+    t2 = time.perf_counter()
+    oracle.tree_verify(w.target_logits, w.draft_logits, w.tokens, w.parents, w.offsets,
+                       w.temperature, seed, w.max_depth + 1)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t2 - t1) * (n_rows / nsel) + (t3 - t2), nsel, n_rows
+
+
+def cpu_baseline(w, nsel=512):
+    import oracle
+    oracle.build()
+    t, nsel, n_rows = oracle_step_time(OracleInputs(w), nsel, 0)
+    return {"value": w.T / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one step: full mask and verification walk, attention on {nsel} of {n_rows} "
+                      f"(node, head) rows scaled to all rows; plain C fp64, 1 thread",
+            "host_cores": os.cpu_count()}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step a bounded sample of the
+    same workload, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    from token_tree_verification_gb300 import synthetic
+    oracle.build()
+    w = synthetic.make_workload(WORKLOAD, seed=0, device="cpu", pad=0.0)
+    oi = OracleInputs(w)
+    n_rows = w.T * w.Hq
+    # size each step's attention sample so that K + W steps take ~2 minutes
+    t_row = oracle_step_time(oi, 64, 999)[0] / n_rows      # scaled time per row
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nsel = int(max(1, min(n_rows, budget / max(t_row, 1e-9) * 0.5)))
+    for i in range(args.warmup):
+        oracle_step_time(oi, nsel, 100 + i)
+    times = [oracle_step_time(oi, nsel, i)[0] for i in range(args.steps)]
+    ms = 1e3 * float(np.mean(times))
+    value = w.T / (ms * 1e-3)
+    sample = (f"each step: full mask and verification walk, attention on {nsel} "
+              f"of {n_rows} (node, head) rows scaled to all rows; plain C fp64, 1 thread")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "parallelism": "1 host thread"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--graph-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_native(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

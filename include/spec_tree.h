@@ -1,0 +1,197 @@
+/*
+ * spec_tree.h — C ABI of the GB300 token-tree verification library
+ * (libspec_tree.so, hand-written CUDA for sm_103a).
+ *
+ * The library computes the data-parallel hot path of tree-based speculative
+ * decoding: the tree mask, tree attention over a contiguous KV cache, and
+ * verification of the speculated tree against the target model's logits.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates device memory and keeps no state between calls.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL means the legacy default stream).  No call synchronises the host.
+ *  - Host-detectable errors (null pointers, bad sizes, workspace too small)
+ *    return a negative spec_status synchronously and launch nothing.
+ *  - Data-dependent errors found on the device (a malformed parent array, a
+ *    tree larger than SPEC_MAX_TREE_NODES, a token outside [0, V), a prefix
+ *    that does not fit the cache, a bounded wait that ran out) are written to
+ *    the caller's `status[b]` for request b with an atomic compare-and-swap
+ *    from 0, so the first error sticks.  The kernels never write 0: the caller
+ *    zero-fills `status` before a step and reads it after synchronising.  The
+ *    outputs of a request with an error are left untouched.
+ *  - A batch is packed ragged: request b owns global nodes
+ *    [tree_offsets[b], tree_offsets[b+1]) with tree_offsets[0] = 0 and
+ *    tree_offsets[B] = T.  Node indices inside a request (parents, path
+ *    nodes) are request-local; node 0 of each request is its root.
+ *  - A parent array satisfies parent[0] = -1 and 0 <= parent[i] < i, so node
+ *    order is topological and siblings are ordered by index.
+ *  - A return value of SPEC_OK means the work was enqueued.
+ */
+#ifndef SPEC_TREE_H
+#define SPEC_TREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_NULL = -1,            /* a required pointer is NULL */
+  SPEC_ERR_SHAPE = -2,           /* a size argument is out of range or unsupported */
+  SPEC_ERR_DTYPE = -3,           /* unknown spec_dtype */
+  SPEC_ERR_TREE_TOO_LARGE = -4,  /* N_b < 1, N_b > SPEC_MAX_TREE_NODES, bad offsets, or a path
+                                    longer than the output rows */
+  SPEC_ERR_BAD_PARENT = -5,      /* parent[0] != -1 or parent[i] not in [0, i) */
+  SPEC_ERR_TOKEN_RANGE = -6,     /* a speculated token outside [0, V) */
+  SPEC_ERR_WORKSPACE = -7,       /* workspace NULL or smaller than the _workspace_size value */
+  SPEC_ERR_CUDA = -8,            /* a CUDA runtime call or launch failed */
+  SPEC_ERR_TIMEOUT = -9,         /* a bounded device-side wait ran out (never expected) */
+  SPEC_ERR_PREFIX_RANGE = -10,   /* prefix_lens[b] < 0, > max_prefix, or L_b + N_b > S_cap */
+  SPEC_ERR_ALIGNMENT = -11       /* a pointer is not 16-byte aligned */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Largest tree (root included) one request may carry. */
+#define SPEC_MAX_TREE_NODES 128
+
+/*
+ * spec_build_tree_mask — step A1, the tree-attention mask.
+ *
+ * Source: SpecInfer news write-up (sunluscious.com.cn), section
+ * "Token 樹驗證器": verification uses a mask matrix built from the token tree;
+ * SpecInfer developer article "SpecInfer：基于树结构的LLM推测性推理加速技术",
+ * §2.1 (tree nodes keep a parent pointer; tree_attention snippet: a mask entry
+ * of 0 hides the key).
+ *
+ * For every node i of request b: bit a of mask[i] is set iff a == i or a is
+ * an ancestor of i (a node sees itself and its ancestors), and
+ * depth[i] = number of edges from the root.
+ *
+ *   parents      [T]    int32, request-local parent indices (see conventions)
+ *   tree_offsets [B+1]  int32
+ *   mask         [T][4] uint32 out: 128-bit ancestor-or-self set, bit a of node
+ *                       i is word a/32, bit a%32
+ *   depth        [T]    int32 out
+ *   status       [B]    int32 in/out (see conventions)
+ * Errors on the device: SPEC_ERR_TREE_TOO_LARGE, SPEC_ERR_BAD_PARENT.
+ */
+int spec_build_tree_mask(const int32_t *parents, const int32_t *tree_offsets, int B, int T,
+                         uint32_t *mask, int32_t *depth, int32_t *status, void *stream);
+
+/*
+ * Bytes of scratch spec_tree_attn needs for these sizes.  The current kernels
+ * merge their key splits on chip, so this is 0; the argument stays part of
+ * the ABI so a future split layout needs no signature change.
+ */
+size_t spec_tree_attn_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_prefix);
+
+/*
+ * spec_tree_attn — steps A2 and A3, tree attention with a split-KV merge.
+ *
+ * Source: SpecInfer developer article §2.1, tree_attention snippet (scores of
+ * the queries against the keys, masked entries removed, softmax, times V);
+ * SpecInfer news write-up "Token 樹驗證器" (the tree's K/V are appended to the
+ * KV cache depth-first, so all paths decode in one pass).
+ *
+ * For node i of request b and query head h, with KV head g = h / (Hq/Hkv)
+ * and scale s (softmax_scale, or 1/sqrt(D) when softmax_scale <= 0):
+ *   o[i][h] = sum_{j in K(i)} softmax_j(s * q[i][h] . k[b][g][j]) * v[b][g][j]
+ * where K(i) = {0 .. L_b-1} (the prefix) u {L_b + a : bit a of mask[i]}.
+ * The tree's own K/V must already sit at cache slots [L_b, L_b + N_b) in node
+ * order.  Slots >= L_b + N_b are never read into the result (they may hold
+ * anything, NaN included).
+ *
+ *   q            [T][Hq][D]           dtype (bf16 or f32)
+ *   k_cache,
+ *   v_cache      [B][Hkv][S_cap][D]   dtype; 16-byte aligned
+ *   o            [T][Hq][D]           dtype out
+ *   dtype        SPEC_BF16 (tensor-core path) or SPEC_F32 (plain fp32 path)
+ *   D            64 or 128;  Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8}
+ *   max_prefix   host-side upper bound on every prefix_lens[b]; sizes the
+ *                key splits (a larger value is safe, only slower)
+ *   prefix_lens  [B] int32 (L_b)
+ *   mask         [T][4] uint32 from spec_build_tree_mask (bits >= N_b ignored)
+ *   workspace    may be NULL when spec_tree_attn_workspace_size() is 0
+ * Accumulation is fp32; the bf16 path rounds the softmax weights to bf16 for
+ * the P·V product and rounds o to bf16.
+ * Errors on the device: SPEC_ERR_TREE_TOO_LARGE, SPEC_ERR_PREFIX_RANGE,
+ * SPEC_ERR_TIMEOUT.
+ */
+int spec_tree_attn(const void *q, const void *k_cache, const void *v_cache, void *o, int dtype,
+                   int B, int T, int Hq, int Hkv, int D, int S_cap, int max_prefix,
+                   const int32_t *prefix_lens, const int32_t *tree_offsets, const uint32_t *mask,
+                   float softmax_scale, void *workspace, size_t workspace_bytes, int32_t *status,
+                   void *stream);
+
+/*
+ * Bytes of scratch spec_tree_verify needs: per-node acceptance flags and
+ * fallback tokens plus one arrival counter per request.  The workspace must
+ * be zero-filled before its FIRST use; every call leaves the counters at zero
+ * again, so one buffer can be reused by later calls on the same stream.  Two
+ * calls that run at the same time need two workspaces.
+ */
+size_t spec_tree_verify_workspace_size(int B, int T, int V);
+
+/*
+ * spec_tree_verify — steps V1-V4 and R, verification of the token tree.
+ *
+ * Sources: SpecInfer developer article §2.1 (the accept stage keeps the
+ * longest verified prefix); speculative-decoding explainer
+ * (intelliparadigm.com) §2.2 三阶段工作流程详解: stage 2 computes the accept
+ * probability alpha = min(1, p_target / p_draft); stage 3 checks left to right,
+ * stops at the first rejection and replaces it with a new target prediction,
+ * keeping the output distribution equal to the target model's.
+ *
+ * Greedy (temperature == 0): at node u (starting at the root) accept the
+ * first child, in index order, whose token equals argmax of u's target logits
+ * (lowest index on ties); when none matches, emit that argmax and stop.
+ * Stochastic (temperature > 0): p = softmax(target/temperature),
+ * q = softmax(draft/temperature) of node u; with r = p, test u's children c in
+ * index order: accept iff U(c) < min(1, r(x_c) / q(x_c)); after a rejection
+ * r becomes max(0, r - q) renormalised (unchanged if that is all zero).  When
+ * every child is rejected, or u is a leaf, emit a draw from r by inverse CDF
+ * and stop.  The emitted tokens are the accepted path's tokens followed by
+ * that one extra (bonus) token.
+ * Uniforms: Philox4x64-10 with key (seed, 0) and counter (node, b, kind, 0),
+ * node request-local, kind 0 for the accept test of child `node`, kind 1 for
+ * the draw at `node`; U = (first output word >> 40) * 2^-24.
+ *
+ *   target_logits [T][V] f32
+ *   draft_logits  [T][V] f32 (row u is the draft distribution u's children
+ *                 were drawn from); may be NULL when temperature == 0
+ *   tokens        [T] int32, the token node i proposes (the root's is ignored)
+ *   parents       [T] int32
+ *   accept_len    [B] int32 out: accepted speculated tokens (path length)
+ *   path_nodes    [B][max_depth_plus1] int32 out: root (0), then the accepted
+ *                 nodes; unused entries -1
+ *   out_tokens    [B][max_depth_plus1] int32 out: accepted tokens then the
+ *                 bonus token (accept_len + 1 entries); unused entries -1
+ *   near_ties     [B] int32 out: decisions on the walked path whose uniform
+ *                 lay within 1e-6 of its threshold (fp32 rounding could have
+ *                 flipped them)
+ *   max_depth_plus1  row stride of path_nodes / out_tokens; must exceed the
+ *                 depth of every tree
+ * Errors on the device: SPEC_ERR_TREE_TOO_LARGE, SPEC_ERR_BAD_PARENT,
+ * SPEC_ERR_TOKEN_RANGE, SPEC_ERR_TIMEOUT.
+ */
+int spec_tree_verify(const float *target_logits, const float *draft_logits,
+                     const int32_t *tokens, const int32_t *parents,
+                     const int32_t *tree_offsets, int B, int T, int V, float temperature,
+                     uint64_t seed, int32_t *accept_len, int32_t *path_nodes,
+                     int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
+                     void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/* Human-readable name of a spec_status value (static storage). */
+const char *spec_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_TREE_H */

@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every entry point declared in
+include/*.h; host-side argument checks return their status codes without
+touching a GPU (they run before any CUDA call)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(spec_\w+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from token_tree_verification_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert {"spec_build_tree_mask", "spec_tree_attn", "spec_tree_verify"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(-11, 1):
+        s = lib.spec_status_string(code).decode()
+        assert s.startswith("SPEC_")
+    assert b"unknown" in lib.spec_status_string(42)
+
+
+def test_workspace_sizes(lib):
+    assert lib.spec_tree_attn_workspace_size(1, 64, 32, 32, 128, 2048) == 0
+    s1 = lib.spec_tree_verify_workspace_size(1, 64, 32000)
+    s2 = lib.spec_tree_verify_workspace_size(16, 900, 32000)
+    assert s1 > 0 and s2 > s1 and s2 % 256 == 0
+    assert lib.spec_tree_verify_workspace_size(0, 1, 1) == 0
+
+
+def test_host_side_validation(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)   # never dereferenced: validation fails before any launch
+    # null pointers
+    assert lib.spec_build_tree_mask(None, fake, 1, 1, fake, fake, fake, None) == -1
+    assert lib.spec_tree_attn(fake, fake, None, fake, 1, 1, 1, 1, 1, 128, 8, 8, fake, fake, fake,
+                              0.0, None, 0, fake, None) == -1
+    # sizes
+    assert lib.spec_build_tree_mask(fake, fake, 0, 1, fake, fake, fake, None) == -2
+    assert lib.spec_build_tree_mask(fake, fake, 1, 129, fake, fake, fake, None) == -2
+    assert lib.spec_tree_attn(fake, fake, fake, fake, 1, 1, 1, 4, 4, 96, 8, 8, fake, fake, fake,
+                              0.0, None, 0, fake, None) == -2          # D = 96 unsupported
+    assert lib.spec_tree_attn(fake, fake, fake, fake, 1, 1, 1, 12, 4, 64, 8, 8, fake, fake, fake,
+                              0.0, None, 0, fake, None) == -2          # G = 3 unsupported
+    assert lib.spec_tree_attn(fake, fake, fake, fake, 7, 1, 1, 4, 4, 64, 8, 8, fake, fake, fake,
+                              0.0, None, 0, fake, None) == -3          # dtype
+    assert lib.spec_tree_attn(P(0x1004), fake, fake, fake, 1, 1, 1, 4, 4, 64, 8, 8, fake, fake,
+                              fake, 0.0, None, 0, fake, None) == -11   # alignment
+    # verify: workspace, temperature, missing draft rows
+    V = 1000
+    ws = lib.spec_tree_verify_workspace_size(1, 8, V)
+    args = [fake, fake, fake, fake, fake, 1, 8, V]
+    outs = [fake, fake, fake, fake, 4]
+    assert lib.spec_tree_verify(*args, ctypes.c_float(0.0), 0, *outs, None, 0, fake, None) == -7
+    assert lib.spec_tree_verify(*args, ctypes.c_float(0.0), 0, *outs, fake, ws - 1, fake, None) == -7
+    assert lib.spec_tree_verify(*args, ctypes.c_float(-1.0), 0, *outs, fake, ws, fake, None) == -2
+    assert lib.spec_tree_verify(fake, None, fake, fake, fake, 1, 8, V, ctypes.c_float(0.7), 0,
+                                *outs, fake, ws, fake, None) == -1
+    assert lib.spec_tree_verify(*args, ctypes.c_float(float("nan")), 0, *outs, fake, ws, fake,
+                                None) == -2

@@ -1,0 +1,101 @@
+"""GPU steps A2-A3 (spec_tree_attn) against the oracle's dense masked
+attention, within max|d| <= 1e-2 max|ref| and relative error <= 2e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import assert_attn_close, gpu_attn, oracle_attn_rows
+from token_tree_verification_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+
+def full_oracle(w):
+    return oracle.tree_attn(w.q.float().numpy(), w.k_cache.float().numpy(), w.v_cache.float().numpy(),
+                            w.prefix_lens, w.offsets, w.parents)
+
+
+def test_tiny_fp32(gpu_lib):
+    w = synthetic.make_workload("tiny", seed=0)
+    got, st = gpu_attn(w)
+    assert (st == 0).all()
+    assert_attn_close(got, full_oracle(w), "tiny fp32")
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,L,N,B", [
+    (128, 4, 4, 0, 8, 1),        # empty prefix
+    (128, 4, 4, 1, 1, 1),        # root only, one prefix key
+    (128, 2, 2, 63, 7, 2),       # ragged tail inside a tile
+    (128, 2, 2, 64, 64, 1),      # tree fills exactly one tile
+    (64, 8, 2, 200, 33, 3),      # D = 64, G = 4, several requests
+    (128, 16, 2, 129, 40, 2),    # G = 8: rows = 320 (5 row blocks)
+    (128, 4, 2, 300, 128, 1),    # largest tree
+    (64, 2, 1, 1000, 17, 2),     # many tiles, many splits
+])
+def test_bf16_shapes(gpu_lib, D, Hq, Hkv, L, N, B):
+    w = synthetic.make_workload("llama70b_gqa", seed=D + Hq + L + N, B=B, Hq=Hq, Hkv=Hkv, D=D, L=L,
+                                N=N, depth=min(5, N - 1), width=8 if N > 40 else 4, V=64)
+    got, st = gpu_attn(w)
+    assert (st == 0).all()
+    assert_attn_close(got, full_oracle(w), f"D{D} Hq{Hq} Hkv{Hkv} L{L} N{N} B{B}")
+
+
+def test_fp32_ragged(gpu_lib):
+    w = synthetic.make_workload("tiny", seed=5, B=3, L=77, N=20, depth=4, width=4, Hq=8, Hkv=2, D=128)
+    got, st = gpu_attn(w)
+    assert (st == 0).all()
+    assert_attn_close(got, full_oracle(w), "fp32 ragged")
+
+
+def test_llama7b_full(gpu_lib):
+    w = synthetic.make_workload("llama7b", seed=0, device="cuda")
+    got, st = gpu_attn(w)
+    assert (st == 0).all()
+    rows = np.arange(w.T * w.Hq)
+    ref = oracle_attn_rows(w, rows)
+    assert_attn_close(got.reshape(-1, w.D), ref, "llama7b")
+
+
+@pytest.mark.parametrize("name", ["dynamic", "llama70b_gqa", "long_chain", "long_tree"])
+def test_large_configs_sampled(gpu_lib, name):
+    w = synthetic.make_workload(name, seed=0, device="cuda")
+    got, st = gpu_attn(w)
+    assert (st == 0).all()
+    rng = np.random.default_rng(1)
+    n_rows = w.T * w.Hq
+    rows = np.unique(np.concatenate([
+        rng.integers(0, n_rows, 96),
+        # last node of every request, first and last head
+        (w.offsets[1:] - 1) * w.Hq, (w.offsets[1:] - 1) * w.Hq + w.Hq - 1, w.offsets[:-1] * w.Hq]))
+    ref = oracle_attn_rows(w, rows)
+    assert_attn_close(got.reshape(-1, w.D)[rows], ref, name)
+
+
+def test_nan_padding_never_leaks(gpu_lib):
+    w = synthetic.make_workload("llama7b", seed=3, L=100, N=10, width=3, depth=2, Hq=4, Hkv=4, V=64,
+                                S_cap=256, pad=float("nan"))
+    got, st = gpu_attn(w)
+    assert np.isfinite(got).all()
+    assert_attn_close(got, full_oracle(w), "nan padding")
+
+
+def test_device_errors(gpu_lib):
+    w = synthetic.make_workload("llama7b", seed=4, B=3, L=100, N=10, width=3, depth=2, Hq=4, Hkv=4,
+                                V=64, S_cap=128)
+    pl = w.prefix_lens.copy()
+    pl[1] = 125          # 125 + 10 > S_cap
+    w2 = w
+    w2.prefix_lens = pl
+    o_before = torch.full_like(w.q, 7.0).cuda()
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
+    import token_tree_verification_gb300 as ttv
+    from parity import dev
+    mask, _ = ttv.build_tree_mask(dev(w.parents, torch.int32), dev(w.offsets, torch.int32), status)
+    o = ttv.tree_attn(w.q.cuda(), w.k_cache.cuda(), w.v_cache.cuda(), dev(pl, torch.int32),
+                      dev(w.offsets, torch.int32), mask, 125, status, o=o_before)
+    torch.cuda.synchronize()
+    assert status.cpu().tolist() == [0, -10, 0]
+    lo, hi = w.offsets[1], w.offsets[2]
+    assert (o[lo:hi].float() == 7.0).all()        # untouched
+    assert not (o[: w.offsets[1]].float() == 7.0).all()

@@ -1,0 +1,137 @@
+"""GPU steps V1-V4 (spec_tree_verify) against the oracle's sequential walk:
+greedy bit-exact; stochastic bit-exact except counted near-ties; the lossless
+chi-square test on the GPU path."""
+import numpy as np
+import pytest
+import torch
+
+from parity import assert_verify_match, dev, gpu_verify, oracle_verify
+from test_oracle_verify import chi2_ok, run_lossless
+from token_tree_verification_gb300 import synthetic
+import token_tree_verification_gb300 as ttv
+
+pytestmark = pytest.mark.gpu
+
+
+def check(w, seed, temperature=None, W=None):
+    g = gpu_verify(w, seed, W=W, temperature=temperature)
+    o = oracle_verify(w, seed, W=W, temperature=temperature)
+    ties = assert_verify_match(g, o, w.parents, w.tokens, w.offsets, f"{w.name} seed {seed}")
+    return g, o, ties
+
+
+@pytest.mark.parametrize("temp", [0.0, 1.0])
+def test_tiny(gpu_lib, temp):
+    for seed in range(20):
+        w = synthetic.make_workload("tiny", seed=seed, temperature=temp)
+        g, o, ties = check(w, seed)
+        if temp == 0.0:
+            assert ties == 0
+
+
+def test_llama7b_stochastic(gpu_lib):
+    w = synthetic.make_workload("llama7b", seed=0)
+    total_ties = 0
+    lens = []
+    for seed in range(8):
+        g, o, ties = check(w, seed)
+        total_ties += ties
+        lens.append(int(g["accept_len"][0]))
+    assert total_ties <= 1
+    assert max(lens) >= 1          # this tree accepts something at T = 0.7
+
+
+def test_llama7b_greedy(gpu_lib):
+    w = synthetic.make_workload("llama7b", seed=1)
+    check(w, 0, temperature=0.0)
+
+
+def test_dynamic_greedy(gpu_lib):
+    w = synthetic.make_workload("dynamic", seed=0)
+    g, o, ties = check(w, 0)
+    assert ties == 0 and (g["status"] == 0).all()
+
+
+@pytest.mark.parametrize("name,temp", [("llama70b_gqa", None), ("long_tree", None), ("long_tree", 0.0),
+                                       ("long_chain", None), ("long_chain", 0.0)])
+def test_large_configs(gpu_lib, name, temp):
+    w = synthetic.make_workload(name, seed=2, L=64)   # verify does not read the KV cache
+    check(w, 5, temperature=temp)
+
+
+def test_accepting_trees(gpu_lib):
+    """Draft equal to the target makes long accepted paths (the walk descends)."""
+    w = synthetic.make_workload("llama70b_gqa", seed=3, L=8, V=512)
+    w.draft_logits = w.target_logits.copy()
+    g, o, _ = check(w, 1)
+    assert (g["accept_len"] >= 1).all()
+
+
+def test_vocab_edge_sizes(gpu_lib):
+    for V in (1, 3, 8, 4095, 4096, 4097, 32003, 65536, 150000):
+        w = synthetic.make_workload("tiny", seed=V % 97, V=V, B=2, N=12, depth=3, width=4)
+        for temp in (0.0, 0.9):
+            check(w, V, temperature=temp)
+
+
+def test_errors(gpu_lib):
+    w = synthetic.make_workload("tiny", seed=9, B=4, N=8, V=100)
+    tok = w.tokens.copy()
+    tok[w.offsets[1] + 3] = 100                 # request 1: token out of range
+    par = w.parents.copy()
+    par[w.offsets[2] + 2] = 5                   # request 2: forward parent
+    g = gpu_verify(w, 0, tokens=tok, parents=par, temperature=1.0)
+    assert g["status"].tolist() == [0, -6, -5, 0]
+    g2 = gpu_verify(w, 0, W=2, temperature=1.0)  # depth-3 trees do not fit 2 output slots
+    assert (g2["status"] == -4).all()
+
+
+def test_workspace_reuse_and_streams(gpu_lib):
+    """Counters are left at zero: the same workspace serves repeated calls."""
+    w = synthetic.make_workload("llama7b", seed=0, L=64)
+    B, T, V = w.B, w.T, w.V
+    ws = ttv.make_verify_workspace(B, T, V)
+    res = []
+    for _ in range(3):
+        status = torch.zeros(B, dtype=torch.int32, device="cuda")
+        r = ttv.tree_verify(dev(w.target_logits), dev(w.draft_logits), dev(w.tokens), dev(w.parents),
+                            dev(w.offsets), 0.7, 11, w.max_depth + 1, status, ws)
+        torch.cuda.synchronize()
+        res.append(r["out_tokens"].cpu().numpy().copy())
+    assert (ws[:256].cpu().numpy() == 0).all()
+    assert all((r == res[0]).all() for r in res)
+
+
+def _gpu_verify_np(tl, dl, tok, par, off, temp, seed, W):
+    B = len(off) - 1
+    T, V = tl.shape
+    status = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ws = ttv.make_verify_workspace(B, T, V)
+    r = ttv.tree_verify(dev(tl), dev(dl), dev(tok), dev(par), dev(off), temp, seed, W, status, ws)
+    out = {k: v.cpu().numpy() for k, v in r.items()}
+    assert (status.cpu().numpy() == 0).all()
+    return out
+
+
+def test_lossless_chi_square_gpu(gpu_lib):
+    c1, c2, p1, p12 = run_lossless(_gpu_verify_np, 1_000_000, 1.0, seed=0)
+    for c, p in ((c1, p1), (c2, p12)):
+        chi, bound = chi2_ok(c, p)
+        assert chi <= bound, (chi, bound)
+
+
+def test_lossless_trials_match_oracle(gpu_lib):
+    """The GPU and the oracle agree trial by trial on the chi-square workload."""
+    import oracle
+    from test_oracle_verify import LOSSLESS_PARENTS, lossless_tables, lossless_trial_batch
+    tab_t, tab_d = lossless_tables(3)
+    rng = np.random.default_rng(4)
+    n = 50000
+    tok, tl, dl = lossless_trial_batch(rng, tab_t, tab_d, np.zeros(n, np.int64), 0, 0.8)
+    par = np.tile(LOSSLESS_PARENTS, n)
+    off = (np.arange(n + 1) * LOSSLESS_PARENTS.size).astype(np.int32)
+    g = _gpu_verify_np(tl, dl, tok.reshape(-1), par, off, 0.8, 77, 4)
+    g["status"] = np.zeros(n, np.int32)
+    o = oracle.tree_verify(tl, dl, tok.reshape(-1), par, off, 0.8, 77, 4)
+    ties = assert_verify_match(g, o, par, tok.reshape(-1), off, "lossless trials")
+    assert ties <= n * 1e-4

@@ -1,0 +1,188 @@
+"""ctypes binding of ``libspec_tree.so`` (declared in include/spec_tree.h).
+
+Argument marshalling only: torch tensors are checked for device, dtype and
+contiguity, and their device pointers plus the current CUDA stream are passed
+to the C ABI.  Every step of the computation runs in the library's CUDA
+kernels; if the library cannot be loaded the calls raise, there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+STATUS = {
+    0: "SPEC_OK", -1: "SPEC_ERR_NULL", -2: "SPEC_ERR_SHAPE", -3: "SPEC_ERR_DTYPE",
+    -4: "SPEC_ERR_TREE_TOO_LARGE", -5: "SPEC_ERR_BAD_PARENT", -6: "SPEC_ERR_TOKEN_RANGE",
+    -7: "SPEC_ERR_WORKSPACE", -8: "SPEC_ERR_CUDA", -9: "SPEC_ERR_TIMEOUT",
+    -10: "SPEC_ERR_PREFIX_RANGE", -11: "SPEC_ERR_ALIGNMENT",
+}
+SPEC_F32, SPEC_BF16 = 0, 1
+MAX_TREE_NODES = 128
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libspec_tree.so")
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with token_tree_verification_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I, U64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_float
+    lib.spec_build_tree_mask.argtypes = [P, P, I, I, P, P, P, P]
+    lib.spec_build_tree_mask.restype = I
+    lib.spec_tree_attn_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.spec_tree_attn_workspace_size.restype = SZ
+    lib.spec_tree_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, F, P, SZ, P, P]
+    lib.spec_tree_attn.restype = I
+    lib.spec_tree_verify_workspace_size.argtypes = [I, I, I]
+    lib.spec_tree_verify_workspace_size.restype = SZ
+    lib.spec_tree_verify.argtypes = [P, P, P, P, P, I, I, I, F, U64, P, P, P, P, I, P, SZ, P, P]
+    lib.spec_tree_verify.restype = I
+    lib.spec_status_string.argtypes = [I]
+    lib.spec_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().spec_status_string(int(code)).decode()
+    except Exception:  # library absent: fall back to the name table
+        return STATUS.get(int(code), f"status {code}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SpecError(code, where)
+
+
+def build_tree_mask(parents, offsets, status, mask=None, depth=None, stream=None):
+    """Step A1.  parents [T] int32, offsets [B+1] int32, status [B] int32 (zeroed
+    by the caller).  Returns (mask [T, 4] int32 view of the uint32 bits, depth [T])."""
+    lib = load()
+    _dev(parents, torch.int32, "parents")
+    _dev(offsets, torch.int32, "offsets")
+    _dev(status, torch.int32, "status")
+    T, B = parents.numel(), offsets.numel() - 1
+    if mask is None:
+        mask = torch.empty((T, 4), dtype=torch.int32, device=parents.device)
+    if depth is None:
+        depth = torch.empty(T, dtype=torch.int32, device=parents.device)
+    _check(lib.spec_build_tree_mask(_ptr(parents), _ptr(offsets), B, T, _ptr(mask), _ptr(depth),
+                                    _ptr(status), _stream(stream)), "spec_build_tree_mask")
+    return mask, depth
+
+
+def tree_attn_workspace_size(B, T, Hq, Hkv, D, max_prefix) -> int:
+    return int(load().spec_tree_attn_workspace_size(B, T, Hq, Hkv, D, max_prefix))
+
+
+def tree_attn(q, k_cache, v_cache, prefix_lens, offsets, mask, max_prefix, status, o=None,
+              softmax_scale: float = 0.0, workspace=None, stream=None):
+    """Steps A2-A3.  q [T, Hq, D]; k_cache, v_cache [B, Hkv, S_cap, D]; bf16 or fp32."""
+    lib = load()
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise TypeError("q must be bfloat16 or float32")
+    _dev(q, dt, "q")
+    _dev(k_cache, dt, "k_cache")
+    _dev(v_cache, dt, "v_cache")
+    _dev(prefix_lens, torch.int32, "prefix_lens")
+    _dev(offsets, torch.int32, "offsets")
+    _dev(mask, torch.int32, "mask")
+    _dev(status, torch.int32, "status")
+    T, Hq, D = q.shape
+    B, Hkv, S_cap, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / k_cache / v_cache shapes disagree")
+    if o is None:
+        o = torch.empty_like(q)
+    ws_need = tree_attn_workspace_size(B, T, Hq, Hkv, D, max_prefix)
+    if ws_need and workspace is None:
+        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
+    _check(lib.spec_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+                              SPEC_BF16 if dt == torch.bfloat16 else SPEC_F32, B, T, Hq, Hkv, D,
+                              S_cap, int(max_prefix), _ptr(prefix_lens), _ptr(offsets), _ptr(mask),
+                              float(softmax_scale), _ptr(workspace),
+                              0 if workspace is None else workspace.numel(), _ptr(status),
+                              _stream(stream)), "spec_tree_attn")
+    return o
+
+
+def tree_verify_workspace_size(B, T, V) -> int:
+    return int(load().spec_tree_verify_workspace_size(B, T, V))
+
+
+def make_verify_workspace(B, T, V, device="cuda"):
+    """A zero-filled verification workspace (reusable across calls on one stream)."""
+    return torch.zeros(tree_verify_workspace_size(B, T, V), dtype=torch.uint8, device=device)
+
+
+def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperature: float,
+                seed: int, max_depth_plus1: int, status, workspace, outputs=None, stream=None):
+    """Steps V1-V4.  Returns dict(accept_len, path_nodes, out_tokens, near_ties)
+    of device tensors."""
+    lib = load()
+    _dev(target_logits, torch.float32, "target_logits")
+    if draft_logits is not None:
+        _dev(draft_logits, torch.float32, "draft_logits")
+    _dev(tokens, torch.int32, "tokens")
+    _dev(parents, torch.int32, "parents")
+    _dev(offsets, torch.int32, "offsets")
+    _dev(status, torch.int32, "status")
+    _dev(workspace, torch.uint8, "workspace")
+    T, V = target_logits.shape
+    B = offsets.numel() - 1
+    W = int(max_depth_plus1)
+    dev = target_logits.device
+    if outputs is None:
+        outputs = dict(
+            accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+            path_nodes=torch.empty((B, W), dtype=torch.int32, device=dev),
+            out_tokens=torch.empty((B, W), dtype=torch.int32, device=dev),
+            near_ties=torch.empty(B, dtype=torch.int32, device=dev),
+        )
+    _check(lib.spec_tree_verify(_ptr(target_logits), _ptr(draft_logits), _ptr(tokens),
+                                _ptr(parents), _ptr(offsets), B, T, V, float(temperature),
+                                int(seed) & (2**64 - 1), _ptr(outputs["accept_len"]),
+                                _ptr(outputs["path_nodes"]), _ptr(outputs["out_tokens"]),
+                                _ptr(outputs["near_ties"]), W, _ptr(workspace), workspace.numel(),
+                                _ptr(status), _stream(stream)), "spec_tree_verify")
+    return outputs

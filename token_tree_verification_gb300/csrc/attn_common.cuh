@@ -1,0 +1,75 @@
+// Shared pieces of the tree-attention kernels: argument block, per-request
+// key geometry, visibility of a key to a row, and the SW128 smem addressing
+// produced by TMA tile loads.
+#pragma once
+
+#include "common.cuh"
+
+namespace spec {
+
+constexpr int kKeyTile = 64;   // keys per TMA tile
+
+struct AttnArgs {
+  const void *q;
+  const void *k;           // [B][Hkv][S_cap][D] (read directly by the fp32 path)
+  const void *v;
+  void *o;
+  const int32_t *prefix_lens;
+  const int32_t *offsets;
+  const uint4 *mask;
+  int32_t *status;
+  int B, T, Hq, Hkv, G, D, S_cap;
+  float scale_log2;        // softmax scale * log2(e)
+  int rows_per_cta;        // rows of one CTA (node-major, head-minor)
+};
+
+// Geometry of request b as one CTA sees it.  Keys [0, L) are the prefix,
+// keys [L, L + n) the tree slots in node order.
+struct ReqGeom {
+  int lo, n, L, keys, err;
+};
+
+__device__ __forceinline__ ReqGeom request_geometry(const AttnArgs &a, int b) {
+  ReqGeom r;
+  r.lo = __ldg(a.offsets + b);
+  const int hi = __ldg(a.offsets + b + 1);
+  r.n = hi - r.lo;
+  r.L = __ldg(a.prefix_lens + b);
+  r.err = 0;
+  if (r.lo < 0 || hi > a.T || r.n < 1 || r.n > SPEC_MAX_TREE_NODES) r.err = SPEC_ERR_TREE_TOO_LARGE;
+  else if (r.L < 0 || r.L + r.n > a.S_cap) r.err = SPEC_ERR_PREFIX_RANGE;
+  r.keys = r.err ? 0 : r.L + r.n;
+  return r;
+}
+
+// Key `key` is visible to a row whose node has ancestor set `m` (bits >= n
+// already cleared): prefix keys always, tree key L + a iff bit a is set.
+__device__ __forceinline__ bool key_visible(int key, int L, int keys, const uint4 &m) {
+  if (key < L) return true;
+  if (key >= keys) return false;
+  const int a = key - L;
+  const uint32_t w = (a < 64) ? ((a < 32) ? m.x : m.y) : ((a < 96) ? m.z : m.w);
+  return (w >> (a & 31)) & 1u;
+}
+
+// Ancestor set of a node with bits at or above n cleared, so a malformed mask
+// can never make the kernels read tree slots the request does not own.
+__device__ __forceinline__ uint4 clip_mask(uint4 m, int n) {
+  uint32_t *w = &m.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int lo = 32 * i;
+    if (n <= lo) w[i] = 0;
+    else if (n < lo + 32) w[i] &= (1u << (n - lo)) - 1u;
+  }
+  return m;
+}
+
+// Byte offset of 16-byte chunk `c16` (0..7) of row `row` inside one SW128
+// box of 128-byte rows (the layout a 128B-swizzled TMA load writes when the
+// box starts on a 1024-byte boundary).
+__device__ __forceinline__ uint32_t sw128_offset(int row, int c16) {
+  return static_cast<uint32_t>(row * 128 + ((c16 ^ (row & 7)) << 4));
+}
+
+}  // namespace spec

@@ -1,0 +1,197 @@
+// Device helpers shared by the library's kernels: status reporting, bounded
+// mbarrier waits, TMA tile loads, cluster/DSMEM access and the counter-based
+// generator.  sm_103a only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spec_tree.h"
+
+namespace spec {
+
+// Iterations of a bounded wait before it gives up and reports
+// SPEC_ERR_TIMEOUT.  With the back-off below this is several seconds, far
+// beyond any legitimate wait in these kernels.
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+// First error for a request sticks; kernels never write SPEC_OK.
+__device__ __forceinline__ void report(int32_t *status, int b, int code) {
+  if (status != nullptr && b >= 0) atomicCAS(status + b, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if (it > 32) __nanosleep(64);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+// 4-D tiled bulk-tensor load into this CTA's shared memory, completion
+// signalled on `bar` as transaction bytes.  Coordinates are in elements,
+// innermost first.
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_t *bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// Full cluster barrier with release/acquire semantics on shared memory:
+// every thread of every CTA in the cluster must execute it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Address of the same shared-memory object in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void *local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_peer_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- Philox
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11, "Parallel Random Numbers:
+// As Easy as 1, 2, 3").  Each round multiplies counter words 0 and 2 by the
+// round multipliers, feeds the 128-bit products' halves back with the other
+// two words and the round key, and the key advances by the golden-ratio and
+// sqrt(3)-derived Weyl increments.
+struct U64x4 {
+  uint64_t w[4];
+};
+
+__device__ __forceinline__ U64x4 philox4x64_10(U64x4 x, uint64_t k0, uint64_t k1) {
+  constexpr uint64_t kMul0 = 0xD2E7470EE14C6C93ull;
+  constexpr uint64_t kMul1 = 0xCA5A826395121157ull;
+  constexpr uint64_t kInc0 = 0x9E3779B97F4A7C15ull;
+  constexpr uint64_t kInc1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t p0_hi = __umul64hi(kMul0, x.w[0]);
+    const uint64_t p0_lo = kMul0 * x.w[0];
+    const uint64_t p1_hi = __umul64hi(kMul1, x.w[2]);
+    const uint64_t p1_lo = kMul1 * x.w[2];
+    U64x4 y;
+    y.w[0] = p1_hi ^ x.w[1] ^ k0;
+    y.w[1] = p1_lo;
+    y.w[2] = p0_hi ^ x.w[3] ^ k1;
+    y.w[3] = p0_lo;
+    x = y;
+    k0 += kInc0;
+    k1 += kInc1;
+  }
+  return x;
+}
+
+// The method's uniform for (seed, request-local node, request, kind), in
+// [0, 1): the top 24 bits of the first output word, exact in fp32.
+__device__ __forceinline__ float spec_uniform(uint64_t seed, int node, int request, int kind) {
+  U64x4 c;
+  c.w[0] = static_cast<uint64_t>(node);
+  c.w[1] = static_cast<uint64_t>(request);
+  c.w[2] = static_cast<uint64_t>(kind);
+  c.w[3] = 0;
+  const U64x4 r = philox4x64_10(c, seed, 0);
+  return static_cast<float>(r.w[0] >> 40) * (1.0f / 16777216.0f);
+}
+
+// Request that owns global node t: the b with off[b] <= t < off[b+1], by
+// binary search over monotone offsets.  Returns -1 when none does.
+__device__ __forceinline__ int find_request(const int32_t *off, int B, int t) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(off + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  if (__ldg(off + lo) <= t && t < __ldg(off + lo + 1)) return lo;
+  return -1;
+}
+
+}  // namespace spec
