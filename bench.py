@@ -229,15 +229,29 @@ def run_native(args, rank, world, local_rank):
             st.run(i)
     torch.cuda.synchronize()
 
+    if args.eager:
+        # profiler mode: plain stream launches, no graphs, no timing claims
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                st.run(i)
+        torch.cuda.synchronize()
+        status = st.status.cpu().numpy()
+        return {"eager": True, "steps": K, "status": status.tolist(),
+                "accept_len": st.outs["accept_len"].cpu().tolist()}
+
     # capture: a warm-up graph of W steps and the timed graph(s) of K steps
     chunk = min(K, args.graph_steps)
-    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)] for _ in range(chunk)]
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+               for _ in range(chunk)]
+    except TypeError:
+        evs = None
 
     def capture(n, with_events):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                st.run(i, ev=evs[i] if with_events else None)
+                st.run(i, ev=evs[i] if (with_events and evs is not None) else None)
         return g
 
     g_warm = capture(max(1, Wm), False)
@@ -282,9 +296,14 @@ def run_native(args, rank, world, local_rank):
         raise RuntimeError(f"device status {status.tolist()}")
 
     # per-kernel durations from the events of the last timed replay of g_main
-    d_mask = np.array([e[0].elapsed_time(e[1]) for e in evs[:chunk]])
-    d_attn = np.array([e[2].elapsed_time(e[3]) for e in evs[:chunk]])
-    d_ver = np.array([e[4].elapsed_time(e[5]) for e in evs[:chunk]])
+    if evs is not None:
+        d_mask = np.array([e[0].elapsed_time(e[1]) for e in evs[:chunk]])
+        d_attn = np.array([e[2].elapsed_time(e[3]) for e in evs[:chunk]])
+        d_ver = np.array([e[4].elapsed_time(e[5]) for e in evs[:chunk]])
+        kernel_timing = "event pairs around each kernel inside the timed graph (last replay)"
+    else:
+        d_mask, d_attn, d_ver = per_kernel_graph_times(st, stream, chunk)
+        kernel_timing = "separate graphs of one kernel kind each (torch lacks graph-recorded events)"
 
     if world > 1:
         t = torch.tensor([elapsed_ms], device="cuda")
@@ -320,6 +339,7 @@ def run_native(args, rank, world, local_rank):
             "step_gbs": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9,
             "step_frac": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9 / peak,
         },
+        "kernel_timing": kernel_timing,
         "gpu_launches": 3 * K,
         "clocks": clocks, "clock_window": "timed region + 1 s soak of the same graph" if soak else "timed region",
     }
@@ -328,6 +348,35 @@ def run_native(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w)
     return result
+
+
+def per_kernel_graph_times(st, stream, n):
+    """Mean duration of each kernel kind from a graph of n launches of it."""
+    import torch
+    ttv, w = st.ttv, st.w
+    out = []
+    for kind in range(3):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                c = st.copies[i % len(st.copies)]
+                if kind == 0:
+                    ttv.build_tree_mask(st.par, st.off, st.status, mask=st.mask, depth=st.depth)
+                elif kind == 1:
+                    ttv.tree_attn(c["q"], c["k"], c["v"], st.pl, st.off, st.mask, st.max_prefix,
+                                  st.status, o=st.o)
+                else:
+                    ttv.tree_verify(c["tl"], c["dl"], st.tok, st.par, st.off, w.temperature,
+                                    i, st.W, st.status, st.ws, outputs=st.outs)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(np.full(n, e0.elapsed_time(e1) / n))
+    return out
 
 
 def run_e2e(st, w, stream, steps):
@@ -451,6 +500,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="plain stream launches without graphs or timing (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3

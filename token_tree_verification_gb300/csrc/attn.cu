@@ -76,6 +76,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// x, y -> bf16x2 high parts and bf16x2 remainders (x - hi, y - hi).
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = pack_bf16(x - hf.x, y - hf.y);
+}
+
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaWarps) : "memory");
 }
@@ -267,22 +275,27 @@ tree_attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
         o[nb][2] *= alpha[1];
         o[nb][3] *= alpha[1];
       }
-      // O += P V   (P re-used from the S accumulators as bf16 A fragments)
+      // O += P V.  P is re-used from the S accumulators as A fragments, split
+      // into a bf16 high part and a bf16 remainder so the weights keep ~16
+      // significant bits: with few visible keys a single bf16 rounding of P
+      // would dominate the error of small outputs.
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-        pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-        pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+        uint32_t ph[4], pl[4];
+        split_bf16(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+        split_bf16(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+        split_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+        split_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
         const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
         for (int np = 0; np < D / 16; ++np) {
           const int dch = np * 2 + (lane >> 4);
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vaddr + (dch >> 3) * C::kBoxBytes + sw128_offset(key, dch & 7), r0, r1, r2, r3);
-          mma_16816(o[2 * np], pa, r0, r1);
-          mma_16816(o[2 * np + 1], pa, r2, r3);
+          mma_16816(o[2 * np], ph, r0, r1);
+          mma_16816(o[2 * np + 1], ph, r2, r3);
+          mma_16816(o[2 * np], pl, r0, r1);
+          mma_16816(o[2 * np + 1], pl, r2, r3);
         }
       }
       __syncwarp();
