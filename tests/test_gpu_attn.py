@@ -11,6 +11,17 @@ from token_tree_verification_gb300 import synthetic
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["tcgen05", "mma"])
+def kernel(request, monkeypatch):
+    """Both bf16 implementations: the tcgen05 kernel (default) and the
+    mma.sync kernel (selected through SPEC_TREE_ATTN_KERNEL=mma)."""
+    if request.param == "mma":
+        monkeypatch.setenv("SPEC_TREE_ATTN_KERNEL", "mma")
+    else:
+        monkeypatch.delenv("SPEC_TREE_ATTN_KERNEL", raising=False)
+    return request.param
+
+
 def full_oracle(w):
     return oracle.tree_attn(w.q.float().numpy(), w.k_cache.float().numpy(), w.v_cache.float().numpy(),
                             w.prefix_lens, w.offsets, w.parents)
@@ -33,7 +44,7 @@ def test_tiny_fp32(gpu_lib):
     (128, 4, 2, 300, 128, 1),    # largest tree
     (64, 2, 1, 1000, 17, 2),     # many tiles, many splits
 ])
-def test_bf16_shapes(gpu_lib, D, Hq, Hkv, L, N, B):
+def test_bf16_shapes(gpu_lib, kernel, D, Hq, Hkv, L, N, B):
     w = synthetic.make_workload("llama70b_gqa", seed=D + Hq + L + N, B=B, Hq=Hq, Hkv=Hkv, D=D, L=L,
                                 N=N, depth=min(5, N - 1), width=8 if N > 40 else 4, V=64)
     got, st = gpu_attn(w)
@@ -48,7 +59,7 @@ def test_fp32_ragged(gpu_lib):
     assert_attn_close(got, full_oracle(w), "fp32 ragged")
 
 
-def test_llama7b_full(gpu_lib):
+def test_llama7b_full(gpu_lib, kernel):
     w = synthetic.make_workload("llama7b", seed=0, device="cuda")
     got, st = gpu_attn(w)
     assert (st == 0).all()
@@ -58,7 +69,7 @@ def test_llama7b_full(gpu_lib):
 
 
 @pytest.mark.parametrize("name", ["dynamic", "llama70b_gqa", "long_chain", "long_tree"])
-def test_large_configs_sampled(gpu_lib, name):
+def test_large_configs_sampled(gpu_lib, kernel, name):
     w = synthetic.make_workload(name, seed=0, device="cuda")
     got, st = gpu_attn(w)
     assert (st == 0).all()
@@ -72,12 +83,33 @@ def test_large_configs_sampled(gpu_lib, name):
     assert_attn_close(got.reshape(-1, w.D)[rows], ref, name)
 
 
-def test_nan_padding_never_leaks(gpu_lib):
+def test_nan_padding_never_leaks(gpu_lib, kernel):
     w = synthetic.make_workload("llama7b", seed=3, L=100, N=10, width=3, depth=2, Hq=4, Hkv=4, V=64,
                                 S_cap=256, pad=float("nan"))
     got, st = gpu_attn(w)
     assert np.isfinite(got).all()
     assert_attn_close(got, full_oracle(w), "nan padding")
+
+
+def test_rescale_path(gpu_lib, kernel):
+    """Scores whose running max grows by far more than 2^8 across tiles (the
+    tcgen05 kernel then rescales the stored O), with an explicit scale."""
+    w = synthetic.make_workload("llama7b", seed=6, L=700, N=24, width=4, depth=3, Hq=4, Hkv=2, V=64)
+    ramp = torch.linspace(0.2, 3.0, w.S_cap).view(1, 1, -1, 1)
+    w.k_cache = (w.k_cache.float() * ramp).to(torch.bfloat16)
+    w.q = (w.q.float() * 4.0).to(torch.bfloat16)
+    import token_tree_verification_gb300 as ttv
+    from parity import dev
+    status = torch.zeros(w.B, dtype=torch.int32, device="cuda")
+    mask, _ = ttv.build_tree_mask(dev(w.parents, torch.int32), dev(w.offsets, torch.int32), status)
+    o = ttv.tree_attn(w.q.cuda(), w.k_cache.cuda(), w.v_cache.cuda(), dev(w.prefix_lens, torch.int32),
+                      dev(w.offsets, torch.int32), mask, int(w.prefix_lens.max()), status,
+                      softmax_scale=0.5)
+    torch.cuda.synchronize()
+    assert (status.cpu().numpy() == 0).all()
+    ref = oracle.tree_attn(w.q.float().numpy(), w.k_cache.float().numpy(), w.v_cache.float().numpy(),
+                           w.prefix_lens, w.offsets, w.parents, scale=0.5)
+    assert_attn_close(o.float().cpu().numpy(), ref, "rescale")
 
 
 def test_device_errors(gpu_lib):

@@ -25,6 +25,8 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "attn_common.cuh"
@@ -489,6 +491,29 @@ bool encode_kv_map(CUtensorMap *m, const void *base, int B, int Hkv, int S_cap, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over q [T][Hq][D] bf16 whose box is one 128-row query block of a
+// KV head: 64 dims x G heads x (128 / G) nodes, loaded with 128-byte swizzle
+// so the block lands as 128 rows of 128 bytes (node-major, head-minor).
+bool encode_q_map(CUtensorMap *m, const void *base, int T, int Hq, int G, int D) {
+  EncodeFn enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Which bf16 kernel runs: tcgen05 by default; SPEC_TREE_ATTN_KERNEL=mma
+// selects the mma.sync kernel (kept as a second implementation for testing).
+bool use_mma_kernel() {
+  const char *e = getenv("SPEC_TREE_ATTN_KERNEL");
+  return e != nullptr && strcmp(e, "mma") == 0;
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -598,5 +623,12 @@ extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_
     spec::tree_attn_f32_kernel<<<dim3(Hq, T), spec::kF32Threads, 0, st>>>(args);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
-  return D == 128 ? launch_mma<128>(args, max_prefix, T, st) : launch_mma<64>(args, max_prefix, T, st);
+  if (use_mma_kernel())
+    return D == 128 ? launch_mma<128>(args, max_prefix, T, st) : launch_mma<64>(args, max_prefix, T, st);
+  CUtensorMap tmq, tmk, tmv;
+  if (!encode_q_map(&tmq, q, T, Hq, G, D) || !encode_kv_map(&tmk, k_cache, B, Hkv, S_cap, D) ||
+      !encode_kv_map(&tmv, v_cache, B, Hkv, S_cap, D))
+    return SPEC_ERR_CUDA;
+  return D == 128 ? spec::launch_attn_tc<128>(args, max_prefix, T, tmq, tmk, tmv, sm_count(), st)
+                  : spec::launch_attn_tc<64>(args, max_prefix, T, tmq, tmk, tmv, sm_count(), st);
 }

@@ -3,6 +3,8 @@
 // produced by TMA tile loads.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace spec {
@@ -71,5 +73,10 @@ __device__ __forceinline__ uint4 clip_mask(uint4 m, int n) {
 __device__ __forceinline__ uint32_t sw128_offset(int row, int c16) {
   return static_cast<uint32_t>(row * 128 + ((c16 ^ (row & 7)) << 4));
 }
+
+// tcgen05 path (attn_tc.cu).
+template <int D>
+int launch_attn_tc(const AttnArgs &args, int max_prefix, int T, const CUtensorMap &tmq,
+                   const CUtensorMap &tmk, const CUtensorMap &tmv, int num_sms, cudaStream_t stream);
 
 }  // namespace spec

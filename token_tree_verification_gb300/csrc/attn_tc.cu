@@ -1,0 +1,467 @@
+// Steps A2 and A3 on the 5th-generation tensor cores (tcgen05), bf16 in,
+// fp32 accumulate.
+//
+// SpecInfer developer article §2.1, tree_attention snippet (masked scores,
+// softmax, times V); SpecInfer news write-up "Token 樹驗證器" (tree K/V
+// appended to the cache depth-first, mask restricted to the node's ancestors).
+//
+// One CTA = one key split x one block of 128 query rows x one (request, KV
+// head).  Rows are (node, head-in-group) pairs, so one K/V tile feeds all G
+// query heads of the KV head.  Warp roles:
+//   warp 0      TMA producer: the Q block once, then 64-key K and V tiles
+//               (128-byte swizzle) into a 3-stage ring.
+//   warp 1      allocates TMEM; one thread issues the MMAs:
+//                 S_i = Q K_i^T            M=128, N=64, K=D   (TMEM S[i%2])
+//                 O  += P_i V_i (hi, lo)   M=128, N=D,  K=64  (TMEM O)
+//               with S_{i+1} issued before P_i is ready, so the softmax of
+//               one tile overlaps the QK^T of the next.
+//   warps 2-5   one thread per TMEM lane (= query row): read S from TMEM,
+//               scale, mask with the node's ancestor bits, online softmax
+//               with a lazily moved reference max (the stored O is rescaled
+//               only when a row's max grows by more than 2^8), write P as
+//               bf16 high and remainder parts to shared memory.
+//   epilogue    the O rows leave TMEM; the splits of one cluster merge their
+//               (m, l, O) through distributed shared memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "attn_common.cuh"
+#include "tcgen05.cuh"
+
+namespace spec {
+
+constexpr int kTcRows = 128;
+constexpr int kTcStages = 3;
+constexpr int kTcThreads = 192;
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D>
+struct TcCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kQBoxBytes = kTcRows * 128;
+  static constexpr int kQBytes = kTcRows * D * 2;
+  static constexpr int kKVBoxBytes = kKeyTile * 128;
+  static constexpr int kTileBytes = kKeyTile * D * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kPBytes = kTcRows * kKeyTile * 2;   // one of the hi / lo parts
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kQBytes;
+  static constexpr int kOffP = kOffKV + kTcStages * kStageBytes;
+  static constexpr int kSmem = kOffP + 2 * 2 * kPBytes + 1024;
+  static constexpr int kMergeStride = D + 8;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 128;
+  static_assert(kTcRows * kMergeStride * 4 <= kTcStages * kStageBytes + 2 * 2 * kPBytes,
+                "merge buffer must fit in the K/V ring and P buffers");
+};
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
+                    const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kTcStages], bar_empty[kTcStages];
+  __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p[2], bar_o[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ float s_m[kTcRows], s_l[kTcRows];
+  __shared__ int s_timeout;
+
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_addr(smem);
+  const int CS = static_cast<int>(cluster_size());
+  const int split = static_cast<int>(cluster_rank());
+  const int rb = blockIdx.y;
+  const int b = blockIdx.z / a.Hkv;
+  const int g = blockIdx.z % a.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const ReqGeom R = request_geometry(a, b);
+  const int rows_total = R.n * a.G;
+  const int row0 = rb * kTcRows;
+  if (R.err) {
+    if (tid == 0 && split == 0 && rb == 0 && g == 0) report(a.status, b, R.err);
+    return;  // uniform across the cluster
+  }
+  if (row0 >= rows_total) return;  // uniform across the cluster
+  const int rows_here = min(kTcRows, rows_total - row0);
+  const int tiles_total = (R.keys + kKeyTile - 1) / kKeyTile;
+  const int per = (tiles_total + CS - 1) / CS;
+  const int t0 = split * per;
+  const int ntiles = max(0, min(t0 + per, tiles_total) - t0);
+
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_q, 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&bar_s[j], 1);
+      mbar_init(&bar_p[j], 4);
+      mbar_init(&bar_o[j], 1);
+    }
+    fence_barrier_init();
+    s_timeout = 0;
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&s_tmem, C::kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_arrive_expect_tx(&bar_q, C::kQBytes);
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx)
+        tma_load_3d(smem + C::kOffQ + bx * C::kQBoxBytes, &tmq, &bar_q, bx * 64, g * a.G,
+                    R.lo + row0 / a.G);
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kTcStages;
+        if (i >= kTcStages && !mbar_wait(&bar_empty[st], ((i / kTcStages) - 1) & 1)) {
+          s_timeout = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar_full[st], C::kStageBytes);
+        const int key0 = (t0 + i) * kKeyTile;
+        uint8_t *kdst = smem + C::kOffKV + st * C::kStageBytes;
+        uint8_t *vdst = kdst + C::kTileBytes;
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_4d(kdst + bx * C::kKVBoxBytes, &tmk, &bar_full[st], bx * 64, key0, g, b);
+          tma_load_4d(vdst + bx * C::kKVBoxBytes, &tmv, &bar_full[st], bx * 64, key0, g, b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kKeyTile, 0, 0);
+      constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
+      bool ok = mbar_wait(&bar_q, 0);
+      tc::fence_after_sync();
+      for (int i = 0; ok && i <= ntiles; ++i) {
+        if (i < ntiles) {
+          const int st = i % kTcStages;
+          if (!mbar_wait(&bar_full[st], (i / kTcStages) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t kb = sb + C::kOffKV + st * C::kStageBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t ad = tc::smem_desc_sw128(
+                sb + C::kOffQ + (ks >> 2) * C::kQBoxBytes + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                tc::smem_desc_sw128(kb + (ks >> 2) * C::kKVBoxBytes + (ks & 3) * 32, 16, 1024);
+            tc::mma_bf16(tmem + C::kColS + (i & 1) * kKeyTile, ad, bd, idS, ks > 0);
+          }
+          tc::commit(&bar_s[i & 1]);
+        }
+        if (i >= 1) {
+          const int j = i - 1, st = j % kTcStages;
+          if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
+          const uint32_t pb = sb + C::kOffP + (j & 1) * 2 * C::kPBytes;
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < kKeyTile / 16; ++kk) {
+              const uint64_t ad = tc::smem_desc_sw128(pb + part * C::kPBytes + kk * 32, 16, 1024);
+              const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
+              tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | part | kk) != 0);
+            }
+          }
+          tc::commit(&bar_o[j & 1]);
+          tc::commit(&bar_empty[st]);
+        }
+      }
+      if (!ok) s_timeout = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const bool row_ok = r < rows_here;
+    const bool warp_active = quad * 32 < rows_here;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    uint4 msk = make_uint4(0, 0, 0, 0);
+    if (row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + r) / a.G), R.n);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      if (!mbar_wait(&bar_s[i & 1], (i >> 1) & 1)) { ok = false; }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc::fence_after_sync();
+      const int key0 = (t0 + i) * kKeyTile;
+      const int st = i % kTcStages;
+      if (key0 + kKeyTile > R.keys) {
+        // V rows past the request's last key may hold anything: zero them so
+        // their zero weights contribute exact zeros.
+        const int valid = R.keys - key0;
+        const int chunks = (kKeyTile - valid) * C::kBoxes * 8;
+        uint8_t *vrow = smem + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
+        for (int c = tid - 64; c < chunks; c += 128) {
+          const int row = valid + c / (C::kBoxes * 8);
+          const int rest = c % (C::kBoxes * 8);
+          *reinterpret_cast<uint4 *>(vrow + (rest >> 3) * C::kKVBoxBytes + row * 128 +
+                                     (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      float s[kKeyTile];
+      if (warp_active) {
+        float (&s0)[32] = *reinterpret_cast<float(*)[32]>(&s[0]);
+        float (&s1)[32] = *reinterpret_cast<float(*)[32]>(&s[32]);
+        tc::ld32(trow + C::kColS + (i & 1) * kKeyTile, s0);
+        tc::ld32(trow + C::kColS + (i & 1) * kKeyTile + 32, s1);
+        tc::wait_ld();
+        const bool need_mask = key0 + kKeyTile > R.L;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kKeyTile; ++j) {
+          float v = s[j] * a.scale_log2;
+          if (need_mask && !key_visible(key0 + j, R.L, R.keys, msk)) v = -INFINITY;
+          s[j] = v;
+          mt = fmaxf(mt, v);
+        }
+        const bool resc = row_ok && (mt > m_used + kRescaleLog2);
+        if (__any_sync(0xffffffffu, resc)) {
+          const float m_new = resc ? mt : m_used;
+          const float alpha = (!resc || m_used == -INFINITY) ? (resc ? 0.f : 1.f)
+                                                              : exp2f(m_used - m_new);
+          if (i > 0) {
+            // O holds the products of tiles < i: wait for the last of them,
+            // then rescale this warp's rows in place.
+            if (!mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1)) { ok = false; }
+            __syncwarp();
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tc::ld32(trow + C::kColO + c * 32, o);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tc::st32(trow + C::kColO + c * 32, o);
+            }
+            tc::wait_st();
+          }
+          l *= alpha;
+          m_used = m_new;
+        }
+        // the P buffer of this parity is free once the PV of tile i-2 is done
+        if (i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        uint8_t *prow = smem + C::kOffP + (i & 1) * 2 * C::kPBytes + r * 128;
+        float psum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = exp2f(s[c * 8 + 2 * e] - base);
+            const float p1 = exp2f(s[c * 8 + 2 * e + 1] - base);
+            psum += p0 + p1;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+            const float2 hf = __bfloat1622float2(h);
+            hi[e] = bf16x2_bits(h);
+            lo[e] = bf16x2_bits(__floats2bfloat162_rn(p0 - hf.x, p1 - hf.y));
+          }
+          const int off = (c ^ (r & 7)) << 4;
+          *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4 *>(prow + C::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        l += psum;
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[i & 1]);
+    }
+    if (!ok) s_timeout = 1;
+    // ---- epilogue: O rows out of TMEM.  Every softmax warp waits for the
+    //      last P V: the merge buffer below reuses the K/V ring.
+    if (ntiles > 0) {
+      if (!mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) s_timeout = 1;
+      __syncwarp();
+      tc::fence_after_sync();
+    }
+    s_m[r] = m_used;
+    s_l[r] = l;
+    if (CS == 1) {
+      if (warp_active && ntiles > 0) {
+        const float inv = 1.f / l;
+        __nv_bfloat16 *dst = nullptr;
+        if (row_ok) {
+          const int rr = row0 + r;
+          dst = static_cast<__nv_bfloat16 *>(a.o) +
+                (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D;
+        }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tc::ld32(trow + C::kColO + c * 32, o);
+          tc::wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+              uint4 pk;
+              pk.x = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 0] * inv, o[q8 * 8 + 1] * inv));
+              pk.y = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 2] * inv, o[q8 * 8 + 3] * inv));
+              pk.z = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 4] * inv, o[q8 * 8 + 5] * inv));
+              pk.w = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 6] * inv, o[q8 * 8 + 7] * inv));
+              *reinterpret_cast<uint4 *>(dst + c * 32 + q8 * 8) = pk;
+            }
+          }
+        }
+      }
+    } else {
+      float *obuf = reinterpret_cast<float *>(smem + C::kOffKV) + r * C::kMergeStride;
+      if (warp_active && ntiles > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tc::ld32(trow + C::kColO + c * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(obuf + c * 32 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        }
+      } else {
+        for (int e = 0; e < D; e += 4) *reinterpret_cast<float4 *>(obuf + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+
+  __syncwarp();
+  tc::fence_before_sync();
+  if (CS > 1) {
+    // ---- split merge through distributed shared memory
+    cluster_sync_all();
+    const int rpr = (rows_here + CS - 1) / CS;
+    const int r_begin = split * rpr, r_end = min(rows_here, r_begin + rpr);
+    const int nvec = max(0, r_end - r_begin) * (D / 4);
+    const float *obase = reinterpret_cast<const float *>(smem + C::kOffKV);
+    for (int idx = tid; idx < nvec; idx += kTcThreads) {
+      const int lr = r_begin + idx / (D / 4);
+      const int c4 = idx % (D / 4);
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < CS; ++s2) M = fmaxf(M, ld_peer_f32(peer_addr(&s_m[lr], s2)));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float L = 0.f;
+      for (int s2 = 0; s2 < CS; ++s2) {
+        const float ms = ld_peer_f32(peer_addr(&s_m[lr], s2));
+        if (ms == -INFINITY) continue;
+        const float w = exp2f(ms - M);
+        L += w * ld_peer_f32(peer_addr(&s_l[lr], s2));
+        const float4 v = ld_peer_f32x4(peer_addr(obase + lr * C::kMergeStride + c4 * 4, s2));
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+      const float inv = 1.f / L;
+      const int rr = row0 + lr;
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
+                           (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + c4 * 4;
+      uint2 pk;
+      pk.x = bf16x2_bits(__floats2bfloat162_rn(acc.x * inv, acc.y * inv));
+      pk.y = bf16x2_bits(__floats2bfloat162_rn(acc.z * inv, acc.w * inv));
+      *reinterpret_cast<uint2 *>(dst) = pk;
+    }
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
+  tc::fence_after_sync();
+  if (s_timeout && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template __global__ void tree_attn_tc_kernel<64>(const AttnArgs, const __grid_constant__ CUtensorMap,
+                                                 const __grid_constant__ CUtensorMap,
+                                                 const __grid_constant__ CUtensorMap);
+template __global__ void tree_attn_tc_kernel<128>(const AttnArgs, const __grid_constant__ CUtensorMap,
+                                                  const __grid_constant__ CUtensorMap,
+                                                  const __grid_constant__ CUtensorMap);
+
+// Host launcher (declared in attn_common.cuh).
+template <int D>
+int launch_attn_tc(const AttnArgs &args, int max_prefix, int T, const CUtensorMap &tmq,
+                   const CUtensorMap &tmk, const CUtensorMap &tmv, int num_sms, cudaStream_t stream) {
+  using C = TcCfg<D>;
+  auto kernel = tree_attn_tc_kernel<D>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+        cudaSuccess)
+      return SPEC_ERR_CUDA;
+    configured = true;
+  }
+  const int max_nodes = T < SPEC_MAX_TREE_NODES ? T : SPEC_MAX_TREE_NODES;
+  const int rowblocks = (max_nodes * args.G + kTcRows - 1) / kTcRows;
+  const long long max_keys = static_cast<long long>(max_prefix) + max_nodes;
+  const long long tiles_max = (max_keys + kKeyTile - 1) / kKeyTile;
+  const long long units = static_cast<long long>(rowblocks) * args.B * args.Hkv;
+  if (units > 65535) return SPEC_ERR_SHAPE;
+  // Pick the split count that minimises (waves x tiles per CTA), one CTA/SM.
+  int cs = 1;
+  long long best = -1;
+  for (int c = 1; c <= 8; c *= 2) {
+    if (c > 1 && tiles_max < 2 * c) break;
+    const long long waves = (units * c + num_sms - 1) / num_sms;
+    const long long cost = waves * ((tiles_max + c - 1) / c) + (c > 1 ? 1 : 0);
+    if (best < 0 || cost < best) {
+      best = cost;
+      cs = c;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, rowblocks, static_cast<unsigned>(args.B * args.Hkv));
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args, tmq, tmk, tmv) == cudaSuccess ? SPEC_OK
+                                                                             : SPEC_ERR_CUDA;
+}
+
+template int launch_attn_tc<64>(const AttnArgs &, int, int, const CUtensorMap &, const CUtensorMap &,
+                                const CUtensorMap &, int, cudaStream_t);
+template int launch_attn_tc<128>(const AttnArgs &, int, int, const CUtensorMap &, const CUtensorMap &,
+                                 const CUtensorMap &, int, cudaStream_t);
+
+}  // namespace spec

@@ -103,6 +103,7 @@ __device__ __forceinline__ uint32_t cluster_size() {
 // Full cluster barrier with release/acquire semantics on shared memory:
 // every thread of every CTA in the cluster must execute it.
 __device__ __forceinline__ void cluster_sync_all() {
+  __syncwarp();
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::

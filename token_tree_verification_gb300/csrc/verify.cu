@@ -86,46 +86,8 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
-// Block-wide reductions through a small shared scratch; every thread gets the
-// result.  Warp partials are combined in warp order (deterministic).
-__device__ float block_sum(float x, float *scratch) {
-  x = warp_sum(x);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) scratch[w] = x;
-  __syncthreads();
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < kVWarps; ++i) s += scratch[i];
-  return s;
-}
 
-__device__ float block_max(float x, float *scratch) {
-  x = warp_max(x);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) scratch[w] = x;
-  __syncthreads();
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kVWarps; ++i) m = fmaxf(m, scratch[i]);
-  return m;
-}
 
-__device__ ArgMax block_argmax(ArgMax a, float *scratch_v, int *scratch_i) {
-  a = warp_argmax(a);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) {
-    scratch_v[w] = a.v;
-    scratch_i[w] = a.i;
-  }
-  __syncthreads();
-  ArgMax r{scratch_v[0], scratch_i[0]};
-#pragma unroll
-  for (int i = 1; i < kVWarps; ++i) r = better(r, ArgMax{scratch_v[i], scratch_i[i]});
-  return r;
-}
 
 // p(x) = exp((l - M) / temp) / S with the exponent's argument carried to
 // near double precision (TwoSum for l - M, an FMA remainder for the
@@ -179,11 +141,10 @@ __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, const in
   int cur = 0, acc = 0, ties = 0;
   for (;;) {
     int next = -1;
-    uint32_t tie_bits[4], child_bits[4];
+    uint32_t tie_bits[4];
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const bool child = par[s] == cur;
-      child_bits[s] = __ballot_sync(0xffffffffu, child);
       tie_bits[s] = __ballot_sync(0xffffffffu, child && (flg[s] & kFlagTie));
       const uint32_t ok = __ballot_sync(0xffffffffu, child && (flg[s] & kFlagAccept));
       if (next < 0 && ok) next = 32 * s + __ffs(ok) - 1;
@@ -198,7 +159,6 @@ __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, const in
       }
       ties += __popc(m);
     }
-    (void)child_bits;
     if (next < 0) {
       const int fb = __ldcg(a.fallback + lo + cur);
       if (lane == 0) ot[acc] = fb & 0x7fffffff;
@@ -233,24 +193,59 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       : "memory");
 }
 
+// Per-CTA scratch for one reduction round, double buffered by round parity
+// so a round never waits for the previous round's readers.
+struct RoundScratch {
+  float w[2][kVWarps][2];
+  int wi[2][kVWarps];
+};
+
+// Sum `x` over the CTA and then over the cluster.  Returns the cluster total
+// (identical in every CTA: partials are added in rank order) and, in `parts`,
+// the per-CTA totals.  One __syncthreads and one cluster barrier.
+__device__ float cluster_round_sum(float x, RoundScratch &rs, float (&xch)[2][8], int parity, int CS,
+                                   float *parts) {
+  x = warp_sum(x);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) rs.w[parity][w][0] = x;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVWarps; ++i) t += rs.w[parity][i][0];
+    xch[parity][0] = t;
+  }
+  cluster_sync_all();
+  float tot = 0.f;
+  for (int r = 0; r < CS; ++r) {
+    const float v = ld_peer_f32(peer_addr(&xch[parity][0], r));
+    if (parts) parts[r] = v;
+    tot += v;
+  }
+  return tot;
+}
+
 __global__ void __launch_bounds__(kVThreads)
 tree_verify_kernel(const VerifyArgs a) {
   extern __shared__ __align__(128) float vsm[];  // [chunk] target side, [chunk] draft side
-  __shared__ float red_f[kVWarps];
-  __shared__ int red_i[kVWarps];
+  __shared__ RoundScratch rs;
   __shared__ __align__(16) float xch[2][8];     // cluster exchange, double buffered
   __shared__ int spar[SPEC_MAX_TREE_NODES];
   __shared__ int stok[SPEC_MAX_TREE_NODES];
   __shared__ int child_id[SPEC_MAX_TREE_NODES];
   __shared__ float childP[SPEC_MAX_TREE_NODES], childQ[SPEC_MAX_TREE_NODES];
-  __shared__ int s_meta[4];                     // n_children, error, request
-  __shared__ int s_walk;
+  __shared__ float childU[SPEC_MAX_TREE_NODES];
+  __shared__ int warp_cnt[4];
+  __shared__ int s_meta[4];                     // error, request, n_children
+  __shared__ float s_ufb;
+  __shared__ int s_walk, s_pick;
+  __shared__ float s_cb[2];
   __shared__ __align__(8) uint64_t bars[2];
 
   const int CS = static_cast<int>(cluster_size());
   const int rank = static_cast<int>(cluster_rank());
   const int t = blockIdx.x / CS;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, w_id = tid >> 5, lane = tid & 31;
   float *lrow = vsm;
   float *drow = vsm + a.chunk;
   const int v0 = rank * a.chunk;
@@ -259,6 +254,8 @@ tree_verify_kernel(const VerifyArgs a) {
   // 1-D bulk copies need 16-byte aligned rows and a length multiple of 16 B.
   const bool bulk = ((a.V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0) &&
                     (greedy || (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0);
+  const float *trow_g = a.target + static_cast<size_t>(t) * a.V;
+  const float *drow_g = greedy ? nullptr : a.draft + static_cast<size_t>(t) * a.V;
 
   // ---- V1 (start): the target row slice streams in while the tree is read
   if (tid == 0) {
@@ -266,25 +263,23 @@ tree_verify_kernel(const VerifyArgs a) {
     mbar_init(&bars[1], 1);
     fence_barrier_init();
     s_meta[0] = 0;
-    s_meta[1] = 0;
-    s_meta[2] = -1;
+    s_meta[1] = -1;
     if (bulk && len > 0) {
       mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(len) * 4u);
-      bulk_copy_g2s(lrow, a.target + static_cast<size_t>(t) * a.V + v0,
-                    static_cast<uint32_t>(len) * 4u, &bars[0]);
+      bulk_copy_g2s(lrow, trow_g + v0, static_cast<uint32_t>(len) * 4u, &bars[0]);
     }
   }
   // ---- locate the node's request (identical in every CTA of the cluster)
   if (a.B < kVThreads) {
     if (tid < a.B) {
       const int o0 = __ldg(a.offsets + tid), o1 = __ldg(a.offsets + tid + 1);
-      if (o0 <= t && t < o1) atomicMax(&s_meta[2], tid);
+      if (o0 <= t && t < o1) atomicMax(&s_meta[1], tid);
     }
   } else if (tid == 0) {
-    s_meta[2] = find_request(a.offsets, a.B, t);
+    s_meta[1] = find_request(a.offsets, a.B, t);
   }
   __syncthreads();
-  const int b = s_meta[2];
+  const int b = s_meta[1];
   int lo = 0, n = 0, err = 0;
   if (b < 0) {
     err = SPEC_ERR_TREE_TOO_LARGE;
@@ -294,50 +289,62 @@ tree_verify_kernel(const VerifyArgs a) {
     if (lo < 0 || lo + n > a.T || n < 1 || n > SPEC_MAX_TREE_NODES) err = SPEC_ERR_TREE_TOO_LARGE;
   }
   const int u = t - lo;
-  if (!err && tid < n) {
-    const int p = __ldg(a.parents + lo + tid);
-    const int x = __ldg(a.tokens + lo + tid);
-    spar[tid] = p;
-    stok[tid] = x;
-    const bool ok = (tid == 0) ? (p == -1) : (p >= 0 && p < tid);
-    if (!ok) atomicCAS(&s_meta[1], 0, SPEC_ERR_BAD_PARENT);
-  }
-  __syncthreads();
-  if (!err && tid == 0 && s_meta[1] == 0) {
-    int k = 0;
-    for (int c = u + 1; c < n; ++c) {
-      if (spar[c] == u) {
-        if (stok[c] < 0 || stok[c] >= a.V) s_meta[1] = SPEC_ERR_TOKEN_RANGE;
-        child_id[k++] = c;
-      }
+  // ---- the request's tree: parents, tokens, and u's children in index order
+  bool is_child = false;
+  uint32_t child_bal = 0;
+  if (!err && tid < SPEC_MAX_TREE_NODES) {
+    int p = -2, x = 0;
+    if (tid < n) {
+      p = __ldg(a.parents + lo + tid);
+      x = __ldg(a.tokens + lo + tid);
+      spar[tid] = p;
+      stok[tid] = x;
+      const bool ok = (tid == 0) ? (p == -1) : (p >= 0 && p < tid);
+      if (!ok) atomicCAS(&s_meta[0], 0, SPEC_ERR_BAD_PARENT);
+      is_child = (tid > u && p == u);
+      if (is_child && (x < 0 || x >= a.V)) atomicCAS(&s_meta[0], 0, SPEC_ERR_TOKEN_RANGE);
     }
-    s_meta[0] = k;
+    child_bal = __ballot_sync(0xffffffffu, is_child);
+    if (lane == 0) warp_cnt[w_id] = __popc(child_bal);
   }
   __syncthreads();
-  if (!err) err = s_meta[1];
-  const int k = err ? 0 : s_meta[0];
-  const bool need_draft = !greedy && k > 0;
+  if (!err) err = s_meta[0];
+  int k = 0;
+  if (!err) {
+    int before = 0;
+    for (int i = 0; i < SPEC_MAX_TREE_NODES / 32; ++i) {
+      if (i < w_id) before += warp_cnt[i];
+      k += warp_cnt[i];
+    }
+    if (is_child) child_id[before + __popc(child_bal & ((1u << lane) - 1u))] = tid;
+  }
+  const bool need_draft = !err && !greedy && k > 0;
   if (tid == 0 && bulk && need_draft && len > 0) {
     mbar_arrive_expect_tx(&bars[1], static_cast<uint32_t>(len) * 4u);
-    bulk_copy_g2s(drow, a.draft + static_cast<size_t>(t) * a.V + v0,
-                  static_cast<uint32_t>(len) * 4u, &bars[1]);
+    bulk_copy_g2s(drow, drow_g + v0, static_cast<uint32_t>(len) * 4u, &bars[1]);
   }
-  // children's target / draft logits at their tokens (read once, in parallel)
-  if (need_draft && tid < k) {
-    const int x = stok[child_id[tid]];
-    childP[tid] = __ldg(a.target + static_cast<size_t>(t) * a.V + x);
-    childQ[tid] = __ldg(a.draft + static_cast<size_t>(t) * a.V + x);
+  __syncthreads();  // child_id complete
+  // the draws and the children's logits at their tokens, in parallel
+  if (!err && !greedy) {
+    if (tid < k) {
+      const int c = child_id[tid];
+      const int x = stok[c];
+      childP[tid] = __ldg(trow_g + x);
+      childQ[tid] = __ldg(drow_g + x);
+      childU[tid] = spec_uniform(a.seed, c, b, 0);
+    } else if (tid == kVThreads - 1) {
+      s_ufb = spec_uniform(a.seed, u, b, 1);
+    }
   }
-  // ---- wait for the slices (a copy was issued even if the node is invalid,
-  //      so it is always waited for before the CTA can exit)
+  // ---- wait for the slices (a copy issued for a node is always waited for)
   bool timed_out = false;
   if (bulk && len > 0) {
     if (!mbar_wait(&bars[0], 0)) timed_out = true;
     if (need_draft && !mbar_wait(&bars[1], 0)) timed_out = true;
   } else if (!err) {
     for (int i = tid; i < len; i += kVThreads) {
-      lrow[i] = __ldcs(a.target + static_cast<size_t>(t) * a.V + v0 + i);
-      if (need_draft) drow[i] = __ldcs(a.draft + static_cast<size_t>(t) * a.V + v0 + i);
+      lrow[i] = __ldcs(trow_g + v0 + i);
+      if (need_draft) drow[i] = __ldcs(drow_g + v0 + i);
     }
   }
   if (timed_out && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
@@ -345,23 +352,29 @@ tree_verify_kernel(const VerifyArgs a) {
 
   if (!err) {
     int parity = 0;
-
     if (greedy) {
       // ---- argmax of the raw target logits, lowest index on ties
       ArgMax am{-INFINITY, 0x7fffffff};
       for (int i = tid; i < len; i += kVThreads) am = better(am, ArgMax{lrow[i], v0 + i});
-      am = block_argmax(am, red_f, red_i);
+      am = warp_argmax(am);
+      if (lane == 0) {
+        rs.w[0][w_id][0] = am.v;
+        rs.wi[0][w_id] = am.i;
+      }
+      __syncthreads();
       if (tid == 0) {
-        xch[parity][0] = am.v;
-        xch[parity][1] = __int_as_float(am.i);
+        ArgMax r{rs.w[0][0][0], rs.wi[0][0]};
+        for (int i = 1; i < kVWarps; ++i) r = better(r, ArgMax{rs.w[0][i][0], rs.wi[0][i]});
+        xch[0][0] = r.v;
+        xch[0][1] = __int_as_float(r.i);
       }
       cluster_sync_all();
-      ArgMax g{-INFINITY, 0x7fffffff};
-      for (int r = 0; r < CS; ++r) {
-        const uint32_t pa = peer_addr(&xch[parity][0], r);
-        g = better(g, ArgMax{ld_peer_f32(pa), __float_as_int(ld_peer_f32(pa + 4))});
-      }
       if (rank == 0 && tid == 0) {
+        ArgMax g{-INFINITY, 0x7fffffff};
+        for (int r = 0; r < CS; ++r) {
+          const uint32_t pa = peer_addr(&xch[0][0], r);
+          g = better(g, ArgMax{ld_peer_f32(pa), __float_as_int(ld_peer_f32(pa + 4))});
+        }
         a.fallback[t] = g.i;
         for (int j = 0; j < k; ++j) {
           const int c = child_id[j];
@@ -370,14 +383,13 @@ tree_verify_kernel(const VerifyArgs a) {
       }
     } else {
       const float T_ = a.temp, iT = a.inv_temp;
-      // ---- V1: local max and local sum of exp((x - m)/T), target and draft
+      // ---- V1: per-thread max and sum of exp((x - m)/T) over the thread's
+      //      elements, combined over the CTA and the cluster in one round
       float ml = -INFINITY, md = -INFINITY;
       for (int i = tid; i < len; i += kVThreads) {
         ml = fmaxf(ml, lrow[i]);
         if (need_draft) md = fmaxf(md, drow[i]);
       }
-      ml = block_max(ml, red_f);
-      if (need_draft) md = block_max(md, red_f);
       float sl = 0.f, sd = 0.f;
       for (int i = tid; i < len; i += kVThreads) {
         const float el = expf((lrow[i] - ml) * iT);
@@ -389,13 +401,33 @@ tree_verify_kernel(const VerifyArgs a) {
           sd += ed;
         }
       }
-      sl = block_sum(sl, red_f);
-      if (need_draft) sd = block_sum(sd, red_f);
+      // warp combine of (m, s) pairs
+      float wml = warp_max(ml), wmd = warp_max(md);
+      float wsl = warp_sum(sl > 0.f ? sl * expf((ml - wml) * iT) : 0.f);
+      float wsd = warp_sum(sd > 0.f ? sd * expf((md - wmd) * iT) : 0.f);
+      __shared__ float s_pair[kVWarps][4];
+      if (lane == 0) {
+        s_pair[w_id][0] = wml;
+        s_pair[w_id][1] = wsl;
+        s_pair[w_id][2] = wmd;
+        s_pair[w_id][3] = wsd;
+      }
+      __syncthreads();
       if (tid == 0) {
-        xch[parity][0] = ml;
-        xch[parity][1] = sl;
-        xch[parity][2] = md;
-        xch[parity][3] = sd;
+        float cm = -INFINITY, cmd = -INFINITY;
+        for (int i = 0; i < kVWarps; ++i) {
+          cm = fmaxf(cm, s_pair[i][0]);
+          cmd = fmaxf(cmd, s_pair[i][2]);
+        }
+        float cs = 0.f, csd = 0.f;
+        for (int i = 0; i < kVWarps; ++i) {
+          if (s_pair[i][1] > 0.f) cs += s_pair[i][1] * expf((s_pair[i][0] - cm) * iT);
+          if (s_pair[i][3] > 0.f) csd += s_pair[i][3] * expf((s_pair[i][2] - cmd) * iT);
+        }
+        xch[parity][0] = cm;
+        xch[parity][1] = cs;
+        xch[parity][2] = cmd;
+        xch[parity][3] = csd;
       }
       cluster_sync_all();
       float Ml = -INFINITY, Md = -INFINITY;
@@ -406,31 +438,31 @@ tree_verify_kernel(const VerifyArgs a) {
         Md = fmaxf(Md, part[r].z);
       }
       float Sp = 0.f, Sq = 0.f;
+      float kept[kMaxCS];
       for (int r = 0; r < CS; ++r) {
-        if (part[r].y > 0.f) Sp += part[r].y * expf((part[r].x - Ml) * iT);
+        kept[r] = part[r].y > 0.f ? part[r].y * expf((part[r].x - Ml) * iT) : 0.f;
+        Sp += kept[r];
         if (need_draft && part[r].w > 0.f) Sq += part[r].w * expf((part[r].z - Md) * iT);
       }
+      for (int r = 0; r < CS; ++r) kept[r] /= Sp;  // chunk sums of p
       parity ^= 1;
-      // p(v), q(v) for this slice
-      const float scale_l = expf((ml - Ml) * iT) / Sp;
-      const float scale_d = need_draft ? expf((md - Md) * iT) / Sq : 0.f;
+      // p(v), q(v) for this thread's elements
+      const float scale_l = ml == -INFINITY ? 0.f : expf((ml - Ml) * iT) / Sp;
+      const float scale_d = (need_draft && md != -INFINITY) ? expf((md - Md) * iT) / Sq : 0.f;
       for (int i = tid; i < len; i += kVThreads) {
         lrow[i] *= scale_l;
         if (need_draft) drow[i] *= scale_d;
       }
-      __syncthreads();
 
       // ---- V2: the children's accept tests, one reduction per rejection
       float c_prev = 0.f, W_prev = 1.f;
-      float kept[kMaxCS];
-      bool have_kept = false;
       for (int j = 0; j < k; ++j) {
         const int c = child_id[j];
         const float P = precise_prob(childP[j], Ml, T_, iT, Sp);
         const float Q = precise_prob(childQ[j], Md, T_, iT, Sq);
         const float alpha = Q > 0.f ? fminf(1.f, fmaxf(0.f, fmaf(-c_prev, Q, P)) / (W_prev * Q)) : 1.f;
         if (rank == 0 && tid == 0) {
-          const float uu = spec_uniform(a.seed, c, b, 0);
+          const float uu = childU[j];
           int f = (uu < alpha) ? kFlagAccept : 0;
           if (fabsf(uu - alpha) < kTieBand) f |= kFlagTie;
           a.flags[lo + c] = f;
@@ -438,39 +470,21 @@ tree_verify_kernel(const VerifyArgs a) {
         const float c_new = c_prev + W_prev;
         float w = 0.f;
         for (int i = tid; i < len; i += kVThreads) w += fmaxf(0.f, fmaf(-c_new, drow[i], lrow[i]));
-        w = block_sum(w, red_f);
-        if (tid == 0) xch[parity][0] = w;
-        cluster_sync_all();
-        float Wn = 0.f, chunks[kMaxCS];
-        for (int r = 0; r < CS; ++r) {
-          chunks[r] = ld_peer_f32(peer_addr(&xch[parity][0], r));
-          Wn += chunks[r];
-        }
+        float chunks[kMaxCS];
+        const float Wn = cluster_round_sum(w, rs, xch, parity, CS, chunks);
         parity ^= 1;
         if (Wn > 0.f) {  // otherwise the residual is all zero: keep r
           c_prev = c_new;
           W_prev = Wn;
           for (int r = 0; r < CS; ++r) kept[r] = chunks[r];
-          have_kept = true;
         }
       }
 
       // ---- V3: the token emitted when the walk stops here, drawn by
       //      inverse CDF from r ∝ max(0, p - c q) (c = 0: r = p)
-      if (!have_kept) {
-        float w = 0.f;
-        for (int i = tid; i < len; i += kVThreads) w += lrow[i];
-        w = block_sum(w, red_f);
-        if (tid == 0) xch[parity][0] = w;
-        cluster_sync_all();
-        for (int r = 0; r < CS; ++r) kept[r] = ld_peer_f32(peer_addr(&xch[parity][0], r));
-        parity ^= 1;
-        c_prev = 0.f;
-      }
       float total = 0.f;
       for (int r = 0; r < CS; ++r) total += kept[r];
-      const float uu = spec_uniform(a.seed, u, b, 1);
-      const float target = uu * total;
+      const float target = s_ufb * total;
       int owner = -1;
       float prefix = 0.f;
       {
@@ -490,31 +504,24 @@ tree_verify_kernel(const VerifyArgs a) {
       if (rank == owner) {
         // Warp-contiguous segments; warp partial sums, then the owning warp
         // scans its segment 32 elements at a time.
-        const int w_id = tid >> 5, lane = tid & 31;
         const int seg = (len + kVWarps - 1) / kVWarps;
         const int s0 = min(len, w_id * seg), s1 = min(len, s0 + seg);
         float ws = 0.f;
-        for (int i = s0 + lane; i < s1; i += 32) {
-          const float wv = c_prev != 0.f ? fmaxf(0.f, fmaf(-c_prev, drow[i], lrow[i])) : lrow[i];
-          ws += wv;
-        }
+        for (int i = s0 + lane; i < s1; i += 32)
+          ws += c_prev != 0.f ? fmaxf(0.f, fmaf(-c_prev, drow[i], lrow[i])) : lrow[i];
         ws = warp_sum(ws);
-        __syncthreads();
-        if (lane == 0) red_f[w_id] = ws;
+        if (lane == 0) rs.w[parity][w_id][1] = ws;
+        if (tid == 0) s_pick = -1;
         __syncthreads();
         float before = prefix;
         int pick_w = -1;
         {
           float run = prefix;
           for (int i = 0; i < kVWarps; ++i) {
-            if (run + red_f[i] > target) { pick_w = i; before = run; break; }
-            run += red_f[i];
+            if (run + rs.w[parity][i][1] > target) { pick_w = i; before = run; break; }
+            run += rs.w[parity][i][1];
           }
         }
-        __shared__ int s_pick;
-        __shared__ float s_cb[2];
-        if (tid == 0) { s_pick = -1; }
-        __syncthreads();
         if (pick_w == w_id) {
           float run = before;
           for (int base = s0; base < s1; base += 32) {
@@ -530,8 +537,7 @@ tree_verify_kernel(const VerifyArgs a) {
             const float cum = run + inc;
             const uint32_t hit = __ballot_sync(0xffffffffu, i < s1 && cum > target);
             if (hit) {
-              const int L0 = __ffs(hit) - 1;
-              if (lane == L0) {
+              if (lane == __ffs(hit) - 1) {
                 s_pick = v0 + i;
                 s_cb[0] = cum - wv;
                 s_cb[1] = cum;
@@ -558,10 +564,10 @@ tree_verify_kernel(const VerifyArgs a) {
           }
           const bool tie = fabsf(target - cb0) < kTieBand * total || fabsf(target - cb1) < kTieBand * total;
           a.fallback[t] = pick | (tie ? (1 << 31) : 0);
+          __threadfence();
         }
       }
     }
-    __threadfence();
     cluster_sync_all();  // no CTA leaves while a peer may still read its exchange slots
   } else if (rank == 0 && tid == 0 && b >= 0) {
     report(a.status, b, err);
