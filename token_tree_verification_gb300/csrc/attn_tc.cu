@@ -15,13 +15,15 @@
 //                 O  += P_i V_i (hi, lo)   M=128, N=D,  K=64  (TMEM O)
 //               with S_{i+1} issued before P_i is ready, so the softmax of
 //               one tile overlaps the QK^T of the next.
-//   warps 2-5   one thread per TMEM lane (= query row): read S from TMEM,
-//               scale, mask with the node's ancestor bits, online softmax
-//               with a lazily moved reference max (the stored O is rescaled
-//               only when a row's max grows by more than 2^8), write P as
-//               bf16 high and remainder parts to shared memory.
-//   epilogue    the O rows leave TMEM; the splits of one cluster merge their
-//               (m, l, O) through distributed shared memory.
+//   warps 2-9   two threads per TMEM lane (= query row), one per half of
+//               the tile's keys: read S from TMEM, mask with the node's
+//               ancestor bits, share the row max with the partner thread,
+//               online softmax with a lazily moved reference max (the stored
+//               O is rescaled only when a row's max grows by more than 2^8),
+//               write P as bf16 high and remainder parts to shared memory.
+//   epilogue    the O rows leave TMEM; the splits of one cluster push their
+//               (m, l, O) rows into the owning CTA's shared memory with
+//               remote stores, which then merges them locally.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -32,7 +34,8 @@ namespace spec {
 
 constexpr int kTcRows = 128;
 constexpr int kTcStages = 3;
-constexpr int kTcThreads = 192;
+constexpr int kTcSoftmaxWarps = 8;   // two warps (key halves) per TMEM lane quadrant
+constexpr int kTcThreads = 32 * (2 + kTcSoftmaxWarps);
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
@@ -48,12 +51,13 @@ struct TcCfg {
   static constexpr int kOffKV = kQBytes;
   static constexpr int kOffP = kOffKV + kTcStages * kStageBytes;
   static constexpr int kSmem = kOffP + 2 * 2 * kPBytes + 1024;
-  static constexpr int kMergeStride = D + 8;
+  static constexpr int kMergeStride = D + 4;             // floats per (split, row) slot
   static constexpr uint32_t kTmemCols = 256;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 128;
-  static_assert(kTcRows * kMergeStride * 4 <= kTcStages * kStageBytes + 2 * 2 * kPBytes,
-                "merge buffer must fit in the K/V ring and P buffers");
+  // owner-side merge slots: (split, row) pairs, at most rows + 7 of them
+  static_assert((kTcRows + 7) * kMergeStride * 4 <= kTcStages * kStageBytes,
+                "merge buffer must fit in the K/V ring");
 };
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
@@ -79,7 +83,9 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   __shared__ __align__(8) uint64_t bar_full[kTcStages], bar_empty[kTcStages];
   __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p[2], bar_o[2];
   __shared__ uint32_t s_tmem;
-  __shared__ float s_m[kTcRows], s_l[kTcRows];
+  __shared__ float x_max[2][2][kTcRows];   // [tile parity][key half][row]
+  __shared__ float x_l[2][kTcRows];
+  __shared__ float m_slot[8][kTcRows], l_slot[8][kTcRows];   // owner-side merge (split, row)
   __shared__ int s_timeout;
 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -105,6 +111,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const int per = (tiles_total + CS - 1) / CS;
   const int t0 = split * per;
   const int ntiles = max(0, min(t0 + per, tiles_total) - t0);
+  const int rpr = (rows_here + CS - 1) / CS;   // rows merged by each CTA of the cluster
 
   if (tid == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -114,7 +121,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     mbar_init(&bar_q, 1);
     for (int j = 0; j < 2; ++j) {
       mbar_init(&bar_s[j], 1);
-      mbar_init(&bar_p[j], 4);
+      mbar_init(&bar_p[j], kTcSoftmaxWarps);
       mbar_init(&bar_o[j], 1);
     }
     fence_barrier_init();
@@ -128,6 +135,16 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
+
+  // softmax-thread geometry (warps 2..9)
+  const int quad = warp & 3;
+  const int half = (warp - 2) >> 2;
+  const int r = quad * 32 + lane;
+  const bool row_ok = r < rows_here;
+  const bool warp_active = warp >= 2 && quad * 32 < rows_here;
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  float o_keep[D / 2];
+  float m_used = -INFINITY, l_half = 0.f, l_row = 0.f;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -203,19 +220,15 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;
-    const bool row_ok = r < rows_here;
-    const bool warp_active = quad * 32 < rows_here;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     uint4 msk = make_uint4(0, 0, 0, 0);
     if (row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + r) / a.G), R.n);
-    float m_used = -INFINITY, l = 0.f;
+    const float sl2 = a.scale_log2;
     bool ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      if (!mbar_wait(&bar_s[i & 1], (i >> 1) & 1)) { ok = false; }
+    // A timed-out wait clears `ok` and later waits are skipped, but the loop
+    // runs to the end so both warps of a pair meet every named barrier.
+    for (int i = 0; i < ntiles; ++i) {
+      if (ok && !mbar_wait(&bar_s[i & 1], (i >> 1) & 1)) ok = false;
       __syncwarp();
-      if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after_sync();
       const int key0 = (t0 + i) * kKeyTile;
       const int st = i % kTcStages;
@@ -225,77 +238,78 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const int valid = R.keys - key0;
         const int chunks = (kKeyTile - valid) * C::kBoxes * 8;
         uint8_t *vrow = smem + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
-        for (int c = tid - 64; c < chunks; c += 128) {
+        for (int c = tid - 64; c < chunks; c += 32 * kTcSoftmaxWarps) {
           const int row = valid + c / (C::kBoxes * 8);
           const int rest = c % (C::kBoxes * 8);
           *reinterpret_cast<uint4 *>(vrow + (rest >> 3) * C::kKVBoxBytes + row * 128 +
                                      (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      float s[kKeyTile];
       if (warp_active) {
-        float (&s0)[32] = *reinterpret_cast<float(*)[32]>(&s[0]);
-        float (&s1)[32] = *reinterpret_cast<float(*)[32]>(&s[32]);
-        tc::ld32(trow + C::kColS + (i & 1) * kKeyTile, s0);
-        tc::ld32(trow + C::kColS + (i & 1) * kKeyTile + 32, s1);
+        float s[32];
+        tc::ld32(trow + C::kColS + (i & 1) * kKeyTile + 32 * half, s);
         tc::wait_ld();
-        const bool need_mask = key0 + kKeyTile > R.L;
-        float mt = -INFINITY;
+        const int kbase = key0 + 32 * half;
+        if (kbase + 32 > R.L) {
 #pragma unroll
-        for (int j = 0; j < kKeyTile; ++j) {
-          float v = s[j] * a.scale_log2;
-          if (need_mask && !key_visible(key0 + j, R.L, R.keys, msk)) v = -INFINITY;
-          s[j] = v;
-          mt = fmaxf(mt, v);
+          for (int j = 0; j < 32; ++j)
+            if (!key_visible(kbase + j, R.L, R.keys, msk)) s[j] = -INFINITY;
         }
+        float mt = s[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) mt = fmaxf(mt, s[j]);
+        // the row max over both halves
+        x_max[i & 1][half][r] = mt;
+        named_bar_sync(2 + quad, 64);
+        mt = fmaxf(mt, x_max[i & 1][half ^ 1][r]) * sl2;
         const bool resc = row_ok && (mt > m_used + kRescaleLog2);
         if (__any_sync(0xffffffffu, resc)) {
           const float m_new = resc ? mt : m_used;
-          const float alpha = (!resc || m_used == -INFINITY) ? (resc ? 0.f : 1.f)
-                                                              : exp2f(m_used - m_new);
+          const float alpha = !resc ? 1.f : (m_used == -INFINITY ? 0.f : exp2f(m_used - m_new));
           if (i > 0) {
             // O holds the products of tiles < i: wait for the last of them,
-            // then rescale this warp's rows in place.
-            if (!mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1)) { ok = false; }
+            // then rescale this thread's half of the row in place.
+            if (ok && !mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1)) ok = false;
             __syncwarp();
             tc::fence_after_sync();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
               float o[32];
-              tc::ld32(trow + C::kColO + c * 32, o);
+              tc::ld32(trow + C::kColO + half * (D / 2) + c * 32, o);
               tc::wait_ld();
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] *= alpha;
-              tc::st32(trow + C::kColO + c * 32, o);
+              tc::st32(trow + C::kColO + half * (D / 2) + c * 32, o);
             }
             tc::wait_st();
           }
-          l *= alpha;
+          l_half *= alpha;
           m_used = m_new;
         }
-        // the P buffer of this parity is free once the PV of tile i-2 is done
-        if (i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
-        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        // the P buffer of this parity is free once the P V of tile i-2 is done
+        if (ok && i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
+        __syncwarp();
+        const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
         uint8_t *prow = smem + C::kOffP + (i & 1) * 2 * C::kPBytes + r * 128;
         float psum = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = exp2f(s[c * 8 + 2 * e] - base);
-            const float p1 = exp2f(s[c * 8 + 2 * e + 1] - base);
+            const float p0 = fast_exp2(fmaf(s[cc * 8 + 2 * e], sl2, nbase));
+            const float p1 = fast_exp2(fmaf(s[cc * 8 + 2 * e + 1], sl2, nbase));
             psum += p0 + p1;
             const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
             const float2 hf = __bfloat1622float2(h);
             hi[e] = bf16x2_bits(h);
             lo[e] = bf16x2_bits(__floats2bfloat162_rn(p0 - hf.x, p1 - hf.y));
           }
-          const int off = (c ^ (r & 7)) << 4;
+          const int off = ((4 * half + cc) ^ (r & 7)) << 4;
           *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4 *>(prow + C::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        l += psum;
+        l_half += psum;
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -304,55 +318,41 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     if (!ok) s_timeout = 1;
     // ---- epilogue: O rows out of TMEM.  Every softmax warp waits for the
-    //      last P V: the merge buffer below reuses the K/V ring.
+    //      last P V before any thread reuses the K/V ring below.
     if (ntiles > 0) {
-      if (!mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) s_timeout = 1;
+      if (ok && !mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) s_timeout = 1;
       __syncwarp();
       tc::fence_after_sync();
     }
-    s_m[r] = m_used;
-    s_l[r] = l;
-    if (CS == 1) {
-      if (warp_active && ntiles > 0) {
-        const float inv = 1.f / l;
-        __nv_bfloat16 *dst = nullptr;
-        if (row_ok) {
-          const int rr = row0 + r;
-          dst = static_cast<__nv_bfloat16 *>(a.o) +
-                (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D;
-        }
+    x_l[half][r] = l_half;
+    named_bar_sync(2 + quad, 64);
+    l_row = l_half + x_l[half ^ 1][r];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tc::ld32(trow + C::kColO + c * 32, o);
-          tc::wait_ld();
-          if (row_ok) {
+    for (int e = 0; e < D / 2; ++e) o_keep[e] = 0.f;
+    if (warp_active && ntiles > 0) {
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-              uint4 pk;
-              pk.x = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 0] * inv, o[q8 * 8 + 1] * inv));
-              pk.y = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 2] * inv, o[q8 * 8 + 3] * inv));
-              pk.z = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 4] * inv, o[q8 * 8 + 5] * inv));
-              pk.w = bf16x2_bits(__floats2bfloat162_rn(o[q8 * 8 + 6] * inv, o[q8 * 8 + 7] * inv));
-              *reinterpret_cast<uint4 *>(dst + c * 32 + q8 * 8) = pk;
-            }
-          }
-        }
+      for (int c = 0; c < D / 64; ++c) {
+        float o[32];
+        tc::ld32(trow + C::kColO + half * (D / 2) + c * 32, o);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o_keep[c * 32 + e] = o[e];
       }
-    } else {
-      float *obuf = reinterpret_cast<float *>(smem + C::kOffKV) + r * C::kMergeStride;
-      if (warp_active && ntiles > 0) {
+    }
+    if (CS == 1 && row_ok && ntiles > 0) {
+      const float inv = 1.f / l_row;
+      const int rr = row0 + r;
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
+                           (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D +
+                           half * (D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tc::ld32(trow + C::kColO + c * 32, o);
-          tc::wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4 *>(obuf + c * 32 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-        }
-      } else {
-        for (int e = 0; e < D; e += 4) *reinterpret_cast<float4 *>(obuf + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q8 = 0; q8 < D / 16; ++q8) {
+        uint4 pk;
+        pk.x = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 0] * inv, o_keep[q8 * 8 + 1] * inv));
+        pk.y = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 2] * inv, o_keep[q8 * 8 + 3] * inv));
+        pk.z = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 4] * inv, o_keep[q8 * 8 + 5] * inv));
+        pk.w = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 6] * inv, o_keep[q8 * 8 + 7] * inv));
+        *reinterpret_cast<uint4 *>(dst + q8 * 8) = pk;
       }
     }
   }
@@ -360,32 +360,45 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   __syncwarp();
   tc::fence_before_sync();
   if (CS > 1) {
-    // ---- split merge through distributed shared memory
-    cluster_sync_all();
-    const int rpr = (rows_here + CS - 1) / CS;
+    // ---- split merge: every CTA pushes its rows into the owner's smem
+    cluster_sync_all();  // every CTA of the cluster is done with its K/V ring
+    if (warp >= 2 && row_ok) {
+      const int owner = r / rpr;
+      const int slot = split * rpr + (r - owner * rpr);
+      float *mbase = reinterpret_cast<float *>(smem + C::kOffKV) + slot * C::kMergeStride + half * (D / 2);
+      const uint32_t dst = peer_addr(mbase, owner);
+#pragma unroll
+      for (int e = 0; e < D / 2; e += 4)
+        st_peer_f32x4(dst + e * 4, make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]));
+      if (half == 0) {
+        st_peer_f32(peer_addr(&m_slot[split][r - owner * rpr], owner), ntiles > 0 ? m_used : -INFINITY);
+        st_peer_f32(peer_addr(&l_slot[split][r - owner * rpr], owner), l_row);
+      }
+    }
+    cluster_sync_all();  // the pushes have landed
     const int r_begin = split * rpr, r_end = min(rows_here, r_begin + rpr);
     const int nvec = max(0, r_end - r_begin) * (D / 4);
-    const float *obase = reinterpret_cast<const float *>(smem + C::kOffKV);
+    const float *mb = reinterpret_cast<const float *>(smem + C::kOffKV);
     for (int idx = tid; idx < nvec; idx += kTcThreads) {
-      const int lr = r_begin + idx / (D / 4);
+      const int lr = idx / (D / 4);
       const int c4 = idx % (D / 4);
       float M = -INFINITY;
-      for (int s2 = 0; s2 < CS; ++s2) M = fmaxf(M, ld_peer_f32(peer_addr(&s_m[lr], s2)));
+      for (int s2 = 0; s2 < CS; ++s2) M = fmaxf(M, m_slot[s2][lr]);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       float L = 0.f;
       for (int s2 = 0; s2 < CS; ++s2) {
-        const float ms = ld_peer_f32(peer_addr(&s_m[lr], s2));
+        const float ms = m_slot[s2][lr];
         if (ms == -INFINITY) continue;
         const float w = exp2f(ms - M);
-        L += w * ld_peer_f32(peer_addr(&s_l[lr], s2));
-        const float4 v = ld_peer_f32x4(peer_addr(obase + lr * C::kMergeStride + c4 * 4, s2));
+        L += w * l_slot[s2][lr];
+        const float4 v = *reinterpret_cast<const float4 *>(mb + (s2 * rpr + lr) * C::kMergeStride + c4 * 4);
         acc.x += w * v.x;
         acc.y += w * v.y;
         acc.z += w * v.z;
         acc.w += w * v.w;
       }
       const float inv = 1.f / L;
-      const int rr = row0 + lr;
+      const int rr = row0 + r_begin + lr;
       __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
                            (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + c4 * 4;
       uint2 pk;
@@ -393,10 +406,8 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       pk.y = bf16x2_bits(__floats2bfloat162_rn(acc.z * inv, acc.w * inv));
       *reinterpret_cast<uint2 *>(dst) = pk;
     }
-    cluster_sync_all();
-  } else {
-    __syncthreads();
   }
+  __syncthreads();
   tc::fence_after_sync();
   if (s_timeout && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
   if (warp == 1) {

@@ -138,6 +138,30 @@ __device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
   return v;
 }
 
+// Remote (distributed shared memory) stores: fire-and-forget, ordered for the
+// target CTA by the next cluster barrier.
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_peer_f32x4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// Named barrier for `nthreads` threads (a multiple of 32) of this CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 2^x with the hardware approximation (max relative error about 2^-22).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- Philox
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11, "Parallel Random Numbers:
 // As Easy as 1, 2, 3").  Each round multiplies counter words 0 and 2 by the

@@ -200,25 +200,38 @@ struct RoundScratch {
   int wi[2][kVWarps];
 };
 
+// Cluster all-gather slots: every CTA pushes its partials into slot [rank]
+// of every peer with remote stores, so after one cluster barrier all values
+// are read from local shared memory.  Double buffered by round parity.
+struct Gather {
+  float v[2][kMaxCS][4];
+};
+
+__device__ __forceinline__ void gather_push(Gather &gx, int parity, int rank, int CS, float4 val) {
+  // threads 0..CS-1 each push to one peer
+  const int r = threadIdx.x;
+  if (r < CS) st_peer_f32x4(peer_addr(&gx.v[parity][rank][0], r), val);
+}
+
 // Sum `x` over the CTA and then over the cluster.  Returns the cluster total
 // (identical in every CTA: partials are added in rank order) and, in `parts`,
 // the per-CTA totals.  One __syncthreads and one cluster barrier.
-__device__ float cluster_round_sum(float x, RoundScratch &rs, float (&xch)[2][8], int parity, int CS,
-                                   float *parts) {
+__device__ float cluster_round_sum(float x, RoundScratch &rs, Gather &gx, int parity, int rank,
+                                   int CS, float *parts) {
   x = warp_sum(x);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) rs.w[parity][w][0] = x;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < CS) {
     float t = 0.f;
 #pragma unroll
     for (int i = 0; i < kVWarps; ++i) t += rs.w[parity][i][0];
-    xch[parity][0] = t;
+    gather_push(gx, parity, rank, CS, make_float4(t, 0.f, 0.f, 0.f));
   }
   cluster_sync_all();
   float tot = 0.f;
   for (int r = 0; r < CS; ++r) {
-    const float v = ld_peer_f32(peer_addr(&xch[parity][0], r));
+    const float v = gx.v[parity][r][0];
     if (parts) parts[r] = v;
     tot += v;
   }
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(kVThreads)
 tree_verify_kernel(const VerifyArgs a) {
   extern __shared__ __align__(128) float vsm[];  // [chunk] target side, [chunk] draft side
   __shared__ RoundScratch rs;
-  __shared__ __align__(16) float xch[2][8];     // cluster exchange, double buffered
+  __shared__ __align__(16) Gather gx;           // cluster all-gather, double buffered
   __shared__ int spar[SPEC_MAX_TREE_NODES];
   __shared__ int stok[SPEC_MAX_TREE_NODES];
   __shared__ int child_id[SPEC_MAX_TREE_NODES];
@@ -362,19 +375,15 @@ tree_verify_kernel(const VerifyArgs a) {
         rs.wi[0][w_id] = am.i;
       }
       __syncthreads();
-      if (tid == 0) {
+      if (tid < CS) {
         ArgMax r{rs.w[0][0][0], rs.wi[0][0]};
         for (int i = 1; i < kVWarps; ++i) r = better(r, ArgMax{rs.w[0][i][0], rs.wi[0][i]});
-        xch[0][0] = r.v;
-        xch[0][1] = __int_as_float(r.i);
+        gather_push(gx, 0, rank, CS, make_float4(r.v, __int_as_float(r.i), 0.f, 0.f));
       }
       cluster_sync_all();
       if (rank == 0 && tid == 0) {
         ArgMax g{-INFINITY, 0x7fffffff};
-        for (int r = 0; r < CS; ++r) {
-          const uint32_t pa = peer_addr(&xch[0][0], r);
-          g = better(g, ArgMax{ld_peer_f32(pa), __float_as_int(ld_peer_f32(pa + 4))});
-        }
+        for (int r = 0; r < CS; ++r) g = better(g, ArgMax{gx.v[0][r][0], __float_as_int(gx.v[0][r][1])});
         a.fallback[t] = g.i;
         for (int j = 0; j < k; ++j) {
           const int c = child_id[j];
@@ -413,7 +422,7 @@ tree_verify_kernel(const VerifyArgs a) {
         s_pair[w_id][3] = wsd;
       }
       __syncthreads();
-      if (tid == 0) {
+      if (tid < CS) {
         float cm = -INFINITY, cmd = -INFINITY;
         for (int i = 0; i < kVWarps; ++i) {
           cm = fmaxf(cm, s_pair[i][0]);
@@ -424,16 +433,13 @@ tree_verify_kernel(const VerifyArgs a) {
           if (s_pair[i][1] > 0.f) cs += s_pair[i][1] * expf((s_pair[i][0] - cm) * iT);
           if (s_pair[i][3] > 0.f) csd += s_pair[i][3] * expf((s_pair[i][2] - cmd) * iT);
         }
-        xch[parity][0] = cm;
-        xch[parity][1] = cs;
-        xch[parity][2] = cmd;
-        xch[parity][3] = csd;
+        gather_push(gx, parity, rank, CS, make_float4(cm, cs, cmd, csd));
       }
       cluster_sync_all();
       float Ml = -INFINITY, Md = -INFINITY;
       float4 part[kMaxCS];
       for (int r = 0; r < CS; ++r) {
-        part[r] = ld_peer_f32x4(peer_addr(&xch[parity][0], r));
+        part[r] = *reinterpret_cast<const float4 *>(&gx.v[parity][r][0]);
         Ml = fmaxf(Ml, part[r].x);
         Md = fmaxf(Md, part[r].z);
       }
@@ -471,7 +477,7 @@ tree_verify_kernel(const VerifyArgs a) {
         float w = 0.f;
         for (int i = tid; i < len; i += kVThreads) w += fmaxf(0.f, fmaf(-c_new, drow[i], lrow[i]));
         float chunks[kMaxCS];
-        const float Wn = cluster_round_sum(w, rs, xch, parity, CS, chunks);
+        const float Wn = cluster_round_sum(w, rs, gx, parity, rank, CS, chunks);
         parity ^= 1;
         if (Wn > 0.f) {  // otherwise the residual is all zero: keep r
           c_prev = c_new;
