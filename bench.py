@@ -258,7 +258,8 @@ def run_native(args, rank, world, local_rank):
     g_main = capture(chunk, True)
     reps, rem = divmod(K, chunk)
     g_rem = capture(rem, False) if rem else None
-    g_warm.replay()
+    with torch.cuda.stream(stream):
+        g_warm.replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -271,12 +272,14 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    t0.record(stream)
-    for _ in range(reps):
-        g_main.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    t1.record(stream)
+    # graphs replay on the current stream: make it the timed stream
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(reps):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -287,8 +290,9 @@ def run_native(args, rank, world, local_rank):
     if elapsed_ms < 1500:
         soak = True
         tend = time.time() + 1.0
-        while time.time() < tend:
-            g_main.replay()
+        with torch.cuda.stream(stream):
+            while time.time() < tend:
+                g_main.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop()
     status = st.status.cpu().numpy()
@@ -368,12 +372,14 @@ def per_kernel_graph_times(st, stream, n):
                 else:
                     ttv.tree_verify(c["tl"], c["dl"], st.tok, st.par, st.off, w.temperature,
                                     i, st.W, st.status, st.ws, outputs=st.outs)
-        g.replay()
+        with torch.cuda.stream(stream):
+            g.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
         torch.cuda.synchronize()
         out.append(np.full(n, e0.elapsed_time(e1) / n))
     return out

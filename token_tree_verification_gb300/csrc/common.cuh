@@ -10,10 +10,15 @@
 
 namespace spec {
 
-// Iterations of a bounded wait before it gives up and reports
-// SPEC_ERR_TIMEOUT.  With the back-off below this is several seconds, far
-// beyond any legitimate wait in these kernels.
-constexpr uint32_t kWaitLimit = 1u << 24;
+// A bounded wait gives up and reports SPEC_ERR_TIMEOUT after this many
+// nanoseconds (2 s), far beyond any legitimate wait in these kernels.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // First error for a request sticks; kernels never write SPEC_OK.
 __device__ __forceinline__ void report(int32_t *status, int b, int code) {
@@ -52,13 +57,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete; false if the limit ran out.
+// Wait for phase `parity` of `bar` to complete; false if the time limit ran
+// out.  try_wait itself suspends the thread in hardware for a while, so the
+// loop polls without sleeping and reads the clock only every 256 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
-    if (it > 32) __nanosleep(64);
+    if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
   }
-  return false;
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
