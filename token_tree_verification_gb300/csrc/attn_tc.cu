@@ -21,6 +21,10 @@
 //               online softmax with a lazily moved reference max (the stored
 //               O is rescaled only when a row's max grows by more than 2^8),
 //               write P as bf16 high and remainder parts to shared memory.
+//               With at most 64 rows the remainder part goes to the unused
+//               rows 64-127 of the same P operand (one 4-MMA P V pass; the
+//               two halves are added from TMEM lanes r and r + 64 at the end,
+//               and the warps of lanes 64-127 mirror their rows' rescaling).
 //   epilogue    the O rows leave TMEM; the splits of one cluster push their
 //               (m, l, O) rows into the owning CTA's shared memory with
 //               remote stores, which then merges them locally.
@@ -58,6 +62,7 @@ struct TcCfg {
   // owner-side merge slots: (split, row) pairs, at most rows + 7 of them
   static_assert((kTcRows + 7) * kMergeStride * 4 <= kTcStages * kStageBytes,
                 "merge buffer must fit in the K/V ring");
+  static_assert(kTcRows / 2 * D * 4 <= 2 * 2 * kPBytes, "packed remainder exchange fits the P buffers");
 };
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
@@ -107,6 +112,10 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   }
   if (row0 >= rows_total) return;  // uniform across the cluster
   const int rows_here = min(kTcRows, rows_total - row0);
+  // Packed mode (at most 64 rows): the bf16 remainder of P goes to rows
+  // 64-127 of the same P operand, so one 4-MMA pass computes both halves
+  // of P V into TMEM lanes r and r + 64.
+  const bool packed = rows_here <= kTcRows / 2;
   const int tiles_total = (R.keys + kKeyTile - 1) / kKeyTile;
   const int per = (tiles_total + CS - 1) / CS;
   const int t0 = split * per;
@@ -136,12 +145,17 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
 
-  // softmax-thread geometry (warps 2..9)
+  // softmax-thread geometry (warps 2..9): TMEM lane r, key / column half
   const int quad = warp & 3;
   const int half = (warp - 2) >> 2;
   const int r = quad * 32 + lane;
-  const bool row_ok = r < rows_here;
-  const bool warp_active = warp >= 2 && quad * 32 < rows_here;
+  // the score row this thread follows: its own, or (helper lanes 64-127 in
+  // packed mode) the row whose remainder part it accumulates
+  const bool helper = packed && quad >= 2;
+  const int srow = helper ? r - kTcRows / 2 : r;
+  const bool row_ok = srow < rows_here;
+  const bool computes = warp >= 2 && !helper && quad * 32 < rows_here;   // reads S, writes P
+  const bool lanes_live = warp >= 2 && (quad & (packed ? 1 : 3)) * 32 < rows_here;
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   float o_keep[D / 2];
   float m_used = -INFINITY, l_half = 0.f, l_row = 0.f;
@@ -179,6 +193,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kKeyTile, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
+      const int parts = packed ? 1 : 2;
       bool ok = mbar_wait(&bar_q, 0);
       tc::fence_after_sync();
       for (int i = 0; ok && i <= ntiles; ++i) {
@@ -203,8 +218,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           tc::fence_after_sync();
           const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
           const uint32_t pb = sb + C::kOffP + (j & 1) * 2 * C::kPBytes;
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
+          for (int part = 0; part < parts; ++part) {
 #pragma unroll
             for (int kk = 0; kk < kKeyTile / 16; ++kk) {
               const uint64_t ad = tc::smem_desc_sw128(pb + part * C::kPBytes + kk * 32, 16, 1024);
@@ -221,11 +235,11 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   } else {
     // ------------------------------------------------------------ softmax warps
     uint4 msk = make_uint4(0, 0, 0, 0);
-    if (row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + r) / a.G), R.n);
+    if (computes && row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + r) / a.G), R.n);
     const float sl2 = a.scale_log2;
     bool ok = true;
     // A timed-out wait clears `ok` and later waits are skipped, but the loop
-    // runs to the end so both warps of a pair meet every named barrier.
+    // runs to the end so every softmax warp meets every named barrier.
     for (int i = 0; i < ntiles; ++i) {
       if (ok && !mbar_wait(&bar_s[i & 1], (i >> 1) & 1)) ok = false;
       __syncwarp();
@@ -245,8 +259,9 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                                      (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      if (warp_active) {
-        float s[32];
+      float s[32];
+      bool want = false;
+      if (computes) {
         tc::ld32(trow + C::kColS + (i & 1) * kKeyTile + 32 * half, s);
         tc::wait_ld();
         const int kbase = key0 + 32 * half;
@@ -258,39 +273,47 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         float mt = s[0];
 #pragma unroll
         for (int j = 1; j < 32; ++j) mt = fmaxf(mt, s[j]);
-        // the row max over both halves
         x_max[i & 1][half][r] = mt;
-        named_bar_sync(2 + quad, 64);
-        mt = fmaxf(mt, x_max[i & 1][half ^ 1][r]) * sl2;
-        const bool resc = row_ok && (mt > m_used + kRescaleLog2);
-        if (__any_sync(0xffffffffu, resc)) {
-          const float m_new = resc ? mt : m_used;
-          const float alpha = !resc ? 1.f : (m_used == -INFINITY ? 0.f : exp2f(m_used - m_new));
-          if (i > 0) {
-            // O holds the products of tiles < i: wait for the last of them,
-            // then rescale this thread's half of the row in place.
-            if (ok && !mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1)) ok = false;
-            __syncwarp();
-            tc::fence_after_sync();
+        want = row_ok && (mt * sl2 > m_used + kRescaleLog2);
+      }
+      // one barrier: both halves' maxima are visible, and whether any row of
+      // the block moves its reference max
+      const bool any_resc = named_bar_or(2, 32 * kTcSoftmaxWarps, want);
+      const float mt = (lanes_live && row_ok)
+                           ? fmaxf(x_max[i & 1][0][srow], x_max[i & 1][1][srow]) * sl2
+                           : -INFINITY;
+      const bool resc = row_ok && lanes_live && (mt > m_used + kRescaleLog2);
+      if (any_resc) {
+        const float m_new = resc ? mt : m_used;
+        const float alpha = !resc ? 1.f : (m_used == -INFINITY ? 0.f : exp2f(m_used - m_new));
+        if (i > 0 && lanes_live) {
+          // O holds the products of tiles < i: wait for the last of them,
+          // then rescale this thread's half of its TMEM lane in place.
+          if (ok && !mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1)) ok = false;
+          __syncwarp();
+          tc::fence_after_sync();
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              float o[32];
-              tc::ld32(trow + C::kColO + half * (D / 2) + c * 32, o);
-              tc::wait_ld();
+          for (int c = 0; c < D / 64; ++c) {
+            float o[32];
+            tc::ld32(trow + C::kColO + half * (D / 2) + c * 32, o);
+            tc::wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= alpha;
-              tc::st32(trow + C::kColO + half * (D / 2) + c * 32, o);
-            }
-            tc::wait_st();
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tc::st32(trow + C::kColO + half * (D / 2) + c * 32, o);
           }
-          l_half *= alpha;
-          m_used = m_new;
+          tc::wait_st();
         }
+        l_half *= alpha;
+        m_used = m_new;
+      }
+      if (computes) {
         // the P buffer of this parity is free once the P V of tile i-2 is done
         if (ok && i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
         __syncwarp();
         const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
-        uint8_t *prow = smem + C::kOffP + (i & 1) * 2 * C::kPBytes + r * 128;
+        uint8_t *pbuf = smem + C::kOffP + (i & 1) * 2 * C::kPBytes;
+        uint8_t *prow_hi = pbuf + r * 128;
+        uint8_t *prow_lo = packed ? pbuf + (r + kTcRows / 2) * 128 : pbuf + C::kPBytes + r * 128;
         float psum = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -305,9 +328,9 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
             hi[e] = bf16x2_bits(h);
             lo[e] = bf16x2_bits(__floats2bfloat162_rn(p0 - hf.x, p1 - hf.y));
           }
-          const int off = ((4 * half + cc) ^ (r & 7)) << 4;
-          *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4 *>(prow + C::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          const int off = ((4 * half + cc) ^ (r & 7)) << 4;   // (r + 64) & 7 == r & 7
+          *reinterpret_cast<uint4 *>(prow_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4 *>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         l_half += psum;
       }
@@ -318,18 +341,15 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     if (!ok) s_timeout = 1;
     // ---- epilogue: O rows out of TMEM.  Every softmax warp waits for the
-    //      last P V before any thread reuses the K/V ring below.
+    //      last P V before any thread reuses the K/V ring or P buffers.
     if (ntiles > 0) {
       if (ok && !mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) s_timeout = 1;
       __syncwarp();
       tc::fence_after_sync();
     }
-    x_l[half][r] = l_half;
-    named_bar_sync(2 + quad, 64);
-    l_row = l_half + x_l[half ^ 1][r];
 #pragma unroll
     for (int e = 0; e < D / 2; ++e) o_keep[e] = 0.f;
-    if (warp_active && ntiles > 0) {
+    if (lanes_live && ntiles > 0) {
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         float o[32];
@@ -339,7 +359,30 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         for (int e = 0; e < 32; ++e) o_keep[c * 32 + e] = o[e];
       }
     }
-    if (CS == 1 && row_ok && ntiles > 0) {
+    // packed: lanes r + 64 hold the remainder part of row r's P V
+    float *xo = reinterpret_cast<float *>(smem + C::kOffP);   // [64 rows][D], P buffers are free
+    if (packed && helper && row_ok) {
+#pragma unroll
+      for (int e = 0; e < D / 2; e += 4)
+        *reinterpret_cast<float4 *>(xo + srow * D + half * (D / 2) + e) =
+            make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
+    }
+    if (!helper) x_l[half][r] = l_half;
+    named_bar_sync(2, 32 * kTcSoftmaxWarps);
+    if (!helper) {
+      l_row = l_half + x_l[half ^ 1][r];
+      if (packed && row_ok) {
+#pragma unroll
+        for (int e = 0; e < D / 2; e += 4) {
+          const float4 v = *reinterpret_cast<const float4 *>(xo + r * D + half * (D / 2) + e);
+          o_keep[e] += v.x;
+          o_keep[e + 1] += v.y;
+          o_keep[e + 2] += v.z;
+          o_keep[e + 3] += v.w;
+        }
+      }
+    }
+    if (CS == 1 && !helper && row_ok && ntiles > 0) {
       const float inv = 1.f / l_row;
       const int rr = row0 + r;
       __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
@@ -362,7 +405,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   if (CS > 1) {
     // ---- split merge: every CTA pushes its rows into the owner's smem
     cluster_sync_all();  // every CTA of the cluster is done with its K/V ring
-    if (warp >= 2 && row_ok) {
+    if (warp >= 2 && !helper && row_ok) {
       const int owner = r / rpr;
       const int slot = split * rpr + (r - owner * rpr);
       float *mbase = reinterpret_cast<float *>(smem + C::kOffKV) + slot * C::kMergeStride + half * (D / 2);
