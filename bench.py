@@ -172,6 +172,9 @@ class Step:
         self.o = torch.empty((w.T, w.Hq, w.D), dtype=w.q.dtype, device=dev)
         self.W = w.max_depth + 1
         self.ws = ttv.make_verify_workspace(w.B, w.T, w.V)
+        self.max_prefix = int(w.prefix_lens.max())
+        na = ttv.tree_attn_workspace_size(w.B, w.T, w.Hq, w.Hkv, w.D, self.max_prefix)
+        self.ws_attn = torch.zeros(max(na, 16), dtype=torch.uint8, device=dev)
         self.outs = dict(
             accept_len=torch.empty(w.B, dtype=torch.int32, device=dev),
             path_nodes=torch.empty((w.B, self.W), dtype=torch.int32, device=dev),
@@ -198,7 +201,7 @@ class Step:
             ev[1].record()
             ev[2].record()
         ttv.tree_attn(c["q"], c["k"], c["v"], self.pl, self.off, self.mask, self.max_prefix,
-                      self.status, o=self.o, stream=stream)
+                      self.status, o=self.o, workspace=self.ws_attn, stream=stream)
         if ev is not None:
             ev[3].record()
             ev[4].record()
@@ -368,7 +371,7 @@ def per_kernel_graph_times(st, stream, n):
                     ttv.build_tree_mask(st.par, st.off, st.status, mask=st.mask, depth=st.depth)
                 elif kind == 1:
                     ttv.tree_attn(c["q"], c["k"], c["v"], st.pl, st.off, st.mask, st.max_prefix,
-                                  st.status, o=st.o)
+                                  st.status, o=st.o, workspace=st.ws_attn)
                 else:
                     ttv.tree_verify(c["tl"], c["dl"], st.tok, st.par, st.off, w.temperature,
                                     i, st.W, st.status, st.ws, outputs=st.outs)

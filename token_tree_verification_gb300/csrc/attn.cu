@@ -491,16 +491,16 @@ bool encode_kv_map(CUtensorMap *m, const void *base, int B, int Hkv, int S_cap, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over q [T][Hq][D] bf16 whose box is one 128-row query block of a
-// KV head: 64 dims x G heads x (128 / G) nodes, loaded with 128-byte swizzle
-// so the block lands as 128 rows of 128 bytes (node-major, head-minor).
-bool encode_q_map(CUtensorMap *m, const void *base, int T, int Hq, int G, int D) {
+// 3-D map over q [T][Hq][D] bf16 whose box is one query block of a KV head:
+// 64 dims x G heads x (rows / G) nodes, loaded with 128-byte swizzle so the
+// block lands as `rows` rows of 128 bytes (node-major, head-minor).
+bool encode_q_map(CUtensorMap *m, const void *base, int T, int Hq, int G, int D, int rows) {
   EncodeFn enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(rows / G)};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -514,13 +514,17 @@ bool use_mma_kernel() {
   return e != nullptr && strcmp(e, "mma") == 0;
 }
 
+// SMs of the current device; 152 (GB300) when no device can be queried, so a
+// host-only caller still gets the workspace size the GPU will ask for.
 int sm_count() {
   static int n = 0;
   if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 152;
   }
   return n;
 }
@@ -575,8 +579,9 @@ int launch_mma(const spec::AttnArgs &args, int max_prefix, int T, cudaStream_t s
 
 extern "C" size_t spec_tree_attn_workspace_size(int B, int T, int Hq, int Hkv, int D,
                                                 int max_prefix) {
-  (void)B; (void)T; (void)Hq; (void)Hkv; (void)D; (void)max_prefix;
-  return 0;
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || (D != 64 && D != 128) || max_prefix < 0)
+    return 0;
+  return spec::attn_tc_workspace_bytes(B, T, Hkv, Hq / Hkv, D, max_prefix, sm_count());
 }
 
 extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_cache, void *o,
@@ -585,7 +590,6 @@ extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_
                               const int32_t *tree_offsets, const uint32_t *mask,
                               float softmax_scale, void *workspace, size_t workspace_bytes,
                               int32_t *status, void *stream) {
-  (void)workspace; (void)workspace_bytes;
   if (!q || !k_cache || !v_cache || !o || !prefix_lens || !tree_offsets || !mask || !status)
     return SPEC_ERR_NULL;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
@@ -625,10 +629,14 @@ extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_
   }
   if (use_mma_kernel())
     return D == 128 ? launch_mma<128>(args, max_prefix, T, st) : launch_mma<64>(args, max_prefix, T, st);
+  // every row block holds at most 64 rows: the packed tcgen05 variant
+  const bool packed = (T < SPEC_MAX_TREE_NODES ? T : SPEC_MAX_TREE_NODES) * G <= 64;
   CUtensorMap tmq, tmk, tmv;
-  if (!encode_q_map(&tmq, q, T, Hq, G, D) || !encode_kv_map(&tmk, k_cache, B, Hkv, S_cap, D) ||
+  if (!encode_q_map(&tmq, q, T, Hq, G, D, packed ? 64 : 128) ||
+      !encode_kv_map(&tmk, k_cache, B, Hkv, S_cap, D) ||
       !encode_kv_map(&tmv, v_cache, B, Hkv, S_cap, D))
     return SPEC_ERR_CUDA;
-  return D == 128 ? spec::launch_attn_tc<128>(args, max_prefix, T, tmq, tmk, tmv, sm_count(), st)
-                  : spec::launch_attn_tc<64>(args, max_prefix, T, tmq, tmk, tmv, sm_count(), st);
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15)) return SPEC_ERR_ALIGNMENT;
+  return spec::launch_attn_tc(args, max_prefix, T, tmq, tmk, tmv, packed, sm_count(), workspace,
+                              workspace_bytes, st);
 }

@@ -5,29 +5,31 @@
 // softmax, times V); SpecInfer news write-up "Token 樹驗證器" (tree K/V
 // appended to the cache depth-first, mask restricted to the node's ancestors).
 //
-// One CTA = one key split x one block of 128 query rows x one (request, KV
-// head).  Rows are (node, head-in-group) pairs, so one K/V tile feeds all G
-// query heads of the KV head.  Warp roles:
+// One CTA = one key split x one block of query rows x one (request, KV head).
+// Rows are (node, head-in-group) pairs, so one K/V tile feeds all G query
+// heads of the KV head.  Warp roles:
 //   warp 0      TMA producer: the Q block once, then 64-key K and V tiles
-//               (128-byte swizzle) into a 3-stage ring.
+//               (128-byte swizzle) into a ring of stages.
 //   warp 1      allocates TMEM; one thread issues the MMAs:
 //                 S_i = Q K_i^T            M=128, N=64, K=D   (TMEM S[i%2])
-//                 O  += P_i V_i (hi, lo)   M=128, N=D,  K=64  (TMEM O)
+//                 O  += P_i V_i            M=128, N=D,  K=64  (TMEM O)
 //               with S_{i+1} issued before P_i is ready, so the softmax of
 //               one tile overlaps the QK^T of the next.
 //   warps 2-9   two threads per TMEM lane (= query row), one per half of
 //               the tile's keys: read S from TMEM, mask with the node's
-//               ancestor bits, share the row max with the partner thread,
-//               online softmax with a lazily moved reference max (the stored
-//               O is rescaled only when a row's max grows by more than 2^8),
-//               write P as bf16 high and remainder parts to shared memory.
-//               With at most 64 rows the remainder part goes to the unused
-//               rows 64-127 of the same P operand (one 4-MMA P V pass; the
-//               two halves are added from TMEM lanes r and r + 64 at the end,
-//               and the warps of lanes 64-127 mirror their rows' rescaling).
-//   epilogue    the O rows leave TMEM; the splits of one cluster push their
-//               (m, l, O) rows into the owning CTA's shared memory with
-//               remote stores, which then merges them locally.
+//               ancestor bits, share the row max, online softmax with a
+//               lazily moved reference max (the stored O is rescaled only
+//               when a row's max grows by more than 2^8), write P as bf16
+//               high and remainder parts to shared memory (P V then keeps
+//               about 16 significant bits of every weight).
+// Blocks of at most 64 rows (PACKED) put the remainder part in the unused
+// rows 64-127 of the same P operand: one 4-MMA P V pass per tile, the two
+// halves added from TMEM lanes r and r + 64 at the end (the warps of lanes
+// 64-127 mirror their rows' rescaling); the smaller Q block and P buffers
+// leave room for a 5-stage K/V ring.
+// Key splits merge through L2: each split writes its (m, l, O) rows to the
+// workspace and bumps the block's counter; the last split to arrive merges
+// them and resets the counter.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -37,33 +39,37 @@
 namespace spec {
 
 constexpr int kTcRows = 128;
-constexpr int kTcStages = 3;
 constexpr int kTcSoftmaxWarps = 8;   // two warps (key halves) per TMEM lane quadrant
 constexpr int kTcThreads = 32 * (2 + kTcSoftmaxWarps);
 constexpr float kRescaleLog2 = 8.f;
 
-template <int D>
+template <int D, bool PACKED>
 struct TcCfg {
+  static constexpr int kStages = PACKED ? 5 : 3;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kQBoxBytes = kTcRows * 128;
-  static constexpr int kQBytes = kTcRows * D * 2;
+  static constexpr int kQRows = PACKED ? kTcRows / 2 : kTcRows;  // rows the TMA loads
+  static constexpr int kQBoxBytes = kQRows * 128;
+  static constexpr int kQBytes = kQRows * D * 2;
   static constexpr int kKVBoxBytes = kKeyTile * 128;
   static constexpr int kTileBytes = kKeyTile * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kPBytes = kTcRows * kKeyTile * 2;   // one of the hi / lo parts
+  static constexpr int kPBytes = kTcRows * kKeyTile * 2;   // one 128-row bf16 P operand
+  static constexpr int kPParts = PACKED ? 1 : 2;           // separate high / remainder operands
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQBytes;
-  static constexpr int kOffP = kOffKV + kTcStages * kStageBytes;
-  static constexpr int kSmem = kOffP + 2 * 2 * kPBytes + 1024;
-  static constexpr int kMergeStride = D + 4;             // floats per (split, row) slot
+  static constexpr int kOffP = kOffKV + kStages * kStageBytes;
+  static constexpr int kSmem = kOffP + 2 * kPParts * kPBytes + 1024;
   static constexpr uint32_t kTmemCols = 256;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 128;
-  // owner-side merge slots: (split, row) pairs, at most rows + 7 of them
-  static_assert((kTcRows + 7) * kMergeStride * 4 <= kTcStages * kStageBytes,
-                "merge buffer must fit in the K/V ring");
-  static_assert(kTcRows / 2 * D * 4 <= 2 * 2 * kPBytes, "packed remainder exchange fits the P buffers");
+  static_assert(!PACKED || kTcRows / 2 * D * 4 <= 2 * kPParts * kPBytes,
+                "packed remainder exchange fits the P buffers");
+  static_assert(kSmem <= 227 * 1024 - 4096, "shared memory budget");
 };
+
+// Workspace record of one split: O rows (fp32, unnormalised) then m and l.
+template <int D>
+__host__ __device__ constexpr int tc_partial_floats() { return kTcRows * (D + 2); }
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
                                             int c1, int c2) {
@@ -78,29 +84,30 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv) {
-  using C = TcCfg<D>;
+                    const __grid_constant__ CUtensorMap tmv, uint32_t *counters, float *partials) {
+  using C = TcCfg<D, PACKED>;
+  constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_full[kTcStages], bar_empty[kTcStages];
+  __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
   __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p[2], bar_o[2];
   __shared__ uint32_t s_tmem;
   __shared__ float x_max[2][2][kTcRows];   // [tile parity][key half][row]
   __shared__ float x_l[2][kTcRows];
-  __shared__ float m_slot[8][kTcRows], l_slot[8][kTcRows];   // owner-side merge (split, row)
-  __shared__ int s_timeout;
+  __shared__ int s_timeout, s_last;
 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_addr(smem);
-  const int CS = static_cast<int>(cluster_size());
-  const int split = static_cast<int>(cluster_rank());
+  const int CS = static_cast<int>(gridDim.x);
+  const int split = static_cast<int>(blockIdx.x);
   const int rb = blockIdx.y;
   const int b = blockIdx.z / a.Hkv;
   const int g = blockIdx.z % a.Hkv;
+  const int unit = blockIdx.z * gridDim.y + blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const ReqGeom R = request_geometry(a, b);
@@ -108,22 +115,21 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const int row0 = rb * kTcRows;
   if (R.err) {
     if (tid == 0 && split == 0 && rb == 0 && g == 0) report(a.status, b, R.err);
-    return;  // uniform across the cluster
+    return;  // uniform across the splits of this block: none touches the counter
   }
-  if (row0 >= rows_total) return;  // uniform across the cluster
+  if (row0 >= rows_total) return;  // uniform across the splits of this block
   const int rows_here = min(kTcRows, rows_total - row0);
-  // Packed mode (at most 64 rows): the bf16 remainder of P goes to rows
-  // 64-127 of the same P operand, so one 4-MMA pass computes both halves
-  // of P V into TMEM lanes r and r + 64.
-  const bool packed = rows_here <= kTcRows / 2;
+  if (PACKED && rows_here > kTcRows / 2) {  // launch contract broken: never expected
+    if (tid == 0) report(a.status, b, SPEC_ERR_SHAPE);
+    return;
+  }
   const int tiles_total = (R.keys + kKeyTile - 1) / kKeyTile;
   const int per = (tiles_total + CS - 1) / CS;
   const int t0 = split * per;
   const int ntiles = max(0, min(t0 + per, tiles_total) - t0);
-  const int rpr = (rows_here + CS - 1) / CS;   // rows merged by each CTA of the cluster
 
   if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
@@ -135,6 +141,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     fence_barrier_init();
     s_timeout = 0;
+    s_last = 0;
   }
   if (warp == 1) {
     tc::tmem_alloc(&s_tmem, C::kTmemCols);
@@ -149,13 +156,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const int quad = warp & 3;
   const int half = (warp - 2) >> 2;
   const int r = quad * 32 + lane;
-  // the score row this thread follows: its own, or (helper lanes 64-127 in
-  // packed mode) the row whose remainder part it accumulates
-  const bool helper = packed && quad >= 2;
+  // the score row this thread follows: its own, or (lanes 64-127 when
+  // packed) the row whose remainder part it accumulates
+  const bool helper = PACKED && quad >= 2;
   const int srow = helper ? r - kTcRows / 2 : r;
   const bool row_ok = srow < rows_here;
   const bool computes = warp >= 2 && !helper && quad * 32 < rows_here;   // reads S, writes P
-  const bool lanes_live = warp >= 2 && (quad & (packed ? 1 : 3)) * 32 < rows_here;
+  const bool lanes_live = warp >= 2 && (quad & (PACKED ? 1 : 3)) * 32 < rows_here;
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   float o_keep[D / 2];
   float m_used = -INFINITY, l_half = 0.f, l_row = 0.f;
@@ -172,8 +179,8 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         tma_load_3d(smem + C::kOffQ + bx * C::kQBoxBytes, &tmq, &bar_q, bx * 64, g * a.G,
                     R.lo + row0 / a.G);
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kTcStages;
-        if (i >= kTcStages && !mbar_wait(&bar_empty[st], ((i / kTcStages) - 1) & 1)) {
+        const int st = i % NS;
+        if (i >= NS && !mbar_wait(&bar_empty[st], ((i / NS) - 1) & 1)) {
           s_timeout = 1;
           break;
         }
@@ -193,17 +200,18 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kKeyTile, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
-      const int parts = packed ? 1 : 2;
       bool ok = mbar_wait(&bar_q, 0);
       tc::fence_after_sync();
       for (int i = 0; ok && i <= ntiles; ++i) {
         if (i < ntiles) {
-          const int st = i % kTcStages;
-          if (!mbar_wait(&bar_full[st], (i / kTcStages) & 1)) { ok = false; break; }
+          const int st = i % NS;
+          if (!mbar_wait(&bar_full[st], (i / NS) & 1)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t kb = sb + C::kOffKV + st * C::kStageBytes;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
+            // Q rows past the loaded block (packed mode) read the next
+            // region: those S rows are padding and never read back.
             const uint64_t ad = tc::smem_desc_sw128(
                 sb + C::kOffQ + (ks >> 2) * C::kQBoxBytes + (ks & 3) * 32, 16, 1024);
             const uint64_t bd =
@@ -213,12 +221,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           tc::commit(&bar_s[i & 1]);
         }
         if (i >= 1) {
-          const int j = i - 1, st = j % kTcStages;
+          const int j = i - 1, st = j % NS;
           if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
-          const uint32_t pb = sb + C::kOffP + (j & 1) * 2 * C::kPBytes;
-          for (int part = 0; part < parts; ++part) {
+          const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPParts * C::kPBytes;
+#pragma unroll
+          for (int part = 0; part < C::kPParts; ++part) {
 #pragma unroll
             for (int kk = 0; kk < kKeyTile / 16; ++kk) {
               const uint64_t ad = tc::smem_desc_sw128(pb + part * C::kPBytes + kk * 32, 16, 1024);
@@ -245,7 +254,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       __syncwarp();
       tc::fence_after_sync();
       const int key0 = (t0 + i) * kKeyTile;
-      const int st = i % kTcStages;
+      const int st = i % NS;
       if (key0 + kKeyTile > R.keys) {
         // V rows past the request's last key may hold anything: zero them so
         // their zero weights contribute exact zeros.
@@ -311,9 +320,9 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         if (ok && i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
         __syncwarp();
         const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
-        uint8_t *pbuf = smem + C::kOffP + (i & 1) * 2 * C::kPBytes;
+        uint8_t *pbuf = smem + C::kOffP + (i & 1) * C::kPParts * C::kPBytes;
         uint8_t *prow_hi = pbuf + r * 128;
-        uint8_t *prow_lo = packed ? pbuf + (r + kTcRows / 2) * 128 : pbuf + C::kPBytes + r * 128;
+        uint8_t *prow_lo = PACKED ? pbuf + (r + kTcRows / 2) * 128 : pbuf + C::kPBytes + r * 128;
         float psum = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -341,7 +350,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     if (!ok) s_timeout = 1;
     // ---- epilogue: O rows out of TMEM.  Every softmax warp waits for the
-    //      last P V before any thread reuses the K/V ring or P buffers.
+    //      last P V before any thread reuses the P buffers.
     if (ntiles > 0) {
       if (ok && !mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) s_timeout = 1;
       __syncwarp();
@@ -361,7 +370,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     // packed: lanes r + 64 hold the remainder part of row r's P V
     float *xo = reinterpret_cast<float *>(smem + C::kOffP);   // [64 rows][D], P buffers are free
-    if (packed && helper && row_ok) {
+    if (PACKED && helper && row_ok) {
 #pragma unroll
       for (int e = 0; e < D / 2; e += 4)
         *reinterpret_cast<float4 *>(xo + srow * D + half * (D / 2) + e) =
@@ -371,7 +380,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     named_bar_sync(2, 32 * kTcSoftmaxWarps);
     if (!helper) {
       l_row = l_half + x_l[half ^ 1][r];
-      if (packed && row_ok) {
+      if (PACKED && row_ok) {
 #pragma unroll
         for (int e = 0; e < D / 2; e += 4) {
           const float4 v = *reinterpret_cast<const float4 *>(xo + r * D + half * (D / 2) + e);
@@ -382,7 +391,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         }
       }
     }
-    if (CS == 1 && !helper && row_ok && ntiles > 0) {
+    if (!helper && row_ok && ntiles > 0 && CS == 1) {
       const float inv = 1.f / l_row;
       const int rr = row0 + r;
       __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
@@ -398,50 +407,62 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         *reinterpret_cast<uint4 *>(dst + q8 * 8) = pk;
       }
     }
+    if (CS > 1 && !helper && row_ok) {
+      // this split's rows to the workspace: O half-row, then m and l
+      float *rec = partials + (static_cast<size_t>(unit) * CS + split) * tc_partial_floats<D>() +
+                   static_cast<size_t>(r) * (D + 2);
+#pragma unroll
+      for (int e = 0; e < D / 2; e += 2)
+        __stcg(reinterpret_cast<float2 *>(rec + half * (D / 2) + e), make_float2(o_keep[e], o_keep[e + 1]));
+      if (half == 0) __stcg(reinterpret_cast<float2 *>(rec + D),
+                            make_float2(ntiles > 0 ? m_used : -INFINITY, l_row));
+      __threadfence();
+    }
   }
 
   __syncwarp();
   tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (s_timeout && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
   if (CS > 1) {
-    // ---- split merge: every CTA pushes its rows into the owner's smem
-    cluster_sync_all();  // every CTA of the cluster is done with its K/V ring
-    if (warp >= 2 && !helper && row_ok) {
-      const int owner = r / rpr;
-      const int slot = split * rpr + (r - owner * rpr);
-      float *mbase = reinterpret_cast<float *>(smem + C::kOffKV) + slot * C::kMergeStride + half * (D / 2);
-      const uint32_t dst = peer_addr(mbase, owner);
-#pragma unroll
-      for (int e = 0; e < D / 2; e += 4)
-        st_peer_f32x4(dst + e * 4, make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]));
-      if (half == 0) {
-        st_peer_f32(peer_addr(&m_slot[split][r - owner * rpr], owner), ntiles > 0 ? m_used : -INFINITY);
-        st_peer_f32(peer_addr(&l_slot[split][r - owner * rpr], owner), l_row);
-      }
+    // ---- split merge through L2: the last split of this block merges
+    if (tid == 0) {
+      const uint32_t prev = atomicAdd(counters + unit, 1u);
+      s_last = (static_cast<int>(prev) == CS - 1) ? 1 : 0;
     }
-    cluster_sync_all();  // the pushes have landed
-    const int r_begin = split * rpr, r_end = min(rows_here, r_begin + rpr);
-    const int nvec = max(0, r_end - r_begin) * (D / 4);
-    const float *mb = reinterpret_cast<const float *>(smem + C::kOffKV);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float *base = partials + static_cast<size_t>(unit) * CS * tc_partial_floats<D>();
+    const int nvec = rows_here * (D / 4);
     for (int idx = tid; idx < nvec; idx += kTcThreads) {
       const int lr = idx / (D / 4);
       const int c4 = idx % (D / 4);
       float M = -INFINITY;
-      for (int s2 = 0; s2 < CS; ++s2) M = fmaxf(M, m_slot[s2][lr]);
+      for (int s2 = 0; s2 < CS; ++s2)
+        M = fmaxf(M, __ldcg(base + s2 * tc_partial_floats<D>() + lr * (D + 2) + D));
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       float L = 0.f;
       for (int s2 = 0; s2 < CS; ++s2) {
-        const float ms = m_slot[s2][lr];
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - M);
-        L += w * l_slot[s2][lr];
-        const float4 v = *reinterpret_cast<const float4 *>(mb + (s2 * rpr + lr) * C::kMergeStride + c4 * 4);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+        const float *rec = base + s2 * tc_partial_floats<D>() + lr * (D + 2);
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(rec + D));
+        if (ml.x == -INFINITY) continue;
+        const float w = exp2f(ml.x - M);
+        L += w * ml.y;
+        const float2 v0 = __ldcg(reinterpret_cast<const float2 *>(rec + c4 * 4));
+        const float2 v1 = __ldcg(reinterpret_cast<const float2 *>(rec + c4 * 4 + 2));
+        acc.x += w * v0.x;
+        acc.y += w * v0.y;
+        acc.z += w * v1.x;
+        acc.w += w * v1.y;
       }
       const float inv = 1.f / L;
-      const int rr = row0 + r_begin + lr;
+      const int rr = row0 + lr;
       __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
                            (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + c4 * 4;
       uint2 pk;
@@ -449,29 +470,50 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       pk.y = bf16x2_bits(__floats2bfloat162_rn(acc.z * inv, acc.w * inv));
       *reinterpret_cast<uint2 *>(dst) = pk;
     }
-  }
-  __syncthreads();
-  tc::fence_after_sync();
-  if (s_timeout && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
-  if (warp == 1) {
-    __syncwarp();
-    tc::tmem_dealloc(tmem, C::kTmemCols);
+    if (tid == 0) counters[unit] = 0u;  // ready for the next call
   }
 }
 
-template __global__ void tree_attn_tc_kernel<64>(const AttnArgs, const __grid_constant__ CUtensorMap,
-                                                 const __grid_constant__ CUtensorMap,
-                                                 const __grid_constant__ CUtensorMap);
-template __global__ void tree_attn_tc_kernel<128>(const AttnArgs, const __grid_constant__ CUtensorMap,
-                                                  const __grid_constant__ CUtensorMap,
-                                                  const __grid_constant__ CUtensorMap);
+// Split plan shared by the launcher and the workspace query: the split count
+// that minimises (waves x tiles per CTA) at one CTA per SM.
+void plan_attn_tc(int B, int T, int Hkv, int G, int max_prefix, int num_sms, int *cs_out,
+                  int *rowblocks_out) {
+  const int max_nodes = T < SPEC_MAX_TREE_NODES ? T : SPEC_MAX_TREE_NODES;
+  const int rowblocks = (max_nodes * G + kTcRows - 1) / kTcRows;
+  const long long max_keys = static_cast<long long>(max_prefix) + max_nodes;
+  const long long tiles_max = (max_keys + kKeyTile - 1) / kKeyTile;
+  const long long units = static_cast<long long>(rowblocks) * B * Hkv;
+  int cs = 1;
+  long long best = -1;
+  for (int c = 1; c <= 16; c *= 2) {
+    if (c > 1 && tiles_max < 2 * c) break;
+    const long long waves = (units * c + num_sms - 1) / num_sms;
+    const long long cost = waves * ((tiles_max + c - 1) / c) + (c > 1 ? 2 : 0);
+    if (best < 0 || cost < best) {
+      best = cost;
+      cs = c;
+    }
+  }
+  *cs_out = cs;
+  *rowblocks_out = rowblocks;
+}
 
-// Host launcher (declared in attn_common.cuh).
-template <int D>
-int launch_attn_tc(const AttnArgs &args, int max_prefix, int T, const CUtensorMap &tmq,
-                   const CUtensorMap &tmk, const CUtensorMap &tmv, int num_sms, cudaStream_t stream) {
-  using C = TcCfg<D>;
-  auto kernel = tree_attn_tc_kernel<D>;
+size_t attn_tc_workspace_bytes(int B, int T, int Hkv, int G, int D, int max_prefix, int num_sms) {
+  int cs, rowblocks;
+  plan_attn_tc(B, T, Hkv, G, max_prefix, num_sms, &cs, &rowblocks);
+  if (cs == 1) return 0;
+  const size_t units = static_cast<size_t>(rowblocks) * B * Hkv;
+  const size_t counters = (units * sizeof(uint32_t) + 255) & ~size_t(255);
+  const size_t rec = static_cast<size_t>(kTcRows) * (D + 2) * sizeof(float);
+  return counters + units * cs * rec;
+}
+
+template <int D, bool PACKED>
+static int launch_tc(const AttnArgs &args, const CUtensorMap &tmq, const CUtensorMap &tmk,
+                     const CUtensorMap &tmv, int cs, int rowblocks, uint32_t *counters,
+                     float *partials, cudaStream_t stream) {
+  using C = TcCfg<D, PACKED>;
+  auto kernel = tree_attn_tc_kernel<D, PACKED>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
@@ -479,43 +521,33 @@ int launch_attn_tc(const AttnArgs &args, int max_prefix, int T, const CUtensorMa
       return SPEC_ERR_CUDA;
     configured = true;
   }
-  const int max_nodes = T < SPEC_MAX_TREE_NODES ? T : SPEC_MAX_TREE_NODES;
-  const int rowblocks = (max_nodes * args.G + kTcRows - 1) / kTcRows;
-  const long long max_keys = static_cast<long long>(max_prefix) + max_nodes;
-  const long long tiles_max = (max_keys + kKeyTile - 1) / kKeyTile;
-  const long long units = static_cast<long long>(rowblocks) * args.B * args.Hkv;
-  if (units > 65535) return SPEC_ERR_SHAPE;
-  // Pick the split count that minimises (waves x tiles per CTA), one CTA/SM.
-  int cs = 1;
-  long long best = -1;
-  for (int c = 1; c <= 8; c *= 2) {
-    if (c > 1 && tiles_max < 2 * c) break;
-    const long long waves = (units * c + num_sms - 1) / num_sms;
-    const long long cost = waves * ((tiles_max + c - 1) / c) + (c > 1 ? 1 : 0);
-    if (best < 0 || cost < best) {
-      best = cost;
-      cs = c;
-    }
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs, rowblocks, static_cast<unsigned>(args.B * args.Hkv));
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args, tmq, tmk, tmv) == cudaSuccess ? SPEC_OK
-                                                                             : SPEC_ERR_CUDA;
+  const dim3 grid(cs, rowblocks, static_cast<unsigned>(args.B * args.Hkv));
+  kernel<<<grid, kTcThreads, C::kSmem, stream>>>(args, tmq, tmk, tmv, counters, partials);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-template int launch_attn_tc<64>(const AttnArgs &, int, int, const CUtensorMap &, const CUtensorMap &,
-                                const CUtensorMap &, int, cudaStream_t);
-template int launch_attn_tc<128>(const AttnArgs &, int, int, const CUtensorMap &, const CUtensorMap &,
-                                 const CUtensorMap &, int, cudaStream_t);
+int launch_attn_tc(const AttnArgs &args, int max_prefix, int T, const CUtensorMap &tmq,
+                   const CUtensorMap &tmk, const CUtensorMap &tmv, bool packed, int num_sms,
+                   void *workspace, size_t ws_bytes, cudaStream_t stream) {
+  int cs, rowblocks;
+  plan_attn_tc(args.B, T, args.Hkv, args.G, max_prefix, num_sms, &cs, &rowblocks);
+  if (static_cast<long long>(rowblocks) * args.B * args.Hkv > 65535) return SPEC_ERR_SHAPE;
+  uint32_t *counters = nullptr;
+  float *partials = nullptr;
+  if (cs > 1) {
+    const size_t need = attn_tc_workspace_bytes(args.B, T, args.Hkv, args.G, args.D, max_prefix,
+                                                num_sms);
+    if (!workspace || ws_bytes < need) return SPEC_ERR_WORKSPACE;
+    const size_t units = static_cast<size_t>(rowblocks) * args.B * args.Hkv;
+    counters = static_cast<uint32_t *>(workspace);
+    partials = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                         ((units * sizeof(uint32_t) + 255) & ~size_t(255)));
+  }
+  if (args.D == 128)
+    return packed ? launch_tc<128, true>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream)
+                  : launch_tc<128, false>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream);
+  return packed ? launch_tc<64, true>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream)
+                : launch_tc<64, false>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream);
+}
 
 }  // namespace spec

@@ -1,6 +1,7 @@
-// Steps V1-V4 and R: verification of a speculated token tree, cluster
-// kernel (one thread-block cluster per node, the vocabulary split across the
-// cluster) for vocabularies too large for one CTA, and the host entry point.
+// Steps V1-V4 and R: verification of a speculated token tree.  Stochastic
+// verification runs one thread-block cluster per node (the node's target and
+// draft rows split across the cluster's shared memory, about 16K entries per
+// CTA); greedy verification runs the per-node kernel of verify_node.cu.
 //
 // Sources: speculative-decoding explainer (intelliparadigm.com) §2.2
 // 三阶段工作流程详解 — stage 2: accept probability alpha = min(1, p/q); stage 3:
@@ -380,13 +381,12 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
   if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 15) return SPEC_ERR_ALIGNMENT;
 
-  const bool node_kernel = greedy || V <= kNodeMaxV;
-  int CS = (V + 4095) / 4096;
+  int CS = (V + kChunkTarget - 1) / kChunkTarget;
   if (CS > kMaxCS) CS = kMaxCS;
   if (CS < 1) CS = 1;
   int chunk = (V + CS - 1) / CS;
   chunk = (chunk + 3) & ~3;
-  if (!node_kernel && chunk > kMaxChunk) return SPEC_ERR_SHAPE;
+  if (!greedy && chunk > kMaxChunk) return SPEC_ERR_SHAPE;
 
   VerifyArgs args;
   args.target = target_logits;
@@ -414,8 +414,7 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
   ws += align256(sizeof(int32_t) * T);
   args.fallback = reinterpret_cast<int32_t *>(ws);
 
-  if (node_kernel)
-    return launch_verify_node(args, static_cast<cudaStream_t>(stream));
+  if (greedy) return launch_verify_greedy(args, static_cast<cudaStream_t>(stream));
   const size_t smem = sizeof(float) * 2 * static_cast<size_t>(chunk);
   static int configured_smem = -1;
   if (configured_smem < static_cast<int>(smem)) {

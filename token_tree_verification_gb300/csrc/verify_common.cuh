@@ -13,14 +13,13 @@
 
 namespace spec {
 
-constexpr int kVThreads = 256;     // cluster kernel: threads per CTA
+constexpr int kVThreads = 1024;    // cluster kernel: threads per CTA
 constexpr int kVWarps = kVThreads / 32;
 constexpr int kMaxCS = 8;          // CTAs per cluster (portable limit)
+constexpr int kChunkTarget = 16384;  // vocabulary entries per CTA the cluster size aims at
 constexpr int kMaxChunk = 27648;   // floats per CTA per row (2 rows fit in 216 KB)
 constexpr int kGreedyThreads = 1024;  // greedy per-node kernel: threads per CTA
-constexpr int kNodeThreads = 512;     // stochastic per-node kernel: threads per CTA
-constexpr int kNodeElems = 64;        // draft entries per thread held in registers
-constexpr int kNodeMaxV = kNodeThreads * kNodeElems;
+constexpr int kTreeWindow = 2 * SPEC_MAX_TREE_NODES - 1;   // nodes t-127 .. t+127
 constexpr int kFlagAccept = 1;
 constexpr int kFlagTie = 2;
 constexpr float kTieBand = 1e-6f;
@@ -43,6 +42,8 @@ struct VerifyArgs {
 
 // A node's tree context, staged in shared memory by load_tree().
 struct TreeSmem {
+  int wpar[kTreeWindow + 1];          // parents / tokens of nodes t-127 .. t+127
+  int wtok[kTreeWindow + 1];
   int par[SPEC_MAX_TREE_NODES];
   int tok[SPEC_MAX_TREE_NODES];
   int child[SPEC_MAX_TREE_NODES];     // u's children in index order
@@ -119,12 +120,13 @@ static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, c
                              const int *stok) {
   const int lane = threadIdx.x & 31;
   if (*reinterpret_cast<volatile int32_t *>(a.status + b) != 0) return;
-  int par[4], flg[4];
+  int par[4], flg[4], fbk[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int i = lane + 32 * s;
     par[s] = i < n ? spar[i] : -2;
     flg[s] = i < n ? __ldcg(a.flags + lo + i) : 0;
+    fbk[s] = i < n ? __ldcg(a.fallback + lo + i) : 0;
   }
   // depth of each node (parents are validated: parent < index)
   int maxd = 0;
@@ -167,7 +169,13 @@ static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, c
       ties += __popc(m);
     }
     if (next < 0) {
-      const int fb = __ldcg(a.fallback + lo + cur);
+      // the fallback of node `cur` sits in lane cur % 32, slot cur / 32
+      const int f0 = __shfl_sync(0xffffffffu, fbk[0], cur & 31);
+      const int f1 = __shfl_sync(0xffffffffu, fbk[1], cur & 31);
+      const int f2 = __shfl_sync(0xffffffffu, fbk[2], cur & 31);
+      const int f3 = __shfl_sync(0xffffffffu, fbk[3], cur & 31);
+      const int sl = cur >> 5;
+      const int fb = sl == 0 ? f0 : (sl == 1 ? f1 : (sl == 2 ? f2 : f3));
       if (lane == 0) ot[acc] = fb & 0x7fffffff;
       ties += (fb >> 31) & 1;
       break;
@@ -201,14 +209,22 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
 }
 
 
-// Every thread of the CTA (blockDim >= 128) calls this: find node t's
+// Every thread of the CTA (blockDim >= 256) calls this: find node t's
 // request, stage its parents and tokens, validate them, and list u's
 // children in index order.  Errors are identical in every CTA of a group.
+// A request holds at most 128 nodes, so the parents and tokens of nodes
+// t-127 .. t+127 are loaded in the same round as the offsets.
 static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (tid == 0) {
     ts.meta[0] = 0;
     ts.meta[1] = -1;
+  }
+  if (tid < kTreeWindow) {
+    const int x = t - (SPEC_MAX_TREE_NODES - 1) + tid;
+    const bool in = x >= 0 && x < a.T;
+    ts.wpar[tid] = in ? __ldg(a.parents + x) : -2;
+    ts.wtok[tid] = in ? __ldg(a.tokens + x) : 0;
   }
   __syncthreads();
   if (a.B < static_cast<int>(blockDim.x)) {
@@ -237,8 +253,9 @@ static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts) {
   uint32_t child_bal = 0;
   if (!c.err && tid < SPEC_MAX_TREE_NODES) {
     if (tid < c.n) {
-      const int p = __ldg(a.parents + c.lo + tid);
-      const int x = __ldg(a.tokens + c.lo + tid);
+      const int wi = c.lo + tid - (t - (SPEC_MAX_TREE_NODES - 1));   // in [0, 254]
+      const int p = ts.wpar[wi];
+      const int x = ts.wtok[wi];
       ts.par[tid] = p;
       ts.tok[tid] = x;
       const bool ok = (tid == 0) ? (p == -1) : (p >= 0 && p < tid);
@@ -309,7 +326,7 @@ static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, Tr
   }
 }
 
-// per-node kernel (verify_node.cu)
-int launch_verify_node(const VerifyArgs &args, cudaStream_t stream);
+// greedy per-node kernel (verify_node.cu)
+int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream);
 
 }  // namespace spec
