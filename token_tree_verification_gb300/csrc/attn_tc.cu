@@ -22,14 +22,16 @@
 //               when a row's max grows by more than 2^8), write P as bf16
 //               high and remainder parts to shared memory (P V then keeps
 //               about 16 significant bits of every weight).
-// Blocks of at most 64 rows (PACKED) put the remainder part in the unused
-// rows 64-127 of the same P operand: one 4-MMA P V pass per tile, the two
-// halves added from TMEM lanes r and r + 64 at the end (the warps of lanes
-// 64-127 mirror their rows' rescaling); the smaller Q block and P buffers
-// leave room for a 5-stage K/V ring.
-// Key splits merge through L2: each split writes its (m, l, O) rows to the
-// workspace and bumps the block's counter; the last split to arrive merges
-// them and resets the counter.
+// Blocks of at most 64 rows (PACKED) load their Q rows twice (rows 0-63 and
+// 64-127 of the MMA), so TMEM lanes r and r + 64 both hold S row r: four
+// threads per row spread the softmax over all four SM sub-partitions, and
+// the remainder part of P goes to P rows 64-127, so one 4-MMA P V pass per
+// tile leaves the high part in lanes 0-63 and the remainder in 64-127 (added
+// at the end).  The single P operand leaves room for a 4-stage K/V ring.
+// Outputs leave through a shared-memory staging buffer so global stores are
+// coalesced.  Key splits merge through L2: each split writes its (m, l, O)
+// rows to the workspace and bumps the block's counter; the last split to
+// arrive merges them and resets the counter.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -45,11 +47,12 @@ constexpr float kRescaleLog2 = 8.f;
 
 template <int D, bool PACKED>
 struct TcCfg {
-  static constexpr int kStages = PACKED ? 5 : 3;
+  static constexpr int kStages = PACKED ? 4 : 3;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kQRows = PACKED ? kTcRows / 2 : kTcRows;  // rows the TMA loads
-  static constexpr int kQBoxBytes = kQRows * 128;
-  static constexpr int kQBytes = kQRows * D * 2;
+  static constexpr int kLoadRows = PACKED ? kTcRows / 2 : kTcRows;  // rows one Q load brings
+  static constexpr int kQLoadBytes = kLoadRows * 128;
+  static constexpr int kQChunkBytes = kTcRows * 128;   // smem per 64-dim chunk of the Q block
+  static constexpr int kQBytes = kTcRows * D * 2;
   static constexpr int kKVBoxBytes = kKeyTile * 128;
   static constexpr int kTileBytes = kKeyTile * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;
@@ -59,17 +62,26 @@ struct TcCfg {
   static constexpr int kOffKV = kQBytes;
   static constexpr int kOffP = kOffKV + kStages * kStageBytes;
   static constexpr int kSmem = kOffP + 2 * kPParts * kPBytes + 1024;
+  static constexpr int kParts = PACKED ? 4 : 2;             // threads per row (key parts)
+  static constexpr int kKeysPer = kKeyTile / kParts;        // keys per thread per tile
+  static constexpr int kStage = D + 4;                      // floats per staged output row
   static constexpr uint32_t kTmemCols = 256;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 128;
   static_assert(!PACKED || kTcRows / 2 * D * 4 <= 2 * kPParts * kPBytes,
                 "packed remainder exchange fits the P buffers");
-  static_assert(kSmem <= 227 * 1024 - 4096, "shared memory budget");
+  static_assert(kTcRows * kStage * 4 <= kStages * kStageBytes, "output staging fits the K/V ring");
+  static_assert(kSmem <= 227 * 1024 - 8192, "shared memory budget");
 };
 
-// Workspace record of one split: O rows (fp32, unnormalised) then m and l.
+constexpr int kTcMaxSplits = 8;
+
+// Workspace record of one split: per row, O (fp32, unnormalised) then m and
+// l, padded to a 16-byte multiple.
 template <int D>
-__host__ __device__ constexpr int tc_partial_floats() { return kTcRows * (D + 2); }
+__host__ __device__ constexpr int tc_row_floats() { return D + 4; }
+template <int D>
+__host__ __device__ constexpr int tc_partial_floats() { return kTcRows * tc_row_floats<D>(); }
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
                                             int c1, int c2) {
@@ -91,12 +103,14 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmv, uint32_t *counters, float *partials) {
   using C = TcCfg<D, PACKED>;
   constexpr int NS = C::kStages;
+  constexpr int KP = C::kKeysPer;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
   __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p[2], bar_o[2];
   __shared__ uint32_t s_tmem;
-  __shared__ float x_max[2][2][kTcRows];   // [tile parity][key half][row]
-  __shared__ float x_l[2][kTcRows];
+  __shared__ float x_max[2][C::kParts][kTcRows];   // [tile parity][key part][row]
+  __shared__ float x_l[C::kParts][kTcRows];
+  __shared__ float s_ml[kTcRows][2];               // per row: reference max, sum
   __shared__ int s_timeout, s_last;
 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -152,20 +166,22 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
 
-  // softmax-thread geometry (warps 2..9): TMEM lane r, key / column half
+  // softmax-thread geometry (warps 2..9).  TMEM lane r = 32 * quad + lane.
+  // Not packed: row r, two threads (key halves) per row.  Packed: the Q block
+  // is loaded twice, so lanes r and r + 64 hold the same S row; four threads
+  // (key quarters) per row, and lanes 64-127 accumulate the remainder part of
+  // P V.  Each thread owns one half of its lane's O columns.
   const int quad = warp & 3;
   const int half = (warp - 2) >> 2;
-  const int r = quad * 32 + lane;
-  // the score row this thread follows: its own, or (lanes 64-127 when
-  // packed) the row whose remainder part it accumulates
-  const bool helper = PACKED && quad >= 2;
-  const int srow = helper ? r - kTcRows / 2 : r;
+  const int part = PACKED ? ((quad >> 1) * 2 + half) : half;
+  const int srow = PACKED ? ((quad & 1) * 32 + lane) : (quad * 32 + lane);
   const bool row_ok = srow < rows_here;
-  const bool computes = warp >= 2 && !helper && quad * 32 < rows_here;   // reads S, writes P
-  const bool lanes_live = warp >= 2 && (quad & (PACKED ? 1 : 3)) * 32 < rows_here;
+  const bool lanes_live = warp >= 2 && (PACKED ? (quad & 1) : quad) * 32 < rows_here;
+  const bool lo_lane = PACKED && quad >= 2;          // holds the remainder part of P V
+  const bool owner = warp >= 2 && !lo_lane;          // assembles the row's final O half
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   float o_keep[D / 2];
-  float m_used = -INFINITY, l_half = 0.f, l_row = 0.f;
+  float m_used = -INFINITY, l_part = 0.f, l_row = 0.f;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -175,9 +191,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       tma_prefetch_desc(&tmv);
       mbar_arrive_expect_tx(&bar_q, C::kQBytes);
 #pragma unroll
-      for (int bx = 0; bx < C::kBoxes; ++bx)
-        tma_load_3d(smem + C::kOffQ + bx * C::kQBoxBytes, &tmq, &bar_q, bx * 64, g * a.G,
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_3d(smem + C::kOffQ + bx * C::kQChunkBytes, &tmq, &bar_q, bx * 64, g * a.G,
                     R.lo + row0 / a.G);
+        if (PACKED)  // the same 64 rows again into rows 64-127
+          tma_load_3d(smem + C::kOffQ + bx * C::kQChunkBytes + C::kQLoadBytes, &tmq, &bar_q,
+                      bx * 64, g * a.G, R.lo + row0 / a.G);
+      }
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
         if (i >= NS && !mbar_wait(&bar_empty[st], ((i / NS) - 1) & 1)) {
@@ -210,10 +230,8 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           const uint32_t kb = sb + C::kOffKV + st * C::kStageBytes;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            // Q rows past the loaded block (packed mode) read the next
-            // region: those S rows are padding and never read back.
             const uint64_t ad = tc::smem_desc_sw128(
-                sb + C::kOffQ + (ks >> 2) * C::kQBoxBytes + (ks & 3) * 32, 16, 1024);
+                sb + C::kOffQ + (ks >> 2) * C::kQChunkBytes + (ks & 3) * 32, 16, 1024);
             const uint64_t bd =
                 tc::smem_desc_sw128(kb + (ks >> 2) * C::kKVBoxBytes + (ks & 3) * 32, 16, 1024);
             tc::mma_bf16(tmem + C::kColS + (i & 1) * kKeyTile, ad, bd, idS, ks > 0);
@@ -227,12 +245,12 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
           const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPParts * C::kPBytes;
 #pragma unroll
-          for (int part = 0; part < C::kPParts; ++part) {
+          for (int pp = 0; pp < C::kPParts; ++pp) {
 #pragma unroll
             for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-              const uint64_t ad = tc::smem_desc_sw128(pb + part * C::kPBytes + kk * 32, 16, 1024);
+              const uint64_t ad = tc::smem_desc_sw128(pb + pp * C::kPBytes + kk * 32, 16, 1024);
               const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
-              tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | part | kk) != 0);
+              tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | pp | kk) != 0);
             }
           }
           tc::commit(&bar_o[j & 1]);
@@ -244,7 +262,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   } else {
     // ------------------------------------------------------------ softmax warps
     uint4 msk = make_uint4(0, 0, 0, 0);
-    if (computes && row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + r) / a.G), R.n);
+    if (lanes_live && row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + srow) / a.G), R.n);
     const float sl2 = a.scale_log2;
     bool ok = true;
     // A timed-out wait clears `ok` and later waits are skipped, but the loop
@@ -268,31 +286,39 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                                      (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      float s[32];
+      float s[KP];
       bool want = false;
-      if (computes) {
-        tc::ld32(trow + C::kColS + (i & 1) * kKeyTile + 32 * half, s);
+      if (lanes_live) {
+        const uint32_t scol = trow + C::kColS + (i & 1) * kKeyTile + KP * part;
+        if constexpr (KP == 32) {
+          tc::ld32(scol, *reinterpret_cast<float(*)[32]>(s));
+        } else {
+          tc::ld16(scol, *reinterpret_cast<float(*)[16]>(s));
+        }
         tc::wait_ld();
-        const int kbase = key0 + 32 * half;
-        if (kbase + 32 > R.L) {
+        const int kbase = key0 + KP * part;
+        if (kbase + KP > R.L) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < KP; ++j)
             if (!key_visible(kbase + j, R.L, R.keys, msk)) s[j] = -INFINITY;
         }
         float mt = s[0];
 #pragma unroll
-        for (int j = 1; j < 32; ++j) mt = fmaxf(mt, s[j]);
-        x_max[i & 1][half][r] = mt;
+        for (int j = 1; j < KP; ++j) mt = fmaxf(mt, s[j]);
+        x_max[i & 1][part][srow] = mt;
         want = row_ok && (mt * sl2 > m_used + kRescaleLog2);
       }
-      // one barrier: both halves' maxima are visible, and whether any row of
+      // one barrier: every part's maximum is visible, and whether any row of
       // the block moves its reference max
       const bool any_resc = named_bar_or(2, 32 * kTcSoftmaxWarps, want);
-      const float mt = (lanes_live && row_ok)
-                           ? fmaxf(x_max[i & 1][0][srow], x_max[i & 1][1][srow]) * sl2
-                           : -INFINITY;
-      const bool resc = row_ok && lanes_live && (mt > m_used + kRescaleLog2);
       if (any_resc) {
+        float mt = -INFINITY;
+        if (lanes_live && row_ok) {
+#pragma unroll
+          for (int q = 0; q < C::kParts; ++q) mt = fmaxf(mt, x_max[i & 1][q][srow]);
+          mt *= sl2;
+        }
+        const bool resc = row_ok && lanes_live && (mt > m_used + kRescaleLog2);
         const float m_new = resc ? mt : m_used;
         const float alpha = !resc ? 1.f : (m_used == -INFINITY ? 0.f : exp2f(m_used - m_new));
         if (i > 0 && lanes_live) {
@@ -312,20 +338,20 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           }
           tc::wait_st();
         }
-        l_half *= alpha;
+        l_part *= alpha;
         m_used = m_new;
       }
-      if (computes) {
+      if (lanes_live) {
         // the P buffer of this parity is free once the P V of tile i-2 is done
         if (ok && i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
         __syncwarp();
         const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
         uint8_t *pbuf = smem + C::kOffP + (i & 1) * C::kPParts * C::kPBytes;
-        uint8_t *prow_hi = pbuf + r * 128;
-        uint8_t *prow_lo = PACKED ? pbuf + (r + kTcRows / 2) * 128 : pbuf + C::kPBytes + r * 128;
+        uint8_t *prow_hi = pbuf + srow * 128;
+        uint8_t *prow_lo = PACKED ? pbuf + (srow + kTcRows / 2) * 128 : pbuf + C::kPBytes + srow * 128;
         float psum = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < KP / 8; ++cc) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -337,11 +363,11 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
             hi[e] = bf16x2_bits(h);
             lo[e] = bf16x2_bits(__floats2bfloat162_rn(p0 - hf.x, p1 - hf.y));
           }
-          const int off = ((4 * half + cc) ^ (r & 7)) << 4;   // (r + 64) & 7 == r & 7
+          const int off = (((KP / 8) * part + cc) ^ (srow & 7)) << 4;   // (srow + 64) & 7 == srow & 7
           *reinterpret_cast<uint4 *>(prow_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4 *>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        l_half += psum;
+        l_part += psum;
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -350,7 +376,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     if (!ok) s_timeout = 1;
     // ---- epilogue: O rows out of TMEM.  Every softmax warp waits for the
-    //      last P V before any thread reuses the P buffers.
+    //      last P V before any thread reuses the K/V ring or the P buffers.
     if (ntiles > 0) {
       if (ok && !mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) s_timeout = 1;
       __syncwarp();
@@ -368,55 +394,37 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         for (int e = 0; e < 32; ++e) o_keep[c * 32 + e] = o[e];
       }
     }
-    // packed: lanes r + 64 hold the remainder part of row r's P V
     float *xo = reinterpret_cast<float *>(smem + C::kOffP);   // [64 rows][D], P buffers are free
-    if (PACKED && helper && row_ok) {
+    if (PACKED && lo_lane && row_ok) {
 #pragma unroll
       for (int e = 0; e < D / 2; e += 4)
         *reinterpret_cast<float4 *>(xo + srow * D + half * (D / 2) + e) =
             make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
     }
-    if (!helper) x_l[half][r] = l_half;
+    if (warp >= 2) x_l[part][srow] = l_part;
     named_bar_sync(2, 32 * kTcSoftmaxWarps);
-    if (!helper) {
-      l_row = l_half + x_l[half ^ 1][r];
-      if (PACKED && row_ok) {
+    if (owner && row_ok) {
+#pragma unroll
+      for (int q = 0; q < C::kParts; ++q) l_row += x_l[q][srow];
+      if (PACKED) {
 #pragma unroll
         for (int e = 0; e < D / 2; e += 4) {
-          const float4 v = *reinterpret_cast<const float4 *>(xo + r * D + half * (D / 2) + e);
+          const float4 v = *reinterpret_cast<const float4 *>(xo + srow * D + half * (D / 2) + e);
           o_keep[e] += v.x;
           o_keep[e + 1] += v.y;
           o_keep[e + 2] += v.z;
           o_keep[e + 3] += v.w;
         }
       }
-    }
-    if (!helper && row_ok && ntiles > 0 && CS == 1) {
-      const float inv = 1.f / l_row;
-      const int rr = row0 + r;
-      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
-                           (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D +
-                           half * (D / 2);
+      // stage the row for coalesced stores (the K/V ring is free)
+      float *stg = reinterpret_cast<float *>(smem + C::kOffKV) + srow * C::kStage + half * (D / 2);
 #pragma unroll
-      for (int q8 = 0; q8 < D / 16; ++q8) {
-        uint4 pk;
-        pk.x = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 0] * inv, o_keep[q8 * 8 + 1] * inv));
-        pk.y = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 2] * inv, o_keep[q8 * 8 + 3] * inv));
-        pk.z = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 4] * inv, o_keep[q8 * 8 + 5] * inv));
-        pk.w = bf16x2_bits(__floats2bfloat162_rn(o_keep[q8 * 8 + 6] * inv, o_keep[q8 * 8 + 7] * inv));
-        *reinterpret_cast<uint4 *>(dst + q8 * 8) = pk;
+      for (int e = 0; e < D / 2; e += 4)
+        *reinterpret_cast<float4 *>(stg + e) = make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
+      if (half == 0) {
+        s_ml[srow][0] = ntiles > 0 ? m_used : -INFINITY;
+        s_ml[srow][1] = l_row;
       }
-    }
-    if (CS > 1 && !helper && row_ok) {
-      // this split's rows to the workspace: O half-row, then m and l
-      float *rec = partials + (static_cast<size_t>(unit) * CS + split) * tc_partial_floats<D>() +
-                   static_cast<size_t>(r) * (D + 2);
-#pragma unroll
-      for (int e = 0; e < D / 2; e += 2)
-        __stcg(reinterpret_cast<float2 *>(rec + half * (D / 2) + e), make_float2(o_keep[e], o_keep[e + 1]));
-      if (half == 0) __stcg(reinterpret_cast<float2 *>(rec + D),
-                            make_float2(ntiles > 0 ? m_used : -INFINITY, l_row));
-      __threadfence();
     }
   }
 
@@ -429,49 +437,106 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     tc::tmem_dealloc(tmem, C::kTmemCols);
   }
   if (s_timeout && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
-  if (CS > 1) {
-    // ---- split merge through L2: the last split of this block merges
-    if (tid == 0) {
-      const uint32_t prev = atomicAdd(counters + unit, 1u);
-      s_last = (static_cast<int>(prev) == CS - 1) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const float *base = partials + static_cast<size_t>(unit) * CS * tc_partial_floats<D>();
-    const int nvec = rows_here * (D / 4);
-    for (int idx = tid; idx < nvec; idx += kTcThreads) {
-      const int lr = idx / (D / 4);
-      const int c4 = idx % (D / 4);
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < CS; ++s2)
-        M = fmaxf(M, __ldcg(base + s2 * tc_partial_floats<D>() + lr * (D + 2) + D));
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float L = 0.f;
-      for (int s2 = 0; s2 < CS; ++s2) {
-        const float *rec = base + s2 * tc_partial_floats<D>() + lr * (D + 2);
-        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(rec + D));
-        if (ml.x == -INFINITY) continue;
-        const float w = exp2f(ml.x - M);
-        L += w * ml.y;
-        const float2 v0 = __ldcg(reinterpret_cast<const float2 *>(rec + c4 * 4));
-        const float2 v1 = __ldcg(reinterpret_cast<const float2 *>(rec + c4 * 4 + 2));
-        acc.x += w * v0.x;
-        acc.y += w * v0.y;
-        acc.z += w * v1.x;
-        acc.w += w * v1.y;
-      }
-      const float inv = 1.f / L;
+  const float *stg = reinterpret_cast<const float *>(smem + C::kOffKV);
+  if (CS == 1) {
+    // ---- final rows, 8 bf16 per thread, consecutive threads on one row
+    const int nv = rows_here * (D / 8);
+    for (int idx = tid; idx < nv; idx += kTcThreads) {
+      const int lr = idx / (D / 8), c8 = idx % (D / 8);
+      const float inv = 1.f / s_ml[lr][1];
+      const float4 v0 = *reinterpret_cast<const float4 *>(stg + lr * C::kStage + c8 * 8);
+      const float4 v1 = *reinterpret_cast<const float4 *>(stg + lr * C::kStage + c8 * 8 + 4);
+      uint4 pk;
+      pk.x = bf16x2_bits(__floats2bfloat162_rn(v0.x * inv, v0.y * inv));
+      pk.y = bf16x2_bits(__floats2bfloat162_rn(v0.z * inv, v0.w * inv));
+      pk.z = bf16x2_bits(__floats2bfloat162_rn(v1.x * inv, v1.y * inv));
+      pk.w = bf16x2_bits(__floats2bfloat162_rn(v1.z * inv, v1.w * inv));
       const int rr = row0 + lr;
-      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
-                           (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + c4 * 4;
-      uint2 pk;
-      pk.x = bf16x2_bits(__floats2bfloat162_rn(acc.x * inv, acc.y * inv));
-      pk.y = bf16x2_bits(__floats2bfloat162_rn(acc.z * inv, acc.w * inv));
-      *reinterpret_cast<uint2 *>(dst) = pk;
+      *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) +
+                                 (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D +
+                                 c8 * 8) = pk;
     }
-    if (tid == 0) counters[unit] = 0u;  // ready for the next call
+    return;
   }
+  // ---- key splits: this split's rows to the workspace, coalesced
+  {
+    float *mine = partials + (static_cast<size_t>(unit) * CS + split) * tc_partial_floats<D>();
+    constexpr int kV4 = D / 4 + 1;   // float4 per record row: O, then (m, l, 0, 0)
+    const int nv = rows_here * kV4;
+    for (int idx = tid; idx < nv; idx += kTcThreads) {
+      const int lr = idx / kV4, c4 = idx % kV4;
+      const float4 v = c4 < D / 4 ? *reinterpret_cast<const float4 *>(stg + lr * C::kStage + c4 * 4)
+                                  : make_float4(s_ml[lr][0], s_ml[lr][1], 0.f, 0.f);
+      __stcg(reinterpret_cast<float4 *>(mine + lr * tc_row_floats<D>()) + c4, v);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(counters + unit, 1u);
+    s_last = (static_cast<int>(prev) == CS - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // ---- the last split merges all splits' rows of this block
+  const float *base = partials + static_cast<size_t>(unit) * CS * tc_partial_floats<D>();
+  // task = (row, eighth of the columns); every split's loads are issued
+  // before any is used, so a task costs about one L2 round trip
+  constexpr int kE = D / 8;
+  const int ntask = rows_here * 8;
+  for (int task = tid; task < ntask; task += kTcThreads) {
+    const int lr = task >> 3;
+    const int col0 = (task & 7) * kE;
+    float2 ml[kTcMaxSplits];
+    float4 ov[kTcMaxSplits][kE / 4];
+#pragma unroll
+    for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
+      if (s2 < CS) {
+        const float *rec = base + s2 * tc_partial_floats<D>() + lr * tc_row_floats<D>();
+        ml[s2] = __ldcg(reinterpret_cast<const float2 *>(rec + D));
+#pragma unroll
+        for (int q4 = 0; q4 < kE / 4; ++q4)
+          ov[s2][q4] = __ldcg(reinterpret_cast<const float4 *>(rec + col0) + q4);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s2 = 0; s2 < kTcMaxSplits; ++s2)
+      if (s2 < CS) M = fmaxf(M, ml[s2].x);
+    float acc[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) acc[e] = 0.f;
+    float L = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
+      if (s2 < CS && ml[s2].x != -INFINITY) {
+        const float w = exp2f(ml[s2].x - M);
+        L += w * ml[s2].y;
+#pragma unroll
+        for (int q4 = 0; q4 < kE / 4; ++q4) {
+          acc[4 * q4 + 0] += w * ov[s2][q4].x;
+          acc[4 * q4 + 1] += w * ov[s2][q4].y;
+          acc[4 * q4 + 2] += w * ov[s2][q4].z;
+          acc[4 * q4 + 3] += w * ov[s2][q4].w;
+        }
+      }
+    }
+    const float inv = 1.f / L;
+    const int rr = row0 + lr;
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
+                         (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + col0;
+#pragma unroll
+    for (int q8 = 0; q8 < kE / 8; ++q8) {
+      uint4 pk;
+      pk.x = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 0] * inv, acc[q8 * 8 + 1] * inv));
+      pk.y = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 2] * inv, acc[q8 * 8 + 3] * inv));
+      pk.z = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 4] * inv, acc[q8 * 8 + 5] * inv));
+      pk.w = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 6] * inv, acc[q8 * 8 + 7] * inv));
+      *reinterpret_cast<uint4 *>(dst + q8 * 8) = pk;
+    }
+  }
+  if (tid == 0) counters[unit] = 0u;  // ready for the next call
 }
 
 // Split plan shared by the launcher and the workspace query: the split count
@@ -485,7 +550,7 @@ void plan_attn_tc(int B, int T, int Hkv, int G, int max_prefix, int num_sms, int
   const long long units = static_cast<long long>(rowblocks) * B * Hkv;
   int cs = 1;
   long long best = -1;
-  for (int c = 1; c <= 16; c *= 2) {
+  for (int c = 1; c <= kTcMaxSplits; c *= 2) {
     if (c > 1 && tiles_max < 2 * c) break;
     const long long waves = (units * c + num_sms - 1) / num_sms;
     const long long cost = waves * ((tiles_max + c - 1) / c) + (c > 1 ? 2 : 0);
@@ -504,7 +569,7 @@ size_t attn_tc_workspace_bytes(int B, int T, int Hkv, int G, int D, int max_pref
   if (cs == 1) return 0;
   const size_t units = static_cast<size_t>(rowblocks) * B * Hkv;
   const size_t counters = (units * sizeof(uint32_t) + 255) & ~size_t(255);
-  const size_t rec = static_cast<size_t>(kTcRows) * (D + 2) * sizeof(float);
+  const size_t rec = static_cast<size_t>(kTcRows) * (D + 4) * sizeof(float);
   return counters + units * cs * rec;
 }
 

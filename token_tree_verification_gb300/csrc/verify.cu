@@ -35,6 +35,7 @@ struct RoundScratch {
   float w[2][kVWarps][2];
   int wi[2][kVWarps];
 };
+static_assert(kVWarps == 32, "warp 0 combines one partial per lane");
 
 // Cluster all-gather slots: every CTA pushes its partials into slot [rank]
 // of every peer with remote stores, so after one cluster barrier all values
@@ -43,27 +44,37 @@ struct Gather {
   float v[2][kMaxCS][4];
 };
 
-__device__ __forceinline__ void gather_push(Gather &gx, int parity, int rank, int CS, float4 val) {
-  const int r = threadIdx.x;  // threads 0..CS-1 each push to one peer
-  if (r < CS) st_peer_f32x4(peer_addr(&gx.v[parity][rank][0], r), val);
+// Barrier of one node's CTA group: the cluster barrier when the group spans
+// several CTAs, else the CTA barrier.
+__device__ __forceinline__ void group_sync(int CS) {
+  if (CS > 1) cluster_sync_all();
+  else __syncthreads();
 }
 
-// Sum `x` over the CTA and then over the cluster.  Returns the cluster total
-// (identical in every CTA: partials are added in rank order) and, in `parts`,
-// the per-CTA totals.  One __syncthreads and one cluster barrier.
+// Publish this CTA's float4 to slot [rank] of every CTA of the group.
+__device__ __forceinline__ void gather_put(Gather &gx, int parity, int rank, int CS, int lane,
+                                           float4 val) {
+  if (lane < CS) {
+    if (CS > 1) st_peer_f32x4(peer_addr(&gx.v[parity][rank][0], lane), val);
+    else *reinterpret_cast<float4 *>(&gx.v[parity][0][0]) = val;
+  }
+}
+
+// Sum `x` over the CTA (warp shuffles, then warp 0 over the 32 warp
+// partials) and over the group.  Returns the group total (identical in every
+// CTA: partials are added in rank order) and, in `parts`, the per-CTA totals.
+// One __syncthreads and one group barrier.
 __device__ float cluster_round_sum(float x, RoundScratch &rs, Gather &gx, int parity, int rank,
                                    int CS, float *parts) {
   x = warp_sum(x);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) rs.w[parity][w][0] = x;
   __syncthreads();
-  if (threadIdx.x < CS) {
-    float t = 0.f;
-#pragma unroll
-    for (int i = 0; i < kVWarps; ++i) t += rs.w[parity][i][0];
-    gather_push(gx, parity, rank, CS, make_float4(t, 0.f, 0.f, 0.f));
+  if (w == 0) {
+    const float v = warp_sum(rs.w[parity][l][0]);
+    gather_put(gx, parity, rank, CS, l, make_float4(v, 0.f, 0.f, 0.f));
   }
-  cluster_sync_all();
+  group_sync(CS);
   float tot = 0.f;
   for (int r = 0; r < CS; ++r) {
     const float v = gx.v[parity][r][0];
@@ -79,8 +90,8 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
   __shared__ RoundScratch rs;
   __shared__ __align__(16) Gather gx;
   __shared__ TreeSmem ts;
-  __shared__ int s_pick;
-  __shared__ float s_cb[2];
+  __shared__ int s_pick, s_pickw;
+  __shared__ float s_cb[2], s_before;
   __shared__ __align__(8) uint64_t bars[2];
 
   const int CS = static_cast<int>(cluster_size());
@@ -142,12 +153,11 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
         rs.wi[0][w_id] = am.i;
       }
       __syncthreads();
-      if (tid < CS) {
-        ArgMax r{rs.w[0][0][0], rs.wi[0][0]};
-        for (int i = 1; i < kVWarps; ++i) r = better(r, ArgMax{rs.w[0][i][0], rs.wi[0][i]});
-        gather_push(gx, 0, rank, CS, make_float4(r.v, __int_as_float(r.i), 0.f, 0.f));
+      if (w_id == 0) {
+        const ArgMax r = warp_argmax(ArgMax{rs.w[0][lane][0], rs.wi[0][lane]});
+        gather_put(gx, 0, rank, CS, lane, make_float4(r.v, __int_as_float(r.i), 0.f, 0.f));
       }
-      cluster_sync_all();
+      group_sync(CS);
       if (rank == 0 && tid == 0) {
         ArgMax g{-INFINITY, 0x7fffffff};
         for (int r = 0; r < CS; ++r) g = better(g, ArgMax{gx.v[0][r][0], __float_as_int(gx.v[0][r][1])});
@@ -190,20 +200,15 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
         s_pair[w_id][3] = wsd;
       }
       __syncthreads();
-      if (tid < CS) {
-        float cm = -INFINITY, cmd = -INFINITY;
-        for (int i = 0; i < kVWarps; ++i) {
-          cm = fmaxf(cm, s_pair[i][0]);
-          cmd = fmaxf(cmd, s_pair[i][2]);
-        }
-        float cs = 0.f, csd = 0.f;
-        for (int i = 0; i < kVWarps; ++i) {
-          if (s_pair[i][1] > 0.f) cs += s_pair[i][1] * fast_exp2((s_pair[i][0] - cm) * l2s);
-          if (s_pair[i][3] > 0.f) csd += s_pair[i][3] * fast_exp2((s_pair[i][2] - cmd) * l2s);
-        }
-        gather_push(gx, parity, rank, CS, make_float4(cm, cs, cmd, csd));
+      if (w_id == 0) {
+        const float pm = s_pair[lane][0], ps = s_pair[lane][1];
+        const float qm = s_pair[lane][2], qs = s_pair[lane][3];
+        const float cm = warp_max(pm), cmd = warp_max(qm);
+        const float cs = warp_sum(ps > 0.f ? ps * fast_exp2((pm - cm) * l2s) : 0.f);
+        const float csd = warp_sum(qs > 0.f ? qs * fast_exp2((qm - cmd) * l2s) : 0.f);
+        gather_put(gx, parity, rank, CS, lane, make_float4(cm, cs, cmd, csd));
       }
-      cluster_sync_all();
+      group_sync(CS);
       float Ml = -INFINITY, Md = -INFINITY;
       float4 part[kMaxCS];
       for (int r = 0; r < CS; ++r) {
@@ -220,6 +225,11 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
       }
       for (int r = 0; r < CS; ++r) kept[r] /= Sp;  // chunk sums of p
       parity ^= 1;
+      // the children's p(x) and q(x), in parallel (read by the chain below)
+      if (tid < k) {
+        ts.cP[tid] = precise_prob(ts.cP[tid], Ml, T_, iT, Sp);
+        ts.cQ[tid] = precise_prob(ts.cQ[tid], Md, T_, iT, Sq);
+      }
       // p(v), q(v) for this thread's elements
       const float scale_l = ml == -INFINITY ? 0.f : fast_exp2((ml - Ml) * l2s) / Sp;
       const float scale_d = (need_draft && md != -INFINITY) ? fast_exp2((md - Md) * l2s) / Sq : 0.f;
@@ -228,12 +238,13 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
         if (need_draft) drow[i] *= scale_d;
       }
 
+      __syncthreads();  // the children's probabilities are in shared memory
       // ---- V2: the children's accept tests, one reduction per rejection
       float c_prev = 0.f, W_prev = 1.f;
       for (int j = 0; j < k; ++j) {
         const int ch = ts.child[j];
-        const float P = precise_prob(ts.cP[j], Ml, T_, iT, Sp);
-        const float Q = precise_prob(ts.cQ[j], Md, T_, iT, Sq);
+        const float P = ts.cP[j];
+        const float Q = ts.cQ[j];
         const float alpha = Q > 0.f ? fminf(1.f, fmaxf(0.f, fmaf(-c_prev, Q, P)) / (W_prev * Q)) : 1.f;
         if (rank == 0 && tid == 0) {
           const float uu = ts.cU[j];
@@ -287,15 +298,26 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
         if (lane == 0) rs.w[parity][w_id][1] = ws;
         if (tid == 0) s_pick = -1;
         __syncthreads();
-        float before = prefix;
-        int pick_w = -1;
-        {
-          float run = prefix;
-          for (int i = 0; i < kVWarps; ++i) {
-            if (run + rs.w[parity][i][1] > target) { pick_w = i; before = run; break; }
-            run += rs.w[parity][i][1];
+        if (w_id == 0) {
+          // inclusive scan of the warp partials, first one passing the target
+          const float v = rs.w[parity][lane][1];
+          float inc = v;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          const uint32_t hit = __ballot_sync(0xffffffffu, prefix + inc > target);
+          const int L = hit ? __ffs(hit) - 1 : -1;
+          const float before_l = __shfl_sync(0xffffffffu, prefix + inc - v, L < 0 ? 0 : L);
+          if (lane == 0) {
+            s_pickw = L;
+            s_before = before_l;
           }
         }
+        __syncthreads();
+        const int pick_w = s_pickw;
+        const float before = s_before;
         if (pick_w == w_id) {
           float run = before;
           for (int base = s0; base < s1; base += 32) {
@@ -342,7 +364,7 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
         }
       }
     }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its exchange slots
+    group_sync(CS);  // no CTA leaves while a peer may still read its exchange slots
   } else if (rank == 0 && tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }
