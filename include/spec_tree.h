@@ -85,14 +85,10 @@ int spec_build_tree_mask(const int32_t *parents, const int32_t *tree_offsets, in
                          uint32_t *mask, int32_t *depth, int32_t *status, void *stream);
 
 /*
- * Bytes of scratch spec_tree_attn needs for these sizes (0 when no key split
- * is needed).  When the keys of a query block are split across CTAs, every
- * split writes its partial softmax state (running max, sum, unnormalised
- * output rows in fp32) to the workspace and the last split of the block
- * merges them.  The workspace must be zero-filled before its FIRST use; every
- * call leaves its arrival counters at zero again, so one buffer serves later
- * calls on the same stream.  Two calls that run at the same time need two
- * workspaces.  The size depends on the current device's SM count.
+ * Bytes of scratch spec_tree_attn needs for these sizes.  The kernels merge
+ * their key splits on chip (the splits of a query block form one thread-block
+ * cluster), so this is 0; the argument stays part of the ABI so a future
+ * split layout needs no signature change.
  */
 size_t spec_tree_attn_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_prefix);
 
@@ -122,13 +118,12 @@ size_t spec_tree_attn_workspace_size(int B, int T, int Hq, int Hkv, int D, int m
  *                key splits (a larger value is safe, only slower)
  *   prefix_lens  [B] int32 (L_b)
  *   mask         [T][4] uint32 from spec_build_tree_mask (bits >= N_b ignored)
- *   workspace    >= spec_tree_attn_workspace_size() bytes, 16-byte aligned,
- *                zero-filled before first use; may be NULL when that size is 0
+ *   workspace    may be NULL while spec_tree_attn_workspace_size() is 0
  * Accumulation is fp32; the bf16 path splits every softmax weight into a bf16
  * high part and a bf16 remainder for the P·V product (about 16 significant
  * bits per weight) and rounds o to bf16.
  * Errors on the device: SPEC_ERR_TREE_TOO_LARGE, SPEC_ERR_PREFIX_RANGE,
- * SPEC_ERR_TIMEOUT.  Host errors include SPEC_ERR_WORKSPACE.
+ * SPEC_ERR_TIMEOUT.
  */
 int spec_tree_attn(const void *q, const void *k_cache, const void *v_cache, void *o, int dtype,
                    int B, int T, int Hq, int Hkv, int D, int S_cap, int max_prefix,

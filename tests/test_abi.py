@@ -41,10 +41,7 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    w7 = lib.spec_tree_attn_workspace_size(1, 64, 32, 32, 128, 2048)
-    assert w7 > 0 and w7 % 256 == 0                          # key splits merge through L2
-    assert lib.spec_tree_attn_workspace_size(1, 8, 4, 4, 64, 0) == 0   # one tile: no split
-    assert lib.spec_tree_attn_workspace_size(1, 64, 32, 32, 96, 2048) == 0  # unsupported D
+    assert lib.spec_tree_attn_workspace_size(1, 64, 32, 32, 128, 2048) == 0  # merged on chip
     s1 = lib.spec_tree_verify_workspace_size(1, 64, 32000)
     s2 = lib.spec_tree_verify_workspace_size(16, 900, 32000)
     assert s1 > 0 and s2 > s1 and s2 % 256 == 0

@@ -78,7 +78,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int c16) {
 // (the Q map's box then holds 64 rows).
 int launch_attn_tc(const AttnArgs &args, int max_prefix, int T, const CUtensorMap &tmq,
                    const CUtensorMap &tmk, const CUtensorMap &tmv, bool packed, int num_sms,
-                   void *workspace, size_t ws_bytes, cudaStream_t stream);
-size_t attn_tc_workspace_bytes(int B, int T, int Hkv, int G, int D, int max_prefix, int num_sms);
+                   cudaStream_t stream);
 
 }  // namespace spec

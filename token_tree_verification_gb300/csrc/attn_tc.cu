@@ -29,9 +29,11 @@
 // tile leaves the high part in lanes 0-63 and the remainder in 64-127 (added
 // at the end).  The single P operand leaves room for a 4-stage K/V ring.
 // Outputs leave through a shared-memory staging buffer so global stores are
-// coalesced.  Key splits merge through L2: each split writes its (m, l, O)
-// rows to the workspace and bumps the block's counter; the last split to
-// arrive merges them and resets the counter.
+// coalesced.  The key splits of a block form one thread-block cluster: each
+// split stages its (m, l, O) rows in shared memory and, after a cluster
+// barrier, merges its share of the rows by reading every peer's staging
+// through distributed shared memory (a cluster stays on one die, so no
+// cross-die L2 round trip is involved).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -65,9 +67,10 @@ struct TcCfg {
   static constexpr int kParts = PACKED ? 4 : 2;             // threads per row (key parts)
   static constexpr int kKeysPer = kKeyTile / kParts;        // keys per thread per tile
   static constexpr int kStage = D + 4;                      // floats per staged output row
-  static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColO = 128;
+  static constexpr int kSBufs = 3;                          // S tiles in flight in TMEM
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;                      // S buffers: 3 x 64 columns
+  static constexpr uint32_t kColO = 256;                    // O: D columns
   static_assert(!PACKED || kTcRows / 2 * D * 4 <= 2 * kPParts * kPBytes,
                 "packed remainder exchange fits the P buffers");
   static_assert(kTcRows * kStage * 4 <= kStages * kStageBytes, "output staging fits the K/V ring");
@@ -76,12 +79,7 @@ struct TcCfg {
 
 constexpr int kTcMaxSplits = 8;
 
-// Workspace record of one split: per row, O (fp32, unnormalised) then m and
-// l, padded to a 16-byte multiple.
-template <int D>
-__host__ __device__ constexpr int tc_row_floats() { return D + 4; }
-template <int D>
-__host__ __device__ constexpr int tc_partial_floats() { return kTcRows * tc_row_floats<D>(); }
+
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
                                             int c1, int c2) {
@@ -100,28 +98,27 @@ template <int D, bool PACKED>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, uint32_t *counters, float *partials) {
+                    const __grid_constant__ CUtensorMap tmv) {
   using C = TcCfg<D, PACKED>;
   constexpr int NS = C::kStages;
   constexpr int KP = C::kKeysPer;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
-  __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p[2], bar_o[2];
+  __shared__ __align__(8) uint64_t bar_q, bar_s[3], bar_p[2], bar_o[2];
   __shared__ uint32_t s_tmem;
   __shared__ float x_max[2][C::kParts][kTcRows];   // [tile parity][key part][row]
   __shared__ float x_l[C::kParts][kTcRows];
   __shared__ float s_ml[kTcRows][2];               // per row: reference max, sum
-  __shared__ int s_timeout, s_last;
+  __shared__ int s_timeout;
 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_addr(smem);
-  const int CS = static_cast<int>(gridDim.x);
+  const int CS = static_cast<int>(gridDim.x);   // the key splits of a block form one cluster
   const int split = static_cast<int>(blockIdx.x);
   const int rb = blockIdx.y;
   const int b = blockIdx.z / a.Hkv;
   const int g = blockIdx.z % a.Hkv;
-  const int unit = blockIdx.z * gridDim.y + blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const ReqGeom R = request_geometry(a, b);
@@ -129,11 +126,11 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const int row0 = rb * kTcRows;
   if (R.err) {
     if (tid == 0 && split == 0 && rb == 0 && g == 0) report(a.status, b, R.err);
-    return;  // uniform across the splits of this block: none touches the counter
+    return;  // uniform across the cluster (same request)
   }
-  if (row0 >= rows_total) return;  // uniform across the splits of this block
+  if (row0 >= rows_total) return;  // uniform across the cluster (same row block)
   const int rows_here = min(kTcRows, rows_total - row0);
-  if (PACKED && rows_here > kTcRows / 2) {  // launch contract broken: never expected
+  if (PACKED && rows_here > kTcRows / 2) {  // launch contract broken: uniform, never expected
     if (tid == 0) report(a.status, b, SPEC_ERR_SHAPE);
     return;
   }
@@ -148,14 +145,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       mbar_init(&bar_empty[s], 1);
     }
     mbar_init(&bar_q, 1);
+    for (int j = 0; j < 3; ++j) mbar_init(&bar_s[j], 1);
     for (int j = 0; j < 2; ++j) {
-      mbar_init(&bar_s[j], 1);
       mbar_init(&bar_p[j], kTcSoftmaxWarps);
       mbar_init(&bar_o[j], 1);
     }
     fence_barrier_init();
     s_timeout = 0;
-    s_last = 0;
   }
   if (warp == 1) {
     tc::tmem_alloc(&s_tmem, C::kTmemCols);
@@ -222,40 +218,44 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
       bool ok = mbar_wait(&bar_q, 0);
       tc::fence_after_sync();
-      for (int i = 0; ok && i <= ntiles; ++i) {
-        if (i < ntiles) {
-          const int st = i % NS;
-          if (!mbar_wait(&bar_full[st], (i / NS) & 1)) { ok = false; break; }
-          tc::fence_after_sync();
-          const uint32_t kb = sb + C::kOffKV + st * C::kStageBytes;
+      // S_i into TMEM buffer i % 3; buffer reuse for tile i + 3 needs P_i
+      // (the softmax has read S_i).  Order: S_0..S_2, then per tile j:
+      // P_j ready -> P_j V_j, S_{j+3}.
+      auto issue_s = [&](int i) -> bool {
+        const int st = i % NS;
+        if (!mbar_wait(&bar_full[st], (i / NS) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t kb = sb + C::kOffKV + st * C::kStageBytes;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t ad = tc::smem_desc_sw128(
-                sb + C::kOffQ + (ks >> 2) * C::kQChunkBytes + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                tc::smem_desc_sw128(kb + (ks >> 2) * C::kKVBoxBytes + (ks & 3) * 32, 16, 1024);
-            tc::mma_bf16(tmem + C::kColS + (i & 1) * kKeyTile, ad, bd, idS, ks > 0);
-          }
-          tc::commit(&bar_s[i & 1]);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t ad = tc::smem_desc_sw128(
+              sb + C::kOffQ + (ks >> 2) * C::kQChunkBytes + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd =
+              tc::smem_desc_sw128(kb + (ks >> 2) * C::kKVBoxBytes + (ks & 3) * 32, 16, 1024);
+          tc::mma_bf16(tmem + C::kColS + (i % C::kSBufs) * kKeyTile, ad, bd, idS, ks > 0);
         }
-        if (i >= 1) {
-          const int j = i - 1, st = j % NS;
-          if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1)) { ok = false; break; }
-          tc::fence_after_sync();
-          const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
-          const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPParts * C::kPBytes;
+        tc::commit(&bar_s[i % C::kSBufs]);
+        return true;
+      };
+      for (int i = 0; ok && i < C::kSBufs && i < ntiles; ++i) ok = issue_s(i);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int st = j % NS;
+        if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
+        const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPParts * C::kPBytes;
 #pragma unroll
-          for (int pp = 0; pp < C::kPParts; ++pp) {
+        for (int pp = 0; pp < C::kPParts; ++pp) {
 #pragma unroll
-            for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-              const uint64_t ad = tc::smem_desc_sw128(pb + pp * C::kPBytes + kk * 32, 16, 1024);
-              const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
-              tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | pp | kk) != 0);
-            }
+          for (int kk = 0; kk < kKeyTile / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc_sw128(pb + pp * C::kPBytes + kk * 32, 16, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
+            tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | pp | kk) != 0);
           }
-          tc::commit(&bar_o[j & 1]);
-          tc::commit(&bar_empty[st]);
         }
+        tc::commit(&bar_o[j & 1]);
+        tc::commit(&bar_empty[st]);
+        if (j + C::kSBufs < ntiles) ok = issue_s(j + C::kSBufs);
       }
       if (!ok) s_timeout = 1;
     }
@@ -268,7 +268,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     // A timed-out wait clears `ok` and later waits are skipped, but the loop
     // runs to the end so every softmax warp meets every named barrier.
     for (int i = 0; i < ntiles; ++i) {
-      if (ok && !mbar_wait(&bar_s[i & 1], (i >> 1) & 1)) ok = false;
+      if (ok && !mbar_wait(&bar_s[i % C::kSBufs], (i / C::kSBufs) & 1)) ok = false;
       __syncwarp();
       tc::fence_after_sync();
       const int key0 = (t0 + i) * kKeyTile;
@@ -289,7 +289,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       float s[KP];
       bool want = false;
       if (lanes_live) {
-        const uint32_t scol = trow + C::kColS + (i & 1) * kKeyTile + KP * part;
+        const uint32_t scol = trow + C::kColS + (i % C::kSBufs) * kKeyTile + KP * part;
         if constexpr (KP == 32) {
           tc::ld32(scol, *reinterpret_cast<float(*)[32]>(s));
         } else {
@@ -458,89 +458,74 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     return;
   }
-  // ---- key splits: this split's rows to the workspace, coalesced
+  // ---- key splits: the CTAs of this block's cluster pull each other's
+  //      staged rows through distributed shared memory; CTA `split` merges
+  //      rows [split * rpr, (split + 1) * rpr)
+  cluster_sync_all();  // every split has staged its rows
   {
-    float *mine = partials + (static_cast<size_t>(unit) * CS + split) * tc_partial_floats<D>();
-    constexpr int kV4 = D / 4 + 1;   // float4 per record row: O, then (m, l, 0, 0)
-    const int nv = rows_here * kV4;
-    for (int idx = tid; idx < nv; idx += kTcThreads) {
-      const int lr = idx / kV4, c4 = idx % kV4;
-      const float4 v = c4 < D / 4 ? *reinterpret_cast<const float4 *>(stg + lr * C::kStage + c4 * 4)
-                                  : make_float4(s_ml[lr][0], s_ml[lr][1], 0.f, 0.f);
-      __stcg(reinterpret_cast<float4 *>(mine + lr * tc_row_floats<D>()) + c4, v);
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(counters + unit, 1u);
-    s_last = (static_cast<int>(prev) == CS - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // ---- the last split merges all splits' rows of this block
-  const float *base = partials + static_cast<size_t>(unit) * CS * tc_partial_floats<D>();
-  // task = (row, eighth of the columns); every split's loads are issued
-  // before any is used, so a task costs about one L2 round trip
-  constexpr int kE = D / 8;
-  const int ntask = rows_here * 8;
-  for (int task = tid; task < ntask; task += kTcThreads) {
-    const int lr = task >> 3;
-    const int col0 = (task & 7) * kE;
-    float2 ml[kTcMaxSplits];
-    float4 ov[kTcMaxSplits][kE / 4];
+    const int rpr = (rows_here + CS - 1) / CS;
+    const int r_begin = split * rpr, r_end = min(rows_here, r_begin + rpr);
+    constexpr int kE = D / 8;   // columns per task
+    const int ntask = max(0, r_end - r_begin) * 8;
+    for (int task = tid; task < ntask; task += kTcThreads) {
+      const int lr = r_begin + (task >> 3);
+      const int col0 = (task & 7) * kE;
+      float mls[kTcMaxSplits][2];
+      float4 ov[kTcMaxSplits][kE / 4];
+      // every peer's loads are issued before any is used
 #pragma unroll
-    for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
-      if (s2 < CS) {
-        const float *rec = base + s2 * tc_partial_floats<D>() + lr * tc_row_floats<D>();
-        ml[s2] = __ldcg(reinterpret_cast<const float2 *>(rec + D));
+      for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
+        if (s2 < CS) {
+          const uint32_t pml = peer_addr(&s_ml[lr][0], s2);
+          mls[s2][0] = ld_peer_f32(pml);
+          mls[s2][1] = ld_peer_f32(pml + 4);
+          const uint32_t prow = peer_addr(stg + lr * C::kStage + col0, s2);
 #pragma unroll
-        for (int q4 = 0; q4 < kE / 4; ++q4)
-          ov[s2][q4] = __ldcg(reinterpret_cast<const float4 *>(rec + col0) + q4);
-      }
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int s2 = 0; s2 < kTcMaxSplits; ++s2)
-      if (s2 < CS) M = fmaxf(M, ml[s2].x);
-    float acc[kE];
-#pragma unroll
-    for (int e = 0; e < kE; ++e) acc[e] = 0.f;
-    float L = 0.f;
-#pragma unroll
-    for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
-      if (s2 < CS && ml[s2].x != -INFINITY) {
-        const float w = exp2f(ml[s2].x - M);
-        L += w * ml[s2].y;
-#pragma unroll
-        for (int q4 = 0; q4 < kE / 4; ++q4) {
-          acc[4 * q4 + 0] += w * ov[s2][q4].x;
-          acc[4 * q4 + 1] += w * ov[s2][q4].y;
-          acc[4 * q4 + 2] += w * ov[s2][q4].z;
-          acc[4 * q4 + 3] += w * ov[s2][q4].w;
+          for (int q4 = 0; q4 < kE / 4; ++q4) ov[s2][q4] = ld_peer_f32x4(prow + 16 * q4);
         }
       }
-    }
-    const float inv = 1.f / L;
-    const int rr = row0 + lr;
-    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
-                         (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + col0;
+      float M = -INFINITY;
 #pragma unroll
-    for (int q8 = 0; q8 < kE / 8; ++q8) {
-      uint4 pk;
-      pk.x = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 0] * inv, acc[q8 * 8 + 1] * inv));
-      pk.y = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 2] * inv, acc[q8 * 8 + 3] * inv));
-      pk.z = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 4] * inv, acc[q8 * 8 + 5] * inv));
-      pk.w = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 6] * inv, acc[q8 * 8 + 7] * inv));
-      *reinterpret_cast<uint4 *>(dst + q8 * 8) = pk;
+      for (int s2 = 0; s2 < kTcMaxSplits; ++s2)
+        if (s2 < CS) M = fmaxf(M, mls[s2][0]);
+      float acc[kE];
+#pragma unroll
+      for (int e = 0; e < kE; ++e) acc[e] = 0.f;
+      float L = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
+        if (s2 < CS && mls[s2][0] != -INFINITY) {
+          const float w = exp2f(mls[s2][0] - M);
+          L += w * mls[s2][1];
+#pragma unroll
+          for (int q4 = 0; q4 < kE / 4; ++q4) {
+            acc[4 * q4 + 0] += w * ov[s2][q4].x;
+            acc[4 * q4 + 1] += w * ov[s2][q4].y;
+            acc[4 * q4 + 2] += w * ov[s2][q4].z;
+            acc[4 * q4 + 3] += w * ov[s2][q4].w;
+          }
+        }
+      }
+      const float inv = 1.f / L;
+      const int rr = row0 + lr;
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
+                           (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + col0;
+#pragma unroll
+      for (int q8 = 0; q8 < kE / 8; ++q8) {
+        uint4 pk;
+        pk.x = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 0] * inv, acc[q8 * 8 + 1] * inv));
+        pk.y = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 2] * inv, acc[q8 * 8 + 3] * inv));
+        pk.z = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 4] * inv, acc[q8 * 8 + 5] * inv));
+        pk.w = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 6] * inv, acc[q8 * 8 + 7] * inv));
+        *reinterpret_cast<uint4 *>(dst + q8 * 8) = pk;
+      }
     }
   }
-  if (tid == 0) counters[unit] = 0u;  // ready for the next call
+  cluster_sync_all();  // peers are done reading this CTA's shared memory
 }
 
-// Split plan shared by the launcher and the workspace query: the split count
-// that minimises (waves x tiles per CTA) at one CTA per SM.
+// Split plan: the split count (cluster size) that minimises (waves x tiles
+// per CTA) at one CTA per SM.
 void plan_attn_tc(int B, int T, int Hkv, int G, int max_prefix, int num_sms, int *cs_out,
                   int *rowblocks_out) {
   const int max_nodes = T < SPEC_MAX_TREE_NODES ? T : SPEC_MAX_TREE_NODES;
@@ -563,20 +548,9 @@ void plan_attn_tc(int B, int T, int Hkv, int G, int max_prefix, int num_sms, int
   *rowblocks_out = rowblocks;
 }
 
-size_t attn_tc_workspace_bytes(int B, int T, int Hkv, int G, int D, int max_prefix, int num_sms) {
-  int cs, rowblocks;
-  plan_attn_tc(B, T, Hkv, G, max_prefix, num_sms, &cs, &rowblocks);
-  if (cs == 1) return 0;
-  const size_t units = static_cast<size_t>(rowblocks) * B * Hkv;
-  const size_t counters = (units * sizeof(uint32_t) + 255) & ~size_t(255);
-  const size_t rec = static_cast<size_t>(kTcRows) * (D + 4) * sizeof(float);
-  return counters + units * cs * rec;
-}
-
 template <int D, bool PACKED>
 static int launch_tc(const AttnArgs &args, const CUtensorMap &tmq, const CUtensorMap &tmk,
-                     const CUtensorMap &tmv, int cs, int rowblocks, uint32_t *counters,
-                     float *partials, cudaStream_t stream) {
+                     const CUtensorMap &tmv, int cs, int rowblocks, cudaStream_t stream) {
   using C = TcCfg<D, PACKED>;
   auto kernel = tree_attn_tc_kernel<D, PACKED>;
   static bool configured = false;
@@ -586,33 +560,33 @@ static int launch_tc(const AttnArgs &args, const CUtensorMap &tmq, const CUtenso
       return SPEC_ERR_CUDA;
     configured = true;
   }
-  const dim3 grid(cs, rowblocks, static_cast<unsigned>(args.B * args.Hkv));
-  kernel<<<grid, kTcThreads, C::kSmem, stream>>>(args, tmq, tmk, tmv, counters, partials);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, rowblocks, static_cast<unsigned>(args.B * args.Hkv));
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args, tmq, tmk, tmv) == cudaSuccess ? SPEC_OK
+                                                                             : SPEC_ERR_CUDA;
 }
 
 int launch_attn_tc(const AttnArgs &args, int max_prefix, int T, const CUtensorMap &tmq,
                    const CUtensorMap &tmk, const CUtensorMap &tmv, bool packed, int num_sms,
-                   void *workspace, size_t ws_bytes, cudaStream_t stream) {
+                   cudaStream_t stream) {
   int cs, rowblocks;
   plan_attn_tc(args.B, T, args.Hkv, args.G, max_prefix, num_sms, &cs, &rowblocks);
   if (static_cast<long long>(rowblocks) * args.B * args.Hkv > 65535) return SPEC_ERR_SHAPE;
-  uint32_t *counters = nullptr;
-  float *partials = nullptr;
-  if (cs > 1) {
-    const size_t need = attn_tc_workspace_bytes(args.B, T, args.Hkv, args.G, args.D, max_prefix,
-                                                num_sms);
-    if (!workspace || ws_bytes < need) return SPEC_ERR_WORKSPACE;
-    const size_t units = static_cast<size_t>(rowblocks) * args.B * args.Hkv;
-    counters = static_cast<uint32_t *>(workspace);
-    partials = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                         ((units * sizeof(uint32_t) + 255) & ~size_t(255)));
-  }
   if (args.D == 128)
-    return packed ? launch_tc<128, true>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream)
-                  : launch_tc<128, false>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream);
-  return packed ? launch_tc<64, true>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream)
-                : launch_tc<64, false>(args, tmq, tmk, tmv, cs, rowblocks, counters, partials, stream);
+    return packed ? launch_tc<128, true>(args, tmq, tmk, tmv, cs, rowblocks, stream)
+                  : launch_tc<128, false>(args, tmq, tmk, tmv, cs, rowblocks, stream);
+  return packed ? launch_tc<64, true>(args, tmq, tmk, tmv, cs, rowblocks, stream)
+                : launch_tc<64, false>(args, tmq, tmk, tmv, cs, rowblocks, stream);
 }
 
 }  // namespace spec
