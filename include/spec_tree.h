@@ -9,7 +9,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All array pointers are DEVICE pointers owned by the caller.  The library
- *    never allocates device memory and keeps no state between calls.
+ *    never allocates device memory and keeps no state between calls, except
+ *    for the fixed scratch array that spec_tree_verify_static uses.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL means the legacy default stream).  No call synchronises the host.
  *  - Host-detectable errors (null pointers, bad sizes, workspace too small)
@@ -188,6 +189,42 @@ int spec_tree_verify(const float *target_logits, const float *draft_logits,
                      uint64_t seed, int32_t *accept_len, int32_t *path_nodes,
                      int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
                      void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
+ * spec_tree_verify_static — spec_tree_verify without a caller workspace.
+ *
+ * No counterpart in the paper: this is a library convenience.  It serves
+ * callers that cannot allocate device memory, such as a plugin inside an
+ * inference engine that owns all device memory and passes the library only
+ * a step's inputs and outputs, or a binding from a runtime without a CUDA
+ * allocator.  The scratch spec_tree_verify takes as `workspace` lives
+ * instead in a fixed array of SPEC_VERIFY_STATIC_SCRATCH_BYTES inside the
+ * library, held on every GPU that loads the library until the process exits.
+ *
+ * Arguments, outputs and device-side errors are those of spec_tree_verify.
+ * The call allocates nothing and frees nothing; it clears the part of the
+ * array it uses (an asynchronous memset on `stream`) and then runs the same
+ * kernels as spec_tree_verify.
+ *  - Returns SPEC_ERR_WORKSPACE, before touching the device, when
+ *    spec_tree_verify_workspace_size(B, T, V) exceeds
+ *    SPEC_VERIFY_STATIC_SCRATCH_BYTES (for example more than about 32000
+ *    tree nodes in one batch); use spec_tree_verify with a workspace then.
+ *  - The first call made with a device current looks up the array's device
+ *    address on that device (cudaGetSymbolAddress).  Make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, and it keeps the last
+ *    call's contents: calls whose work overlaps on the GPU (different
+ *    streams, or different host threads) race and give wrong results.
+ *    Serialise them, for example on one stream.
+ */
+#define SPEC_VERIFY_STATIC_SCRATCH_BYTES (256u * 1024u)
+
+int spec_tree_verify_static(const float *target_logits, const float *draft_logits,
+                            const int32_t *tokens, const int32_t *parents,
+                            const int32_t *tree_offsets, int B, int T, int V, float temperature,
+                            uint64_t seed, int32_t *accept_len, int32_t *path_nodes,
+                            int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
+                            int32_t *status, void *stream);
 
 /* Human-readable name of a spec_status value (static storage). */
 const char *spec_status_string(int code);
