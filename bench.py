@@ -190,25 +190,14 @@ class Step:
         self.max_prefix = int(w.prefix_lens.max())
         self.seed = seed
 
-    def run(self, i: int, stream=None, ev=None):
-        """Enqueue step i: mask, attention, verification.  ``ev`` (optional)
-        holds three (start, end) event pairs recorded around the kernels."""
+    def run(self, i: int, stream=None):
+        """Enqueue step i: mask, attention, verification."""
         ttv, w, c = self.ttv, self.w, self.copies[i % len(self.copies)]
-        if ev is not None:
-            ev[0].record()
         ttv.build_tree_mask(self.par, self.off, self.status, mask=self.mask, depth=self.depth, stream=stream)
-        if ev is not None:
-            ev[1].record()
-            ev[2].record()
         ttv.tree_attn(c["q"], c["k"], c["v"], self.pl, self.off, self.mask, self.max_prefix,
                       self.status, o=self.o, workspace=self.ws_attn, stream=stream)
-        if ev is not None:
-            ev[3].record()
-            ev[4].record()
         ttv.tree_verify(c["tl"], c["dl"], self.tok, self.par, self.off, w.temperature,
                         self.seed + i, self.W, self.status, self.ws, outputs=self.outs, stream=stream)
-        if ev is not None:
-            ev[5].record()
 
 
 def run_native(args, rank, world, local_rank):
@@ -243,24 +232,20 @@ def run_native(args, rank, world, local_rank):
                 "accept_len": st.outs["accept_len"].cpu().tolist()}
 
     # capture: a warm-up graph of W steps and the timed graph(s) of K steps
+    # (nothing but the steps' own kernels: no event nodes between them)
     chunk = min(K, args.graph_steps)
-    try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
-               for _ in range(chunk)]
-    except TypeError:
-        evs = None
 
-    def capture(n, with_events):
+    def capture(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                st.run(i, ev=evs[i] if (with_events and evs is not None) else None)
+                st.run(i)
         return g
 
-    g_warm = capture(max(1, Wm), False)
-    g_main = capture(chunk, True)
+    g_warm = capture(max(1, Wm))
+    g_main = capture(chunk)
     reps, rem = divmod(K, chunk)
-    g_rem = capture(rem, False) if rem else None
+    g_rem = capture(rem) if rem else None
     with torch.cuda.stream(stream):
         g_warm.replay()
     torch.cuda.synchronize()
@@ -302,15 +287,11 @@ def run_native(args, rank, world, local_rank):
     if (status != 0).any():
         raise RuntimeError(f"device status {status.tolist()}")
 
-    # per-kernel durations from the events of the last timed replay of g_main
-    if evs is not None:
-        d_mask = np.array([e[0].elapsed_time(e[1]) for e in evs[:chunk]])
-        d_attn = np.array([e[2].elapsed_time(e[3]) for e in evs[:chunk]])
-        d_ver = np.array([e[4].elapsed_time(e[5]) for e in evs[:chunk]])
-        kernel_timing = "event pairs around each kernel inside the timed graph (last replay)"
-    else:
-        d_mask, d_attn, d_ver = per_kernel_graph_times(st, stream, chunk)
-        kernel_timing = "separate graphs of one kernel kind each (torch lacks graph-recorded events)"
+    # per-kernel durations: each kernel alone, back to back in a graph, on the
+    # same stream and over the same rotating inputs
+    d_mask, d_attn, d_ver = per_kernel_graph_times(st, stream, chunk)
+    kernel_timing = ("each kernel kind timed alone: a CUDA graph of %d launches over the rotating "
+                     "inputs, CUDA events on the launching stream" % chunk)
 
     elapsed_ms, value = combine_over_ranks(elapsed_ms, w.T, K, world, "cuda")
     ms_per_step = elapsed_ms / K
@@ -322,8 +303,8 @@ def run_native(args, rank, world, local_rank):
     achieved = ab / (attn_ms * 1e-3) / 1e9
     # the roofline block describes the kernel that takes the larger share of the step
     if ver_ms > attn_ms:
-        dom = {"kernel": "tree_verify_cluster_kernel" if w.temperature > 0
-               else "tree_verify_greedy_node_kernel",
+        dom = {"kernel": ("tree_verify_reg_kernel" if w.V <= 131072 else "tree_verify_cluster_kernel")
+               if w.temperature > 0 else "tree_verify_greedy_node_kernel",
                "bytes": vb, "ms": ver_ms, "traffic": profiled_traffic("tree_verify_llama7b")}
     else:
         dom = {"kernel": "tree_attn_tc_kernel", "bytes": ab, "ms": attn_ms,
@@ -373,8 +354,9 @@ def combine_over_ranks(elapsed_ms: float, units_per_step: int, steps: int, world
     return elapsed_ms, world * units_per_step * steps / (elapsed_ms / 1e3)
 
 
-def per_kernel_graph_times(st, stream, n):
-    """Mean duration of each kernel kind from a graph of n launches of it."""
+def per_kernel_graph_times(st, stream, n, reps=3):
+    """Mean duration per launch of each kernel kind, from a graph of n
+    back-to-back launches of that kernel alone (best of `reps` replays)."""
     import torch
     ttv, w = st.ttv, st.w
     out = []
@@ -390,17 +372,21 @@ def per_kernel_graph_times(st, stream, n):
                                   st.status, o=st.o, workspace=st.ws_attn)
                 else:
                     ttv.tree_verify(c["tl"], c["dl"], st.tok, st.par, st.off, w.temperature,
-                                    i, st.W, st.status, st.ws, outputs=st.outs)
+                                    st.seed + i, st.W, st.status, st.ws, outputs=st.outs)
         with torch.cuda.stream(stream):
             g.replay()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        out.append(np.full(n, e0.elapsed_time(e1) / n))
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            best = ms if best is None else min(best, ms)
+        out.append(np.full(n, best))
     return out
 
 

@@ -121,24 +121,8 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const int g = blockIdx.z % a.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const ReqGeom R = request_geometry(a, b);
-  const int rows_total = R.n * a.G;
-  const int row0 = rb * kTcRows;
-  if (R.err) {
-    if (tid == 0 && split == 0 && rb == 0 && g == 0) report(a.status, b, R.err);
-    return;  // uniform across the cluster (same request)
-  }
-  if (row0 >= rows_total) return;  // uniform across the cluster (same row block)
-  const int rows_here = min(kTcRows, rows_total - row0);
-  if (PACKED && rows_here > kTcRows / 2) {  // launch contract broken: uniform, never expected
-    if (tid == 0) report(a.status, b, SPEC_ERR_SHAPE);
-    return;
-  }
-  const int tiles_total = (R.keys + kKeyTile - 1) / kKeyTile;
-  const int per = (tiles_total + CS - 1) / CS;
-  const int t0 = split * per;
-  const int ntiles = max(0, min(t0 + per, tiles_total) - t0);
-
+  // ---- set-up that reads no global memory, overlapping the previous kernel
+  pdl_trigger();
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -153,6 +137,11 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     fence_barrier_init();
     s_timeout = 0;
   }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
   if (warp == 1) {
     tc::tmem_alloc(&s_tmem, C::kTmemCols);
     tc::tmem_relinquish();
@@ -161,6 +150,28 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
+  pdl_wait();
+
+  const ReqGeom R = request_geometry(a, b);
+  const int rows_total = R.n * a.G;
+  const int row0 = rb * kTcRows;
+  const int rows_here = min(kTcRows, rows_total - row0);
+  // Whole-block exits are uniform across the cluster (same request and row
+  // block); the block frees its tensor memory first.
+  const bool bad_block = PACKED && !R.err && row0 < rows_total && rows_here > kTcRows / 2;
+  if (R.err || row0 >= rows_total || bad_block) {
+    if (R.err && tid == 0 && split == 0 && rb == 0 && g == 0) report(a.status, b, R.err);
+    if (bad_block && tid == 0) report(a.status, b, SPEC_ERR_SHAPE);  // launch contract broken
+    if (warp == 1) {
+      __syncwarp();
+      tc::tmem_dealloc(tmem, C::kTmemCols);
+    }
+    return;
+  }
+  const int tiles_total = (R.keys + kKeyTile - 1) / kKeyTile;
+  const int per = (tiles_total + CS - 1) / CS;
+  const int t0 = split * per;
+  const int ntiles = max(0, min(t0 + per, tiles_total) - t0);
 
   // softmax-thread geometry (warps 2..9).  TMEM lane r = 32 * quad + lane.
   // Not packed: row r, two threads (key halves) per row.  Packed: the Q block
@@ -182,9 +193,6 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
       mbar_arrive_expect_tx(&bar_q, C::kQBytes);
 #pragma unroll
       for (int bx = 0; bx < C::kBoxes; ++bx) {
@@ -565,13 +573,14 @@ static int launch_tc(const AttnArgs &args, const CUtensorMap &tmq, const CUtenso
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  pdl_attribute(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, args, tmq, tmk, tmv) == cudaSuccess ? SPEC_OK
                                                                              : SPEC_ERR_CUDA;
 }

@@ -20,6 +20,24 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  Kernels launched with the
+// programmatic-serialization attribute may start before the previous kernel
+// in the stream has finished: they signal their own dependents at once, do
+// only set-up (barriers, tensor-memory allocation) before pdl_wait(), and
+// touch no global memory before it; pdl_wait() returns once the previous
+// grid has completed and its writes are visible (at once without a
+// programmatic predecessor).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+inline void pdl_attribute(cudaLaunchAttribute &attr) {
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+}
+
 // First error for a request sticks; kernels never write SPEC_OK.
 __device__ __forceinline__ void report(int32_t *status, int b, int code) {
   if (status != nullptr && b >= 0) atomicCAS(status + b, 0, code);
@@ -118,6 +136,19 @@ __device__ __forceinline__ void cluster_sync_all() {
           : "memory");
 }
 
+// Split cluster barrier: arrive early (relaxed, no ordering), wait later.
+// Used once at kernel start so that every CTA of the cluster is known to be
+// running before the first access to a peer's shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  __syncwarp();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory object in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t peer_addr(const void *local, uint32_t rank) {
   uint32_t r;
@@ -156,6 +187,31 @@ __device__ __forceinline__ void st_peer_f32x4(uint32_t addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
                "f"(v.y), "f"(v.z), "f"(v.w)
                : "memory");
+}
+
+// Remote stores that complete on the destination CTA's mbarrier as
+// transaction bytes (`addr` and `bar` are shared::cluster addresses of the
+// same CTA, from peer_addr).  The destination waits on its barrier; no
+// cluster-wide barrier is involved.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr),
+               "f"(v), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_v2_f32(uint32_t addr, float x, float y, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::
+                   "r"(addr),
+               "f"(x), "f"(y), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4_f32(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
 }
 
 // Named barrier for `nthreads` threads (a multiple of 32) of this CTA.

@@ -24,6 +24,8 @@ build_tree_mask_kernel(const int32_t *__restrict__ parents, const int32_t *__res
   __shared__ int bad;
   const int b = blockIdx.x;
   const int i = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   const int lo = __ldg(offsets + b), hi = __ldg(offsets + b + 1);
   const int n = hi - lo;
   if (lo < 0 || hi > T || n < 1 || n > SPEC_MAX_TREE_NODES) {
@@ -89,7 +91,15 @@ extern "C" int spec_build_tree_mask(const int32_t *parents, const int32_t *tree_
   if (!parents || !tree_offsets || !mask || !depth || !status) return SPEC_ERR_NULL;
   if (B < 1 || T < 1 || T > B * SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
   if (reinterpret_cast<uintptr_t>(mask) & 15) return SPEC_ERR_ALIGNMENT;
-  spec::build_tree_mask_kernel<<<B, SPEC_MAX_TREE_NODES, 0, static_cast<cudaStream_t>(stream)>>>(
-      parents, tree_offsets, B, T, reinterpret_cast<uint4 *>(mask), depth, status);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+  cfg.blockDim = dim3(SPEC_MAX_TREE_NODES, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  spec::pdl_attribute(attr[0]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, spec::build_tree_mask_kernel, parents, tree_offsets, B, T, reinterpret_cast<uint4 *>(mask), depth, status) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }

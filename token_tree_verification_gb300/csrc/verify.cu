@@ -1,7 +1,9 @@
-// Steps V1-V4 and R: verification of a speculated token tree.  Stochastic
-// verification runs one thread-block cluster per node (the node's target and
-// draft rows split across the cluster's shared memory, about 16K entries per
-// CTA); greedy verification runs the per-node kernel of verify_node.cu.
+// Steps V1-V4 and R: verification of a speculated token tree.  Greedy
+// verification runs the per-node kernel of verify_node.cu; stochastic
+// verification runs one thread-block cluster per node, with the node's rows
+// in registers (verify_reg.cu) up to 131072 vocabulary entries, and for
+// larger vocabularies split across the cluster's shared memory (the kernel
+// below, up to 27648 entries per CTA).
 //
 // Sources: speculative-decoding explainer (intelliparadigm.com) §2.2
 // 三阶段工作流程详解 — stage 2: accept probability alpha = min(1, p/q); stage 3:
@@ -14,8 +16,10 @@
 // always tested in index order against the residual left by their earlier
 // siblings, so the accept decision of every child and the token emitted when
 // the walk stops at a node can all be computed at once, one node per CTA
-// group.  The last group of a request to finish then walks the tree in one
-// warp.
+// group.  A node's chain stops at its first accepted child (the walk never
+// tests later children, nor draws at a node it leaves), so most nodes need
+// no reduction round and no draw.  The last group of a request to finish
+// then walks the tree in one warp.
 //
 // Residual chain in closed form.  With r_0 = p and r_j = norm(max(0,
 // r_{j-1} - q)), induction gives r_j = max(0, p - c_j q) / W(c_j) with
@@ -29,70 +33,30 @@
 
 namespace spec {
 
-// Per-CTA scratch for one reduction round, double buffered by round parity
-// so a round never waits for the previous round's readers.
-struct RoundScratch {
-  float w[2][kVWarps][2];
-  int wi[2][kVWarps];
+// Exchange slots of a node's CTA group.  Every warp pushes its partial sum
+// into slot [rank][warp] of every CTA of the group with st.async, and the
+// round's mbarrier in each CTA completes once all CS x 32 partials (in the
+// statistics round also the slice maxima and the children's logits) have
+// landed: no CTA-wide or cluster-wide barrier per round.  Every warp then
+// adds the partials in the same order, so all threads of the group hold
+// bit-identical totals.
+struct Exchange {
+  float2 statm[kMaxCS];                // per slice: max target logit, max draft logit
+  float2 stat[kMaxCS][kVWarps];        // per warp: sums of 2^((x - max) * l2s), target and draft
+  float part[2][kMaxCS][kVWarps];      // reduction rounds, by round parity
+  float2 child[SPEC_MAX_TREE_NODES];   // the children's raw logits (target, draft)
 };
-static_assert(kVWarps == 32, "warp 0 combines one partial per lane");
-
-// Cluster all-gather slots: every CTA pushes its partials into slot [rank]
-// of every peer with remote stores, so after one cluster barrier all values
-// are read from local shared memory.  Double buffered by round parity.
-struct Gather {
-  float v[2][kMaxCS][4];
-};
-
-// Barrier of one node's CTA group: the cluster barrier when the group spans
-// several CTAs, else the CTA barrier.
-__device__ __forceinline__ void group_sync(int CS) {
-  if (CS > 1) cluster_sync_all();
-  else __syncthreads();
-}
-
-// Publish this CTA's float4 to slot [rank] of every CTA of the group.
-__device__ __forceinline__ void gather_put(Gather &gx, int parity, int rank, int CS, int lane,
-                                           float4 val) {
-  if (lane < CS) {
-    if (CS > 1) st_peer_f32x4(peer_addr(&gx.v[parity][rank][0], lane), val);
-    else *reinterpret_cast<float4 *>(&gx.v[parity][0][0]) = val;
-  }
-}
-
-// Sum `x` over the CTA (warp shuffles, then warp 0 over the 32 warp
-// partials) and over the group.  Returns the group total (identical in every
-// CTA: partials are added in rank order) and, in `parts`, the per-CTA totals.
-// One __syncthreads and one group barrier.
-__device__ float cluster_round_sum(float x, RoundScratch &rs, Gather &gx, int parity, int rank,
-                                   int CS, float *parts) {
-  x = warp_sum(x);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) rs.w[parity][w][0] = x;
-  __syncthreads();
-  if (w == 0) {
-    const float v = warp_sum(rs.w[parity][l][0]);
-    gather_put(gx, parity, rank, CS, l, make_float4(v, 0.f, 0.f, 0.f));
-  }
-  group_sync(CS);
-  float tot = 0.f;
-  for (int r = 0; r < CS; ++r) {
-    const float v = gx.v[parity][r][0];
-    if (parts) parts[r] = v;
-    tot += v;
-  }
-  return tot;
-}
 
 __global__ void __launch_bounds__(kVThreads)
 tree_verify_cluster_kernel(const VerifyArgs a) {
   extern __shared__ __align__(128) float vsm[];  // [chunk] target side, [chunk] draft side
-  __shared__ RoundScratch rs;
-  __shared__ __align__(16) Gather gx;
+  __shared__ __align__(16) Exchange ex;
   __shared__ TreeSmem ts;
-  __shared__ int s_pick, s_pickw;
-  __shared__ float s_cb[2], s_before;
-  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ float s_red[2][kVWarps];
+  __shared__ float s_kept[kMaxCS];    // per slice: its share of p
+  __shared__ float s_sc[2];
+  __shared__ __align__(8) uint64_t bars[2];   // the slice copies
+  __shared__ __align__(8) uint64_t xbar[3];   // exchange: statistics round, rounds by parity
 
   const int CS = static_cast<int>(cluster_size());
   const int rank = static_cast<int>(cluster_rank());
@@ -102,273 +66,302 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
   float *drow = vsm + a.chunk;
   const int v0 = rank * a.chunk;
   const int len = max(0, min(a.V, v0 + a.chunk) - v0);
-  const bool greedy = !(a.temp > 0.f);
+  // Every pass gives warp w the contiguous range [e0, e1) of the slice (lanes
+  // strided), so a pass's per-warp sums are also the first level of the
+  // inverse-CDF search.
+  const int seg = (((len + kVWarps - 1) / kVWarps) + 31) & ~31;
+  const int e0 = min(len, w_id * seg), e1 = min(len, e0 + seg);
   // 1-D bulk copies need 16-byte aligned rows and a length multiple of 16 B.
   const bool bulk = ((a.V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0) &&
-                    (greedy || (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0);
+                    ((reinterpret_cast<uintptr_t>(a.draft) & 15) == 0) && len > 0;
   const float *trow_g = a.target + static_cast<size_t>(t) * a.V;
-  const float *drow_g = greedy ? nullptr : a.draft + static_cast<size_t>(t) * a.V;
+  const float *drow_g = a.draft + static_cast<size_t>(t) * a.V;
 
-  // ---- V1 (start): the target row slice streams in while the tree is read
+  pdl_trigger();
   if (tid == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&xbar[i], 1);
     fence_barrier_init();
-    if (bulk && len > 0) {
+  }
+  pdl_wait();
+  const TreeLoads tl = tree_loads(a, t);   // issued ahead of the row copies
+  // ---- V1 (start): the target row slice streams in while the tree is read
+  if (tid == 0) {
+    if (bulk) {
       mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(len) * 4u);
       bulk_copy_g2s(lrow, trow_g + v0, static_cast<uint32_t>(len) * 4u, &bars[0]);
     }
   }
-  const NodeCtx c = load_tree(a, t, ts);
+  // waited for before the first remote store (the barriers are initialised)
+  if (CS > 1) cluster_arrive_relaxed();
+  const NodeCtx c = load_tree(a, t, ts, tl);
   const int k = c.k;
-  const bool need_draft = !c.err && !greedy && k > 0;
-  if (tid == 0 && bulk && need_draft && len > 0) {
+  const bool need_draft = !c.err && k > 0;   // leaves never read their draft row
+  if (tid == 0 && bulk && need_draft) {
     mbar_arrive_expect_tx(&bars[1], static_cast<uint32_t>(len) * 4u);
     bulk_copy_g2s(drow, drow_g + v0, static_cast<uint32_t>(len) * 4u, &bars[1]);
   }
-  load_children(a, c, t, ts);
+  if (!c.err) {
+    // step R: the children's accept-test uniforms and the fallback draw's
+    if (tid < k) ts.cU[tid] = spec_uniform(a.seed, ts.child[tid], c.b, 0);
+    else if (tid == kVThreads - 1) ts.ufb = spec_uniform(a.seed, c.u, c.b, 1);
+    if (tid == 0)
+      mbar_arrive_expect_tx(&xbar[0], static_cast<uint32_t>(CS * (8 + kVWarps * 8) + 8 * k));
+  }
   // ---- wait for the slices (a copy issued for a node is always waited for)
-  bool timed_out = false;
-  if (bulk && len > 0) {
-    if (!mbar_wait(&bars[0], 0)) timed_out = true;
-    if (need_draft && !mbar_wait(&bars[1], 0)) timed_out = true;
-  } else if (!c.err) {
+  bool ok = true;
+  if (bulk) {
+    if (!mbar_wait(&bars[0], 0)) ok = false;
+    if (need_draft && !mbar_wait(&bars[1], 0)) ok = false;
+  }
+  if (CS > 1) cluster_wait();  // every CTA of the group is running
+  if (!bulk && !c.err) {
     for (int i = tid; i < len; i += kVThreads) {
       lrow[i] = __ldcs(trow_g + v0 + i);
       if (need_draft) drow[i] = __ldcs(drow_g + v0 + i);
     }
   }
-  if (timed_out && tid == 0) report(a.status, c.b, SPEC_ERR_TIMEOUT);
-  __syncthreads();
+  // The children's raw logits, from the CTA whose slice holds them, to every
+  // CTA of the group (read before the slices are overwritten below).
+  if (need_draft && tid < k) {
+    const int x = ts.tok[ts.child[tid]];
+    if (x >= v0 && x < v0 + len) {
+      const float pl = bulk ? lrow[x - v0] : __ldg(trow_g + x);
+      const float ql = bulk ? drow[x - v0] : __ldg(drow_g + x);
+      for (int r = 0; r < CS; ++r)
+        st_async_v2_f32(peer_addr(&ex.child[tid], r), pl, ql, peer_addr(&xbar[0], r));
+    }
+  }
+  if (!bulk) __syncthreads();  // the plainly loaded slices are complete
 
+  int stop = k;        // first accepted child, k when every child is rejected
+  int my_flag = 0;     // thread j < k: the flag of child j
+  int p_ok = -1;       // parity of the last reduction round that moved the residual
+  float c_prev = 0.f, sc_l = 0.f, sc_d = 0.f;
   if (!c.err) {
-    int parity = 0;
-    if (greedy) {
-      // ---- argmax of the raw target logits, lowest index on ties
-      ArgMax am{-INFINITY, 0x7fffffff};
-      for (int i = tid; i < len; i += kVThreads) am = better(am, ArgMax{lrow[i], v0 + i});
-      am = warp_argmax(am);
-      if (lane == 0) {
-        rs.w[0][w_id][0] = am.v;
-        rs.wi[0][w_id] = am.i;
+    const float T_ = a.temp, iT = a.inv_temp;
+    const float l2s = iT * 1.4426950408889634f;  // exp(x / T) = 2^(x * l2s)
+    // ---- V1: the slice's maxima, then its exponentials in place (one scale
+    //      per slice: p(v) = sc_l * lrow[v], q(v) = sc_d * drow[v])
+    float ml = -INFINITY, md = -INFINITY;
+    for (int i = e0 + lane; i < e1; i += 32) {
+      ml = fmaxf(ml, lrow[i]);
+      if (need_draft) md = fmaxf(md, drow[i]);
+    }
+    ml = warp_max(ml);
+    md = warp_max(md);
+    if (lane == 0) {
+      s_red[0][w_id] = ml;
+      s_red[1][w_id] = md;
+    }
+    __syncthreads();
+    ml = warp_max(s_red[0][lane]);
+    md = warp_max(s_red[1][lane]);
+    float sl = 0.f, sd = 0.f;
+    for (int i = e0 + lane; i < e1; i += 32) {
+      const float el = fast_exp2((lrow[i] - ml) * l2s);
+      lrow[i] = el;
+      sl += el;
+      if (need_draft) {
+        const float ed = fast_exp2((drow[i] - md) * l2s);
+        drow[i] = ed;
+        sd += ed;
       }
-      __syncthreads();
-      if (w_id == 0) {
-        const ArgMax r = warp_argmax(ArgMax{rs.w[0][lane][0], rs.wi[0][lane]});
-        gather_put(gx, 0, rank, CS, lane, make_float4(r.v, __int_as_float(r.i), 0.f, 0.f));
-      }
-      group_sync(CS);
-      if (rank == 0 && tid == 0) {
-        ArgMax g{-INFINITY, 0x7fffffff};
-        for (int r = 0; r < CS; ++r) g = better(g, ArgMax{gx.v[0][r][0], __float_as_int(gx.v[0][r][1])});
-        a.fallback[t] = g.i;
-        for (int j = 0; j < k; ++j) {
-          const int ch = ts.child[j];
-          a.flags[c.lo + ch] = (ts.tok[ch] == g.i) ? kFlagAccept : 0;
-        }
-      }
-    } else {
-      const float T_ = a.temp, iT = a.inv_temp;
-      const float l2s = iT * 1.4426950408889634f;  // exp(x / T) = 2^(x * l2s)
-      // ---- V1: per-thread max and sum of exp((x - m)/T) over the thread's
-      //      elements, combined over the CTA and the cluster in one round
-      float ml = -INFINITY, md = -INFINITY;
-      for (int i = tid; i < len; i += kVThreads) {
-        ml = fmaxf(ml, lrow[i]);
-        if (need_draft) md = fmaxf(md, drow[i]);
-      }
-      float sl = 0.f, sd = 0.f;
-      for (int i = tid; i < len; i += kVThreads) {
-        const float el = fast_exp2((lrow[i] - ml) * l2s);
-        lrow[i] = el;
-        sl += el;
-        if (need_draft) {
-          const float ed = fast_exp2((drow[i] - md) * l2s);
-          drow[i] = ed;
-          sd += ed;
-        }
-      }
-      // warp combine of (m, s) pairs
-      const float wml = warp_max(ml), wmd = warp_max(md);
-      const float wsl = warp_sum(sl > 0.f ? sl * fast_exp2((ml - wml) * l2s) : 0.f);
-      const float wsd = warp_sum(sd > 0.f ? sd * fast_exp2((md - wmd) * l2s) : 0.f);
-      __shared__ float s_pair[kVWarps][4];
-      if (lane == 0) {
-        s_pair[w_id][0] = wml;
-        s_pair[w_id][1] = wsl;
-        s_pair[w_id][2] = wmd;
-        s_pair[w_id][3] = wsd;
-      }
-      __syncthreads();
-      if (w_id == 0) {
-        const float pm = s_pair[lane][0], ps = s_pair[lane][1];
-        const float qm = s_pair[lane][2], qs = s_pair[lane][3];
-        const float cm = warp_max(pm), cmd = warp_max(qm);
-        const float cs = warp_sum(ps > 0.f ? ps * fast_exp2((pm - cm) * l2s) : 0.f);
-        const float csd = warp_sum(qs > 0.f ? qs * fast_exp2((qm - cmd) * l2s) : 0.f);
-        gather_put(gx, parity, rank, CS, lane, make_float4(cm, cs, cmd, csd));
-      }
-      group_sync(CS);
+    }
+    sl = warp_sum(sl);
+    sd = warp_sum(sd);
+    if (lane < CS) {
+      const uint32_t bar = peer_addr(&xbar[0], lane);
+      st_async_v2_f32(peer_addr(&ex.stat[rank][w_id], lane), sl, sd, bar);
+      if (w_id == 0) st_async_v2_f32(peer_addr(&ex.statm[rank], lane), ml, md, bar);
+    }
+    if (ok && !mbar_wait(&xbar[0], 0)) ok = false;
+    if (w_id == 0) {
+      // group maxima and sums, the slices' shares of p, the children's p and q
       float Ml = -INFINITY, Md = -INFINITY;
-      float4 part[kMaxCS];
       for (int r = 0; r < CS; ++r) {
-        part[r] = *reinterpret_cast<const float4 *>(&gx.v[parity][r][0]);
-        Ml = fmaxf(Ml, part[r].x);
-        Md = fmaxf(Md, part[r].z);
+        Ml = fmaxf(Ml, ex.statm[r].x);
+        Md = fmaxf(Md, ex.statm[r].y);
       }
-      float Sp = 0.f, Sq = 0.f;
-      float kept[kMaxCS];
+      float Sp = 0.f, Sq = 0.f, mine = 0.f;
       for (int r = 0; r < CS; ++r) {
-        kept[r] = part[r].y > 0.f ? part[r].y * fast_exp2((part[r].x - Ml) * l2s) : 0.f;
-        Sp += kept[r];
-        if (need_draft && part[r].w > 0.f) Sq += part[r].w * fast_exp2((part[r].z - Md) * l2s);
+        const float2 v = ex.stat[r][lane];
+        const float sp = warp_sum(v.x), sq = warp_sum(v.y);
+        const float2 m = ex.statm[r];
+        const float fp = sp > 0.f ? sp * fast_exp2((m.x - Ml) * l2s) : 0.f;
+        Sp += fp;
+        if (need_draft && sq > 0.f) Sq += sq * fast_exp2((m.y - Md) * l2s);
+        if (lane == r) mine = fp;
       }
-      for (int r = 0; r < CS; ++r) kept[r] /= Sp;  // chunk sums of p
-      parity ^= 1;
-      // the children's p(x) and q(x), in parallel (read by the chain below)
-      if (tid < k) {
-        ts.cP[tid] = precise_prob(ts.cP[tid], Ml, T_, iT, Sp);
-        ts.cQ[tid] = precise_prob(ts.cQ[tid], Md, T_, iT, Sq);
+      if (lane < CS) s_kept[lane] = mine / Sp;
+      for (int j = lane; j < k; j += 32) {
+        ts.cP[j] = precise_prob(ex.child[j].x, Ml, T_, iT, Sp);
+        ts.cQ[j] = precise_prob(ex.child[j].y, Md, T_, iT, Sq);
       }
-      // p(v), q(v) for this thread's elements
-      const float scale_l = ml == -INFINITY ? 0.f : fast_exp2((ml - Ml) * l2s) / Sp;
-      const float scale_d = (need_draft && md != -INFINITY) ? fast_exp2((md - Md) * l2s) / Sq : 0.f;
-      for (int i = tid; i < len; i += kVThreads) {
-        lrow[i] *= scale_l;
-        if (need_draft) drow[i] *= scale_d;
+      if (lane == 0) {
+        s_sc[0] = ml == -INFINITY ? 0.f : fast_exp2((ml - Ml) * l2s) / Sp;
+        s_sc[1] = (need_draft && md != -INFINITY) ? fast_exp2((md - Md) * l2s) / Sq : 0.f;
       }
+    }
+    __syncthreads();
+    sc_l = s_sc[0];
+    sc_d = s_sc[1];
 
-      __syncthreads();  // the children's probabilities are in shared memory
-      // ---- V2: the children's accept tests, one reduction per rejection
-      float c_prev = 0.f, W_prev = 1.f;
-      for (int j = 0; j < k; ++j) {
-        const int ch = ts.child[j];
-        const float P = ts.cP[j];
-        const float Q = ts.cQ[j];
-        const float alpha = Q > 0.f ? fminf(1.f, fmaxf(0.f, fmaf(-c_prev, Q, P)) / (W_prev * Q)) : 1.f;
-        if (rank == 0 && tid == 0) {
-          const float uu = ts.cU[j];
-          int f = (uu < alpha) ? kFlagAccept : 0;
-          if (fabsf(uu - alpha) < kTieBand) f |= kFlagTie;
-          a.flags[c.lo + ch] = f;
-        }
-        const float c_new = c_prev + W_prev;
-        float w = 0.f;
-        for (int i = tid; i < len; i += kVThreads) w += fmaxf(0.f, fmaf(-c_new, drow[i], lrow[i]));
-        float chunks[kMaxCS];
-        const float Wn = cluster_round_sum(w, rs, gx, parity, rank, CS, chunks);
-        parity ^= 1;
-        if (Wn > 0.f) {  // otherwise the residual is all zero: keep r
-          c_prev = c_new;
-          W_prev = Wn;
-          for (int r = 0; r < CS; ++r) kept[r] = chunks[r];
-        }
+    // ---- V2: the children's accept tests in index order.  The walk accepts
+    //      the first accepted child, so the chain stops there: later children
+    //      and this node's fallback draw can never be used.
+    float W_prev = 1.f;
+    bool frozen = false;   // a residual that summed to zero stays as it is
+    int rounds = 0;
+    for (int j = 0; j < k; ++j) {
+      const float P = ts.cP[j];
+      const float Q = ts.cQ[j];
+      const float alpha = Q > 0.f ? fminf(1.f, fmaxf(0.f, fmaf(-c_prev, Q, P)) / (W_prev * Q)) : 1.f;
+      const float uu = ts.cU[j];
+      const bool accept = uu < alpha;
+      if (tid == j) my_flag = (accept ? kFlagAccept : 0) | (fabsf(uu - alpha) < kTieBand ? kFlagTie : 0);
+      if (accept) {
+        stop = j;
+        break;
       }
+      if (frozen) continue;
+      // rejected: r becomes max(0, p - c q) / W(c) with c = c_prev + W_prev
+      const float c_new = c_prev + W_prev;
+      const float cq = c_new * sc_d;
+      float wsum = 0.f;
+      for (int i = e0 + lane; i < e1; i += 32) wsum += fmaxf(0.f, fmaf(-cq, drow[i], sc_l * lrow[i]));
+      wsum = warp_sum(wsum);
+      const int p = rounds & 1;
+      if (tid == 0) mbar_arrive_expect_tx(&xbar[1 + p], static_cast<uint32_t>(CS * kVWarps * 4));
+      if (lane < CS)
+        st_async_f32(peer_addr(&ex.part[p][rank][w_id], lane), wsum, peer_addr(&xbar[1 + p], lane));
+      if (ok && !mbar_wait(&xbar[1 + p], (rounds >> 1) & 1)) ok = false;
+      ++rounds;
+      float Wn = 0.f;
+      for (int r = 0; r < CS; ++r) Wn += warp_sum(ex.part[p][r][lane]);
+      if (Wn > 0.f) {
+        c_prev = c_new;
+        W_prev = Wn;
+        p_ok = p;
+      } else {
+        frozen = true;
+      }
+    }
+  }
+  // No CTA touches a peer's shared memory after this point: arrive now, wait
+  // before exiting, so that no CTA leaves while a peer may still store to it.
+  if (CS > 1) cluster_arrive_relaxed();
+  if (!ok && tid == 0) report(a.status, c.b, SPEC_ERR_TIMEOUT);
 
-      // ---- V3: the token emitted when the walk stops here, drawn by
-      //      inverse CDF from r ∝ max(0, p - c q) (c = 0: r = p)
+  int writer = 0;  // the CTA of the group that publishes the node's results
+  if (!c.err) {
+    // ---- V3: when every child is rejected (or u is a leaf), the token
+    //      emitted on stopping here: inverse CDF of r ∝ max(0, p - c q)
+    if (stop == k) {
       float total = 0.f;
-      for (int r = 0; r < CS; ++r) total += kept[r];
+      for (int r = 0; r < CS; ++r)
+        total += p_ok >= 0 ? warp_sum(ex.part[p_ok][r][lane]) : s_kept[r];
       const float target = ts.ufb * total;
       int owner = -1;
-      float prefix = 0.f;
-      {
-        float run = 0.f;
-        for (int r = 0; r < CS; ++r) {
-          if (run + kept[r] > target) { owner = r; prefix = run; break; }
-          run += kept[r];
+      float prefix = 0.f, run = 0.f;
+      for (int r = 0; r < CS; ++r) {
+        const float m = p_ok >= 0 ? warp_sum(ex.part[p_ok][r][lane]) : s_kept[r];
+        if (owner < 0 && run + m > target) {
+          owner = r;
+          prefix = run;
         }
-        if (owner < 0) {  // rounding kept the running sum below the target
-          run = 0.f;
-          for (int r = 0; r < CS; ++r) {
-            if (kept[r] > 0.f) { owner = r; prefix = run; }
-            run += kept[r];
-          }
-        }
+        run += m;
       }
+      if (owner < 0) {  // rounding kept the running sum below the target
+        run = 0.f;
+        for (int r = 0; r < CS; ++r) {
+          const float m = p_ok >= 0 ? warp_sum(ex.part[p_ok][r][lane]) : s_kept[r];
+          if (m > 0.f) {
+            owner = r;
+            prefix = run;
+          }
+          run += m;
+        }
+        if (owner < 0) owner = 0;
+      }
+      writer = owner;
       if (rank == owner) {
-        // Warp-contiguous segments; warp partial sums, then the owning warp
-        // scans its segment 32 elements at a time.
-        const int seg = (len + kVWarps - 1) / kVWarps;
-        const int s0 = min(len, w_id * seg), s1 = min(len, s0 + seg);
-        float ws = 0.f;
-        for (int i = s0 + lane; i < s1; i += 32)
-          ws += c_prev != 0.f ? fmaxf(0.f, fmaf(-c_prev, drow[i], lrow[i])) : lrow[i];
-        ws = warp_sum(ws);
-        if (lane == 0) rs.w[parity][w_id][1] = ws;
-        if (tid == 0) s_pick = -1;
-        __syncthreads();
-        if (w_id == 0) {
-          // inclusive scan of the warp partials, first one passing the target
-          const float v = rs.w[parity][lane][1];
-          float inc = v;
+        const float cq = c_prev * sc_d;
+        auto weight = [&](int i) -> float {
+          return c_prev != 0.f ? fmaxf(0.f, fmaf(-cq, drow[i], sc_l * lrow[i])) : sc_l * lrow[i];
+        };
+        auto scan = [&](float v) -> float {  // inclusive warp scan
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
+            const float y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
           }
-          const uint32_t hit = __ballot_sync(0xffffffffu, prefix + inc > target);
-          const int L = hit ? __ffs(hit) - 1 : -1;
-          const float before_l = __shfl_sync(0xffffffffu, prefix + inc - v, L < 0 ? 0 : L);
-          if (lane == 0) {
-            s_pickw = L;
-            s_before = before_l;
-          }
-        }
+          return v;
+        };
+        // level 1: the slice's warp ranges, from the last pass's partials
+        const float v1 = p_ok >= 0 ? ex.part[p_ok][rank][lane] : ex.stat[rank][lane].x * sc_l;
+        const float inc1 = scan(v1);
+        const uint32_t hit1 = __ballot_sync(0xffffffffu, prefix + inc1 > target);
+        const int sw = hit1 ? __ffs(hit1) - 1 : -1;
+        const float before1 = __shfl_sync(0xffffffffu, prefix + inc1 - v1, sw < 0 ? 0 : sw);
+        // level 2: that range, one element per thread, 32-element groups
+        const int g0 = sw < 0 ? 0 : min(len, sw * seg);
+        const int g1 = sw < 0 ? 0 : min(len, g0 + seg);
+        const int gi = g0 + tid;
+        const float wv = gi < g1 ? weight(gi) : 0.f;
+        const float gs = warp_sum(wv);
+        if (lane == 0) s_red[1][w_id] = gs;
         __syncthreads();
-        const int pick_w = s_pickw;
-        const float before = s_before;
-        if (pick_w == w_id) {
-          float run = before;
-          for (int base = s0; base < s1; base += 32) {
-            const int i = base + lane;
-            float wv = 0.f;
-            if (i < s1) wv = c_prev != 0.f ? fmaxf(0.f, fmaf(-c_prev, drow[i], lrow[i])) : lrow[i];
-            float inc = wv;  // inclusive warp scan
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const float y = __shfl_up_sync(0xffffffffu, inc, o);
-              if (lane >= o) inc += y;
-            }
-            const float cum = run + inc;
-            const uint32_t hit = __ballot_sync(0xffffffffu, i < s1 && cum > target);
-            if (hit) {
-              if (lane == __ffs(hit) - 1) {
-                s_pick = v0 + i;
-                s_cb[0] = cum - wv;
-                s_cb[1] = cum;
-              }
+        const float v2 = s_red[1][lane];
+        const float inc2 = scan(v2);
+        const uint32_t hit2 = __ballot_sync(0xffffffffu, before1 + inc2 > target);
+        const int gw = (sw >= 0 && hit2) ? __ffs(hit2) - 1 : -1;
+        if (gw >= 0 && w_id == gw) {
+          // level 3: the group's elements
+          const float before2 = __shfl_sync(0xffffffffu, before1 + inc2 - v2, gw);
+          const float inc3 = scan(wv);
+          const float cum = before2 + inc3;
+          const uint32_t hit3 = __ballot_sync(0xffffffffu, gi < g1 && cum > target);
+          int L;
+          float cb0, cb1;
+          if (hit3) {
+            L = __ffs(hit3) - 1;
+            cb0 = __shfl_sync(0xffffffffu, cum - wv, L);
+            cb1 = __shfl_sync(0xffffffffu, cum, L);
+          } else {  // rounding: the group's last positive weight, on the boundary
+            const uint32_t pos = __ballot_sync(0xffffffffu, gi < g1 && wv > 0.f);
+            L = pos ? 31 - __clz(pos) : 0;
+            cb0 = cb1 = target;
+          }
+          if (lane == 0) {
+            const bool tie = fabsf(target - cb0) < kTieBand * total || fabsf(target - cb1) < kTieBand * total;
+            a.fallback[t] = (v0 + g0 + 32 * gw + L) | (tie ? (1 << 31) : 0);
+          }
+        } else if (gw < 0 && tid == 0) {
+          // rounding: the slice's last positive weight, on the boundary
+          int pick = -1;
+          for (int i = len - 1; i >= 0; --i) {
+            if (weight(i) > 0.f) {
+              pick = v0 + i;
               break;
             }
-            run += __shfl_sync(0xffffffffu, inc, 31);
           }
-        }
-        __syncthreads();
-        if (tid == 0) {
-          int pick = s_pick;
-          float cb0, cb1;
-          if (pick >= 0) {
-            cb0 = s_cb[0];
-            cb1 = s_cb[1];
-          } else {  // not reached in this slice: last positive weight of the slice
-            for (int i = len - 1; i >= 0; --i) {
-              const float wv = c_prev != 0.f ? fmaxf(0.f, fmaf(-c_prev, drow[i], lrow[i])) : lrow[i];
-              if (wv > 0.f) { pick = v0 + i; break; }
-            }
-            if (pick < 0) pick = v0;
-            cb0 = cb1 = target;  // the draw sits on the boundary
-          }
-          const bool tie = fabsf(target - cb0) < kTieBand * total || fabsf(target - cb1) < kTieBand * total;
-          a.fallback[t] = pick | (tie ? (1 << 31) : 0);
-          __threadfence();
+          if (pick < 0) pick = v0;
+          a.fallback[t] = pick | (1 << 31);
         }
       }
     }
-    group_sync(CS);  // no CTA leaves while a peer may still read its exchange slots
+    // every CTA computed the same decisions; the writer publishes them
+    if (rank == writer && tid < k) a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
   } else if (rank == 0 && tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }
-  if (rank == 0) arrive_and_walk(a, c, ts, gridDim.x / CS);
+  if (rank == writer) {
+    __syncthreads();  // the node's flags and fallback are written
+    arrive_and_walk(a, c, ts);
+  }
+  if (CS > 1) cluster_wait();
 }
 
 }  // namespace spec
@@ -437,6 +430,8 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
   args.fallback = reinterpret_cast<int32_t *>(ws);
 
   if (greedy) return launch_verify_greedy(args, static_cast<cudaStream_t>(stream));
+  if (V <= kMaxCS * kRegChunk)
+    return launch_verify_reg(args, (V + kRegChunk - 1) / kRegChunk, static_cast<cudaStream_t>(stream));
   const size_t smem = sizeof(float) * 2 * static_cast<size_t>(chunk);
   static int configured_smem = -1;
   if (configured_smem < static_cast<int>(smem)) {
@@ -450,13 +445,14 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
   cfg.blockDim = dim3(kVThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  pdl_attribute(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, tree_verify_cluster_kernel, args) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }

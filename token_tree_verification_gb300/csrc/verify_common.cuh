@@ -37,7 +37,7 @@ struct VerifyArgs {
   int32_t *accept_len, *path_nodes, *out_tokens, *near_ties, *status;
   int32_t *flags;      // [T] written by the parent's CTA group: accept / tie bits
   int32_t *fallback;   // [T] token emitted on stopping at the node | tie << 31
-  uint32_t *done;      // [B] arrival counters, then one global counter at [B]
+  uint32_t *done;      // [B] arrival counters (zero between calls)
 };
 
 // A node's tree context, staged in shared memory by load_tree().
@@ -50,14 +50,16 @@ struct TreeSmem {
   float cP[SPEC_MAX_TREE_NODES];      // target logit of each child's token
   float cQ[SPEC_MAX_TREE_NODES];      // draft logit of each child's token
   float cU[SPEC_MAX_TREE_NODES];      // the accept-test uniform of each child
-  int warp_cnt[SPEC_MAX_TREE_NODES / 32];
-  int meta[4];                        // error, request
+  int wmatch[32];                     // per warp: the request found to own the node, or -1
+  int wbad[32];                       // per warp: the offsets break their contract
+  int meta[4];                        // error, child count, first node, node count
   float ufb;                          // the uniform of u's fallback draw
   int walk;
 };
 
 struct NodeCtx {
   int b, lo, n, u, k, err;
+  bool count;   // the node counts toward its request's arrivals (the offsets are valid)
 };
 
 // ---------------------------------------------------------------- reductions
@@ -119,7 +121,8 @@ __device__ __forceinline__ float precise_prob(float l, float M, float temp, floa
 static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, const int *spar,
                              const int *stok) {
   const int lane = threadIdx.x & 31;
-  if (*reinterpret_cast<volatile int32_t *>(a.status + b) != 0) return;
+  // the request's status, flags and fallbacks, all in one round trip
+  const int st = __ldcg(a.status + b);
   int par[4], flg[4], fbk[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
@@ -141,6 +144,7 @@ static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, c
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) maxd = max(maxd, __shfl_xor_sync(0xffffffffu, maxd, o));
+  if (__shfl_sync(0xffffffffu, st, 0) != 0) return;  // an error was reported for the request
   if (maxd + 1 > a.W) {
     if (lane == 0) report(a.status, b, SPEC_ERR_TREE_TOO_LARGE);
     return;
@@ -209,124 +213,151 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
 }
 
 
-// Every thread of the CTA (blockDim >= 256) calls this: find node t's
-// request, stage its parents and tokens, validate them, and list u's
-// children in index order.  Errors are identical in every CTA of a group.
-// A request holds at most 128 nodes, so the parents and tokens of nodes
-// t-127 .. t+127 are loaded in the same round as the offsets.
-static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  if (tid == 0) {
-    ts.meta[0] = 0;
-    ts.meta[1] = -1;
-  }
+// A node's tree context is read in one round trip: the parents and tokens of
+// nodes t-127 .. t+127 (a request holds at most 128 nodes) and the offsets.
+// tree_loads() issues this thread's share of those loads into registers, so
+// a kernel can issue them before its bulk row loads and let load_tree()
+// consume them afterwards.
+struct TreeLoads {
+  int par, tok, o0, o1;
+};
+
+__device__ __forceinline__ TreeLoads tree_loads(const VerifyArgs &a, int t) {
+  const int tid = threadIdx.x;
+  TreeLoads r{-2, 0, 0, 0};
   if (tid < kTreeWindow) {
     const int x = t - (SPEC_MAX_TREE_NODES - 1) + tid;
-    const bool in = x >= 0 && x < a.T;
-    ts.wpar[tid] = in ? __ldg(a.parents + x) : -2;
-    ts.wtok[tid] = in ? __ldg(a.tokens + x) : 0;
-  }
-  __syncthreads();
-  if (a.B < static_cast<int>(blockDim.x)) {
-    if (tid < a.B) {
-      const int o0 = __ldg(a.offsets + tid), o1 = __ldg(a.offsets + tid + 1);
-      if (o0 <= t && t < o1) atomicMax(&ts.meta[1], tid);
+    if (x >= 0 && x < a.T) {
+      r.par = __ldg(a.parents + x);
+      r.tok = __ldg(a.tokens + x);
     }
-  } else if (tid == 0) {
-    ts.meta[1] = find_request(a.offsets, a.B, t);
+  }
+  if (tid < a.B) {
+    r.o0 = __ldg(a.offsets + tid);
+    r.o1 = __ldg(a.offsets + tid + 1);
+  }
+  return r;
+}
+
+// Every thread of the CTA (blockDim >= 256) calls this with its
+// tree_loads(): find node t's request, stage its parents and tokens,
+// validate them, and list u's children in index order (one warp).  Errors
+// are identical in every CTA of a group.
+static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, const TreeLoads &ld) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  if (tid < kTreeWindow) {
+    ts.wpar[tid] = ld.par;
+    ts.wtok[tid] = ld.tok;
+  }
+  // The offsets must start at 0, never decrease and end at T; then exactly
+  // one request owns t.
+  int match = -1;
+  bool bad = false;
+  for (int i = tid; i < a.B; i += static_cast<int>(blockDim.x)) {
+    const int o0 = i == tid ? ld.o0 : __ldg(a.offsets + i);
+    const int o1 = i == tid ? ld.o1 : __ldg(a.offsets + i + 1);
+    bad |= (o1 < o0) || (i == 0 && o0 != 0) || (i == a.B - 1 && o1 != a.T);
+    if (o0 <= t && t < o1) {
+      match = i;
+      ts.meta[2] = o0;
+      ts.meta[3] = o1 - o0;
+    }
+  }
+  match = __reduce_max_sync(0xffffffffu, match);
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    ts.wmatch[w] = match;
+    ts.wbad[w] = bad ? 1 : 0;
   }
   __syncthreads();
+  match = __reduce_max_sync(0xffffffffu, lane < nwarps ? ts.wmatch[lane] : -1);
+  bad = __any_sync(0xffffffffu, lane < nwarps && ts.wbad[lane] != 0);
   NodeCtx c;
-  c.b = ts.meta[1];
+  c.b = match;
   c.lo = c.n = c.k = 0;
   c.err = 0;
-  if (c.b < 0) {
+  c.count = !bad && match >= 0;
+  if (!c.count) {
     c.err = SPEC_ERR_TREE_TOO_LARGE;
   } else {
-    c.lo = __ldg(a.offsets + c.b);
-    c.n = __ldg(a.offsets + c.b + 1) - c.lo;
-    if (c.lo < 0 || c.lo + c.n > a.T || c.n < 1 || c.n > SPEC_MAX_TREE_NODES)
-      c.err = SPEC_ERR_TREE_TOO_LARGE;
+    c.lo = ts.meta[2];
+    c.n = ts.meta[3];
+    if (c.n < 1 || c.n > SPEC_MAX_TREE_NODES) c.err = SPEC_ERR_TREE_TOO_LARGE;
   }
   c.u = t - c.lo;
-  bool is_child = false;
-  uint32_t child_bal = 0;
-  if (!c.err && tid < SPEC_MAX_TREE_NODES) {
-    if (tid < c.n) {
-      const int wi = c.lo + tid - (t - (SPEC_MAX_TREE_NODES - 1));   // in [0, 254]
-      const int p = ts.wpar[wi];
-      const int x = ts.wtok[wi];
-      ts.par[tid] = p;
-      ts.tok[tid] = x;
-      const bool ok = (tid == 0) ? (p == -1) : (p >= 0 && p < tid);
-      if (!ok) atomicCAS(&ts.meta[0], 0, SPEC_ERR_BAD_PARENT);
-      is_child = (tid > c.u && p == c.u);
-      if (is_child && (x < 0 || x >= a.V)) atomicCAS(&ts.meta[0], 0, SPEC_ERR_TOKEN_RANGE);
+  if (!c.err && w == 0) {
+    bool bad_parent = false, bad_token = false;
+    int k = 0;
+#pragma unroll
+    for (int s = 0; s < SPEC_MAX_TREE_NODES / 32; ++s) {
+      const int i = lane + 32 * s;
+      bool is_child = false;
+      if (i < c.n) {
+        const int wi = c.lo + i - (t - (SPEC_MAX_TREE_NODES - 1));   // in [0, 254]
+        const int p = ts.wpar[wi];
+        const int x = ts.wtok[wi];
+        ts.par[i] = p;
+        ts.tok[i] = x;
+        bad_parent |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
+        is_child = i > c.u && p == c.u;
+        bad_token |= is_child && (x < 0 || x >= a.V);
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, is_child);
+      if (is_child) ts.child[k + __popc(bal & ((1u << lane) - 1u))] = i;
+      k += __popc(bal);
     }
-    child_bal = __ballot_sync(0xffffffffu, is_child);
-    if (lane == 0) ts.warp_cnt[w] = __popc(child_bal);
-  }
-  __syncthreads();
-  if (!c.err) c.err = ts.meta[0];
-  if (!c.err) {
-    int before = 0;
-    for (int i = 0; i < SPEC_MAX_TREE_NODES / 32; ++i) {
-      if (i < w) before += ts.warp_cnt[i];
-      c.k += ts.warp_cnt[i];
+    bad_parent = __any_sync(0xffffffffu, bad_parent);
+    bad_token = __any_sync(0xffffffffu, bad_token);
+    if (lane == 0) {
+      ts.meta[0] = bad_parent ? SPEC_ERR_BAD_PARENT : (bad_token ? SPEC_ERR_TOKEN_RANGE : 0);
+      ts.meta[1] = k;
     }
-    if (is_child) ts.child[before + __popc(child_bal & ((1u << lane) - 1u))] = tid;
   }
   __syncthreads();  // child list complete
+  if (!c.err) {
+    c.err = ts.meta[0];
+    c.k = ts.meta[1];
+  }
+  if (c.err) c.k = 0;
   return c;
 }
 
-// Uniforms of the children's accept tests and of u's fallback draw, and the
-// children's logits at their tokens (stochastic mode), in parallel.
-__device__ __forceinline__ void load_children(const VerifyArgs &a, const NodeCtx &c, int t,
-                                              TreeSmem &ts) {
-  const int tid = threadIdx.x;
-  if (c.err || !(a.temp > 0.f)) return;
-  const float *trow = a.target + static_cast<size_t>(t) * a.V;
-  const float *drow = a.draft + static_cast<size_t>(t) * a.V;
-  if (tid < c.k) {
-    const int ch = ts.child[tid];
-    const int x = ts.tok[ch];
-    ts.cP[tid] = __ldg(trow + x);
-    ts.cQ[tid] = __ldg(drow + x);
-    ts.cU[tid] = spec_uniform(a.seed, ch, c.b, 0);
-  } else if (tid == static_cast<int>(blockDim.x) - 1) {
-    ts.ufb = spec_uniform(a.seed, c.u, c.b, 1);
-  }
-}
-
-// Called by every thread of one CTA per node group once the group's outputs
-// are written: the last group of a request walks it, and the last group of
-// the grid clears every counter for the next call.
-static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts, int ngroups) {
+// Called by every thread of the one CTA per node that publishes the node's
+// results, once they are written.  The last node of a request to arrive
+// walks it and clears the request's counter for the next call (with valid
+// offsets every node of the request arrives exactly once).
+static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts) {
   const int tid = threadIdx.x;
   if (tid == 0) {
-    __threadfence();
     int walk = 0;
-    if (c.b >= 0) {
-      const uint32_t prev = atomicAdd(a.done + c.b, 1u);
-      walk = (!c.err && static_cast<int>(prev) == c.n - 1) ? 1 : 0;
+    if (c.count) {
+      // release: this CTA's results (ordered before by the caller's barrier);
+      // acquire: every earlier arrival's results
+      uint32_t prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(a.done + c.b)
+                   : "memory");
+      if (static_cast<int>(prev) == c.n - 1) {
+        a.done[c.b] = 0u;
+        walk = c.err ? 0 : 1;
+      }
     }
     ts.walk = walk;
   }
   __syncthreads();
-  if (ts.walk) {
-    __threadfence();
-    if (tid < 32) walk_request(a, c.b, c.lo, c.n, ts.par, ts.tok);
-  }
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(a.done + a.B, 1u);
-    if (static_cast<int>(prev) == ngroups - 1)
-      for (int i = 0; i <= a.B; ++i) a.done[i] = 0u;
-  }
+  // The walker's loads are ordered after thread 0's acquire by the barrier
+  // and read L2 (ld.global.cg), where the other nodes' released results sit.
+  if (ts.walk && tid < 32) walk_request(a, c.b, c.lo, c.n, ts.par, ts.tok);
 }
 
 // greedy per-node kernel (verify_node.cu)
 int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream);
+
+// stochastic kernel with the rows in registers (verify_reg.cu): CTAs of
+// kRegChunk vocabulary entries, `cs` = ceil(V / kRegChunk) <= kMaxCS per node
+constexpr int kRegChunk = 16384;
+int launch_verify_reg(const VerifyArgs &args, int cs, cudaStream_t stream);
 
 }  // namespace spec

@@ -27,6 +27,9 @@ tree_verify_greedy_node_kernel(const VerifyArgs a) {
   const float *row = a.target + static_cast<size_t>(t) * a.V;
   const bool vec = ((a.V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0);
   const int n4 = vec ? a.V >> 2 : 0;
+  pdl_trigger();
+  pdl_wait();
+  const TreeLoads tl = tree_loads(a, t);
   // first batch of the row, in flight while the tree is read
   float4 pre[kGreedyPrefetch];
 #pragma unroll
@@ -35,7 +38,7 @@ tree_verify_greedy_node_kernel(const VerifyArgs a) {
     pre[e] = i < n4 ? __ldcs(reinterpret_cast<const float4 *>(row) + i)
                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   }
-  const NodeCtx c = load_tree(a, t, ts);
+  const NodeCtx c = load_tree(a, t, ts, tl);
   if (!c.err) {
     ArgMax am{-INFINITY, 0x7fffffff};
     if (vec) {
@@ -77,12 +80,20 @@ tree_verify_greedy_node_kernel(const VerifyArgs a) {
   } else if (tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }
-  arrive_and_walk(a, c, ts, gridDim.x);
+  arrive_and_walk(a, c, ts);
 }
 
 int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream) {
-  tree_verify_greedy_node_kernel<<<args.T, kGreedyThreads, 0, stream>>>(args);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(args.T), 1, 1);
+  cfg.blockDim = dim3(kGreedyThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  pdl_attribute(attr[0]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tree_verify_greedy_node_kernel, args) == cudaSuccess ? SPEC_OK
+                                                                                      : SPEC_ERR_CUDA;
 }
 
 }  // namespace spec

@@ -1,0 +1,465 @@
+// Steps V1-V4 and R for stochastic verification with the node's rows held in
+// registers: one thread-block cluster of CS = ceil(V / 16384) CTAs per node,
+// each CTA's 512 threads holding 32 entries of its slice of the target row
+// and, for internal nodes, of the draft row.
+//
+// Sources: speculative-decoding explainer (intelliparadigm.com) §2.2
+// 三阶段工作流程详解 — stage 2: accept probability alpha = min(1, p/q); stage 3:
+// check left to right, stop at the first rejection and replace it with a new
+// target prediction (output distribution equal to the target's).  SpecInfer
+// developer article §2.1: the accept stage keeps the longest verified prefix.
+//
+// Layout.  Warp w of the CTA at cluster rank r owns the 1024 vocabulary
+// entries [v0 + 1024 w, v0 + 1024 (w + 1)), v0 = 16384 r; lane l holds, for
+// steps m = 0..7, the four entries v0 + 1024 w + 128 m + 4 l + (0..3).  The
+// rows go from global memory straight into registers (coalesced 16-byte
+// loads), and every pass over the vocabulary is a register loop: no shared
+// memory traffic, and each warp's exponentials share the warp's own maximum,
+// so no CTA barrier is needed before the group totals.
+//
+// Group totals.  Every warp pushes its partial into slot [rank][warp] of
+// every CTA of the group with st.async; a round's mbarrier completes when all
+// CS x 16 partials have landed, and every warp adds them in the same order,
+// so all threads of the group hold bit-identical totals.
+//
+// The acceptance chain (residual in closed form, stop at the first accepted
+// child) and the inverse-CDF draw follow the description in verify.cu.
+#include "verify_common.cuh"
+
+namespace spec {
+
+namespace {
+
+constexpr int kRThreads = 512;
+constexpr int kRWarps = kRThreads / 32;
+constexpr int kRVec = 8;                     // float4 per thread per row
+constexpr int kRSpan = 32 * 4 * kRVec;       // vocabulary entries per warp
+static_assert(kRWarps * kRSpan == kRegChunk, "CTA slice");
+
+struct RegExchange {
+  float4 stat[kMaxCS][kRWarps];     // per warp: max target logit, sum of target exps, same for draft
+  float part[2][kMaxCS][kRWarps];   // reduction rounds, by round parity
+  int last[kRWarps];                // rare path: per warp, its last entry of positive weight
+};
+
+// 32 entries of a row into registers; entries at or past `end` read as -inf.
+__device__ __forceinline__ void load_row(const float *row, int base, int end, bool vec,
+                                         float4 (&x)[kRVec]) {
+#pragma unroll
+  for (int m = 0; m < kRVec; ++m) {
+    const int i = base + 128 * m;
+    if (vec && i + 3 < end) {
+      x[m] = __ldcs(reinterpret_cast<const float4 *>(row + i));
+    } else {
+      x[m].x = i < end ? __ldcs(row + i) : -INFINITY;
+      x[m].y = i + 1 < end ? __ldcs(row + i + 1) : -INFINITY;
+      x[m].z = i + 2 < end ? __ldcs(row + i + 2) : -INFINITY;
+      x[m].w = i + 3 < end ? __ldcs(row + i + 3) : -INFINITY;
+    }
+  }
+}
+
+__device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
+
+// The residual weight of one entry: max(0, p - c q), or p while c == 0.
+__device__ __forceinline__ float resid(float p, float q, float c) {
+  return c != 0.f ? fmaxf(0.f, fmaf(-c, q, p)) : p;
+}
+
+__device__ __forceinline__ float sum4_resid(float4 p, float4 q, float c) {
+  return (resid(p.x, q.x, c) + resid(p.y, q.y, c)) + (resid(p.z, q.z, c) + resid(p.w, q.w, c));
+}
+
+__device__ __forceinline__ float pick4(const float4 v, int c) {
+  return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ float pick_slot(const float (&v)[4], int s) {
+  return s == 0 ? v[0] : (s == 1 ? v[1] : (s == 2 ? v[2] : v[3]));
+}
+
+__device__ __forceinline__ float warp_scan(float v, int lane) {  // inclusive
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kRThreads, 1)
+tree_verify_reg_kernel(const VerifyArgs a) {
+  __shared__ __align__(16) RegExchange ex;
+  __shared__ TreeSmem ts;
+  __shared__ __align__(8) uint64_t xbar[3];   // exchange: statistics round, rounds by parity
+
+  const int CS = static_cast<int>(cluster_size());
+  const int rank = static_cast<int>(cluster_rank());
+  const int t = blockIdx.x / CS;
+  const int tid = threadIdx.x, w_id = tid >> 5, lane = tid & 31;
+  const int v0 = rank * kRegChunk;
+  const int end = min(a.V, v0 + kRegChunk);     // this CTA's slice is [v0, end)
+  const int base = v0 + w_id * kRSpan + 4 * lane;
+  const bool vec = ((a.V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(a.draft) & 15) == 0);
+  const float *trow = a.target + static_cast<size_t>(t) * a.V;
+  const float *drow = a.draft + static_cast<size_t>(t) * a.V;
+
+  pdl_trigger();
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&xbar[i], 1);
+    fence_barrier_init();
+  }
+  pdl_wait();
+  // the tree first, then the target row, straight into registers
+  const TreeLoads tl = tree_loads(a, t);
+  float4 xp[kRVec], xq[kRVec];
+  load_row(trow, base, end, vec, xp);
+  if (CS > 1) cluster_arrive_relaxed();   // waited for before the first remote store
+  const NodeCtx c = load_tree(a, t, ts, tl);
+  const int k = c.k;
+  const bool need_draft = !c.err && k > 0;   // leaves never read their draft row
+  if (need_draft) {
+    load_row(drow, base, end, vec, xq);
+  } else {
+#pragma unroll
+    for (int m = 0; m < kRVec; ++m) xq[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // the fallback draw's uniform (used only if the walk can stop here), and
+  // child j's raw logits and accept uniform in lane j % 32, slot j / 32 —
+  // computed while the row loads are in flight
+  const float u_fb = c.err ? 0.f : spec_uniform(a.seed, c.u, c.b, 1);
+  float cP[4], cQ[4], cU[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int j = lane + 32 * s;
+    cP[s] = cQ[s] = cU[s] = 0.f;
+    if (!c.err && j < k) {
+      const int ch = ts.child[j];
+      const int x = ts.tok[ch];
+      cP[s] = __ldg(trow + x);
+      cQ[s] = __ldg(drow + x);
+      cU[s] = spec_uniform(a.seed, ch, c.b, 0);
+    }
+  }
+  if (tid == 0 && !c.err) mbar_arrive_expect_tx(&xbar[0], static_cast<uint32_t>(CS * kRWarps * 16));
+  if (CS > 1) cluster_wait();  // every CTA of the group is running
+
+  bool ok = true;
+  int stop = k;        // first accepted child, k when every child is rejected
+  int my_flag = 0;     // thread j < k: the flag of child j
+  int p_ok = -1;       // parity of the last reduction round that moved the residual
+  float c_prev = 0.f, Ml = 0.f, Sp = 1.f;
+  const float l2s = a.inv_temp * 1.4426950408889634f;  // exp(x / T) = 2^(x * l2s)
+  if (!c.err) {
+    // ---- V1: the warp's maxima, exponentials in place, the warp's sums
+    float ml = -INFINITY, md = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < kRVec; ++m) {
+      ml = fmaxf(ml, max4(xp[m]));
+      md = fmaxf(md, max4(xq[m]));
+    }
+    ml = warp_max(ml);
+    md = need_draft ? warp_max(md) : -INFINITY;
+    const float nl = ml == -INFINITY ? 0.f : -ml * l2s;
+    const float nd = md == -INFINITY ? 0.f : -md * l2s;
+    float sl = 0.f, sd = 0.f;
+#pragma unroll
+    for (int m = 0; m < kRVec; ++m) {
+      xp[m].x = fast_exp2(fmaf(xp[m].x, l2s, nl));
+      xp[m].y = fast_exp2(fmaf(xp[m].y, l2s, nl));
+      xp[m].z = fast_exp2(fmaf(xp[m].z, l2s, nl));
+      xp[m].w = fast_exp2(fmaf(xp[m].w, l2s, nl));
+      sl += (xp[m].x + xp[m].y) + (xp[m].z + xp[m].w);
+      if (need_draft) {
+        xq[m].x = fast_exp2(fmaf(xq[m].x, l2s, nd));
+        xq[m].y = fast_exp2(fmaf(xq[m].y, l2s, nd));
+        xq[m].z = fast_exp2(fmaf(xq[m].z, l2s, nd));
+        xq[m].w = fast_exp2(fmaf(xq[m].w, l2s, nd));
+        sd += (xq[m].x + xq[m].y) + (xq[m].z + xq[m].w);
+      }
+    }
+    sl = warp_sum(sl);
+    sd = warp_sum(sd);
+    if (lane < CS)
+      st_async_v4_f32(peer_addr(&ex.stat[rank][w_id], lane), make_float4(ml, sl, md, sd),
+                      peer_addr(&xbar[0], lane));
+    if (!mbar_wait(&xbar[0], 0)) ok = false;
+    // group maxima and sums, added in the same order by every warp
+    const int nslot = CS * kRWarps;
+    const float4 *flat = &ex.stat[0][0];
+    float4 e[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int i = lane + 32 * s;
+      e[s] = i < nslot ? flat[i] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    }
+    float Mx = -INFINITY, Mdx = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      Mx = fmaxf(Mx, e[s].x);
+      Mdx = fmaxf(Mdx, e[s].z);
+    }
+    Ml = warp_max(Mx);
+    const float Md = warp_max(Mdx);
+    float sp = 0.f, sq = 0.f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (e[s].y > 0.f) sp += e[s].y * fast_exp2((e[s].x - Ml) * l2s);
+      if (need_draft && e[s].w > 0.f) sq += e[s].w * fast_exp2((e[s].z - Md) * l2s);
+    }
+    Sp = warp_sum(sp);
+    const float Sq = warp_sum(sq);
+    // this warp's entries become p and q
+    const float inv_sp = 1.f / Sp;
+    const float inv_sq = need_draft ? 1.f / Sq : 0.f;
+    const float sc_l = ml == -INFINITY ? 0.f : fast_exp2((ml - Ml) * l2s) * inv_sp;
+    const float sc_d = (need_draft && md != -INFINITY) ? fast_exp2((md - Md) * l2s) * inv_sq : 0.f;
+#pragma unroll
+    for (int m = 0; m < kRVec; ++m) {
+      xp[m].x *= sc_l; xp[m].y *= sc_l; xp[m].z *= sc_l; xp[m].w *= sc_l;
+      xq[m].x *= sc_d; xq[m].y *= sc_d; xq[m].z *= sc_d; xq[m].w *= sc_d;
+    }
+    // the children's p and q from their raw logits
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (lane + 32 * s < k) {
+        cP[s] = precise_prob(cP[s], Ml, a.temp, a.inv_temp, 1.f) * inv_sp;
+        cQ[s] = precise_prob(cQ[s], Md, a.temp, a.inv_temp, 1.f) * inv_sq;
+      }
+    }
+
+    // ---- V2: the children's accept tests in index order, stopping at the
+    //      first accepted child (the walk never looks past it).  The test
+    //      u < min(1, num / den) is taken as u * den < num, without a division.
+    float W_prev = 1.f;
+    bool frozen = false;   // a residual that summed to zero stays as it is
+    int rounds = 0;
+    for (int j = 0; j < k; ++j) {
+      const int sl_ = j >> 5, src = j & 31;
+      const float P = __shfl_sync(0xffffffffu, pick_slot(cP, sl_), src);
+      const float Q = __shfl_sync(0xffffffffu, pick_slot(cQ, sl_), src);
+      const float U = __shfl_sync(0xffffffffu, pick_slot(cU, sl_), src);
+      bool accept, tie;
+      const float num = fmaxf(0.f, fmaf(-c_prev, Q, P));
+      const float den = W_prev * Q;
+      if (Q > 0.f && num < den) {
+        const float d = fmaf(U, den, -num);
+        accept = d < 0.f;
+        tie = fabsf(d) < kTieBand * den;
+      } else {  // alpha = 1
+        accept = true;
+        tie = 1.f - U < kTieBand;
+      }
+      if (tid == j) my_flag = (accept ? kFlagAccept : 0) | (tie ? kFlagTie : 0);
+      if (accept) {
+        stop = j;
+        break;
+      }
+      if (frozen) continue;
+      // rejected: r becomes max(0, p - c q) / W(c) with c = c_prev + W_prev
+      const float c_new = c_prev + W_prev;
+      float wsum = 0.f;
+#pragma unroll
+      for (int m = 0; m < kRVec; ++m) wsum += sum4_resid(xp[m], xq[m], c_new);
+      wsum = warp_sum(wsum);
+      const int p = rounds & 1;
+      if (tid == 0) mbar_arrive_expect_tx(&xbar[1 + p], static_cast<uint32_t>(CS * kRWarps * 4));
+      if (lane < CS)
+        st_async_f32(peer_addr(&ex.part[p][rank][w_id], lane), wsum, peer_addr(&xbar[1 + p], lane));
+      if (ok && !mbar_wait(&xbar[1 + p], (rounds >> 1) & 1)) ok = false;
+      ++rounds;
+      const float *fl = &ex.part[p][0][0];
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int i = lane + 32 * s;
+        if (i < nslot) acc += fl[i];
+      }
+      const float Wn = warp_sum(acc);
+      if (Wn > 0.f) {
+        c_prev = c_new;
+        W_prev = Wn;
+        p_ok = p;
+      } else {
+        frozen = true;
+      }
+    }
+  }
+  // No CTA touches a peer's shared memory after this point: arrive now, wait
+  // before exiting, so that no CTA leaves while a peer may still store to it.
+  if (CS > 1) cluster_arrive_relaxed();
+  if (!ok && tid == 0) report(a.status, c.b, SPEC_ERR_TIMEOUT);
+
+  int writer = 0;  // the CTA of the group that publishes the node's results
+  if (!c.err) {
+    // ---- V3: when every child is rejected (or u is a leaf), the token
+    //      emitted on stopping here: inverse CDF of r ∝ max(0, p - c q)
+    if (stop == k) {
+      // the mass of warp w of slice r under the final residual
+      auto mass = [&](int r, int w) -> float {
+        if (p_ok >= 0) return ex.part[p_ok][r][w];
+        const float4 e = ex.stat[r][w];
+        return e.y > 0.f ? e.y * fast_exp2((e.x - Ml) * l2s) / Sp : 0.f;
+      };
+      float slice[kMaxCS];
+      float total = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxCS; ++r) {
+        slice[r] = r < CS ? warp_sum(lane < kRWarps ? mass(r, lane) : 0.f) : 0.f;
+        total += slice[r];
+      }
+      const float target = u_fb * total;
+      int owner = -1;
+      float prefix = 0.f, run = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxCS; ++r) {
+        if (owner < 0 && r < CS && run + slice[r] > target) {
+          owner = r;
+          prefix = run;
+        }
+        run += slice[r];
+      }
+      if (owner < 0) {  // rounding kept the running sum below the target
+        run = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCS; ++r) {
+          if (r < CS && slice[r] > 0.f) {
+            owner = r;
+            prefix = run;
+          }
+          run += slice[r];
+        }
+        if (owner < 0) owner = 0;
+      }
+      writer = owner;
+      if (rank == owner) {
+        // level 1: the slice's 16 warp ranges
+        const float v1 = lane < kRWarps ? mass(rank, lane) : 0.f;
+        const float inc1 = warp_scan(v1, lane);
+        const uint32_t hit1 = __ballot_sync(0xffffffffu, lane < kRWarps && prefix + inc1 > target);
+        const int sw = hit1 ? __ffs(hit1) - 1 : -1;
+        if (sw >= 0 && w_id == sw) {
+          float run2 = __shfl_sync(0xffffffffu, prefix + inc1 - v1, sw);
+          // level 2: the warp's eight 128-entry steps
+          float ls[kRVec];
+#pragma unroll
+          for (int m = 0; m < kRVec; ++m) ls[m] = sum4_resid(xp[m], xq[m], c_prev);
+          int ms = -1;
+          float before = run2;
+#pragma unroll
+          for (int m = 0; m < kRVec; ++m) {
+            const float cs_ = warp_sum(ls[m]);
+            if (ms < 0 && run2 + cs_ > target) {
+              ms = m;
+              before = run2;
+            }
+            run2 += cs_;
+          }
+          int pick = -1;
+          float cb0 = target, cb1 = target;
+          if (ms >= 0) {
+            // level 3: the step's lanes; level 4: the lane's four entries
+            float lsv = 0.f;
+#pragma unroll
+            for (int m = 0; m < kRVec; ++m) if (m == ms) lsv = ls[m];
+            const float inc3 = warp_scan(lsv, lane);
+            const uint32_t hit3 = __ballot_sync(0xffffffffu, before + inc3 > target);
+            if (hit3) {
+              const int L = __ffs(hit3) - 1;
+              if (lane == L) {
+                float4 pp = xp[0], qq = xq[0];
+#pragma unroll
+                for (int m = 1; m < kRVec; ++m) if (m == ms) { pp = xp[m]; qq = xq[m]; }
+                float cum = before + inc3 - lsv;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                  const float wv = resid(pick4(pp, cc), pick4(qq, cc), c_prev);
+                  if (pick < 0 && cum + wv > target) {
+                    pick = base + 128 * ms + cc;
+                    cb0 = cum;
+                    cb1 = cum + wv;
+                  }
+                  cum += wv;
+                }
+                if (pick < 0) {  // rounding: the lane's last entry of positive weight
+                  for (int cc = 3; cc >= 0 && pick < 0; --cc)
+                    if (resid(pick4(pp, cc), pick4(qq, cc), c_prev) > 0.f) pick = base + 128 * ms + cc;
+                  if (pick < 0) pick = base + 128 * ms;
+                  cb0 = cb1 = target;
+                }
+              }
+              pick = __shfl_sync(0xffffffffu, pick, L);
+              cb0 = __shfl_sync(0xffffffffu, cb0, L);
+              cb1 = __shfl_sync(0xffffffffu, cb1, L);
+            }
+          }
+          if (pick < 0) {
+            // rounding: the warp range's last entry of positive weight
+            int mine = -1;
+#pragma unroll
+            for (int m = 0; m < kRVec; ++m)
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                if (resid(pick4(xp[m], cc), pick4(xq[m], cc), c_prev) > 0.f) mine = base + 128 * m + cc;
+            pick = __reduce_max_sync(0xffffffffu, mine);
+            if (pick < 0) pick = v0 + sw * kRSpan;
+            cb0 = cb1 = target;
+          }
+          if (lane == 0) {
+            const bool tie = fabsf(target - cb0) < kTieBand * total || fabsf(target - cb1) < kTieBand * total;
+            a.fallback[t] = pick | (tie ? (1 << 31) : 0);
+          }
+        } else if (sw < 0) {
+          // rounding: the slice's last entry of positive weight
+          int mine = -1;
+#pragma unroll
+          for (int m = 0; m < kRVec; ++m)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              if (resid(pick4(xp[m], cc), pick4(xq[m], cc), c_prev) > 0.f) mine = base + 128 * m + cc;
+          mine = __reduce_max_sync(0xffffffffu, mine);
+          if (lane == 0) ex.last[w_id] = mine;
+          __syncthreads();
+          if (tid == 0) {
+            int pick = -1;
+            for (int w = 0; w < kRWarps; ++w) pick = max(pick, ex.last[w]);
+            if (pick < 0) pick = v0;
+            a.fallback[t] = pick | (1 << 31);
+          }
+        }
+      }
+    }
+    // every CTA computed the same decisions; the writer publishes them
+    if (rank == writer && tid < k) a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
+  } else if (rank == 0 && tid == 0 && c.b >= 0) {
+    report(a.status, c.b, c.err);
+  }
+  if (rank == writer) {
+    __syncthreads();  // the node's flags and fallback are written
+    arrive_and_walk(a, c, ts);
+  }
+  if (CS > 1) cluster_wait();
+}
+
+int launch_verify_reg(const VerifyArgs &args, int cs, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(args.T) * cs, 1, 1);
+  cfg.blockDim = dim3(kRThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  pdl_attribute(attr[1]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, tree_verify_reg_kernel, args) == cudaSuccess ? SPEC_OK
+                                                                              : SPEC_ERR_CUDA;
+}
+
+}  // namespace spec
