@@ -30,10 +30,10 @@
 // at the end).  The single P operand leaves room for a 4-stage K/V ring.
 // Outputs leave through a shared-memory staging buffer so global stores are
 // coalesced.  The key splits of a block form one thread-block cluster: each
-// split stages its (m, l, O) rows in shared memory and, after a cluster
-// barrier, merges its share of the rows by reading every peer's staging
-// through distributed shared memory (a cluster stays on one die, so no
-// cross-die L2 round trip is involved).
+// split stages its (O, m, l) rows in shared memory, and after a cluster
+// barrier sends each row's owner that owner's rows with one bulk
+// shared-to-shared copy; owners merge locally (a cluster stays on one die,
+// so no cross-die L2 round trip is involved).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -74,6 +74,11 @@ struct TcCfg {
   static_assert(!PACKED || kTcRows / 2 * D * 4 <= 2 * kPParts * kPBytes,
                 "packed remainder exchange fits the P buffers");
   static_assert(kTcRows * kStage * 4 <= kStages * kStageBytes, "output staging fits the K/V ring");
+  // staged rows plus the receive slots of the split merge, in the ring and P buffers
+  static_assert((2 * (PACKED ? kTcRows / 2 : kTcRows) + 8) * kStage * 4 <=
+                    kStages * kStageBytes + 2 * kPParts * kPBytes,
+                "split-merge buffers fit");
+  static_assert(kOffP == kOffKV + kStages * kStageBytes, "ring and P buffers are contiguous");
   static_assert(kSmem <= 227 * 1024 - 8192, "shared memory budget");
 };
 
@@ -108,7 +113,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   __shared__ uint32_t s_tmem;
   __shared__ float x_max[2][C::kParts][kTcRows];   // [tile parity][key part][row]
   __shared__ float x_l[C::kParts][kTcRows];
-  __shared__ float s_ml[kTcRows][2];               // per row: reference max, sum
+  __shared__ __align__(8) uint64_t bar_m;          // key splits: the peers' rows have arrived
   __shared__ int s_timeout;
 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -129,6 +134,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       mbar_init(&bar_empty[s], 1);
     }
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_m, 1);
     for (int j = 0; j < 3; ++j) mbar_init(&bar_s[j], 1);
     for (int j = 0; j < 2; ++j) {
       mbar_init(&bar_p[j], kTcSoftmaxWarps);
@@ -402,12 +408,17 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         for (int e = 0; e < 32; ++e) o_keep[c * 32 + e] = o[e];
       }
     }
-    float *xo = reinterpret_cast<float *>(smem + C::kOffP);   // [64 rows][D], P buffers are free
+    // [64 rows][D] floats in the free P buffers; 16-byte chunks swizzled by
+    // row so that eight consecutive rows hit eight different bank groups
+    float *xo = reinterpret_cast<float *>(smem + C::kOffP);
+    auto xo_at = [&](int e) -> float4 * {
+      const int chunk = (half * (D / 2) + e) >> 2;
+      return reinterpret_cast<float4 *>(xo + srow * D) + (chunk ^ (srow & 7));
+    };
     if (PACKED && lo_lane && row_ok) {
 #pragma unroll
       for (int e = 0; e < D / 2; e += 4)
-        *reinterpret_cast<float4 *>(xo + srow * D + half * (D / 2) + e) =
-            make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
+        *xo_at(e) = make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
     }
     if (warp >= 2) x_l[part][srow] = l_part;
     named_bar_sync(2, 32 * kTcSoftmaxWarps);
@@ -417,22 +428,22 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       if (PACKED) {
 #pragma unroll
         for (int e = 0; e < D / 2; e += 4) {
-          const float4 v = *reinterpret_cast<const float4 *>(xo + srow * D + half * (D / 2) + e);
+          const float4 v = *xo_at(e);
           o_keep[e] += v.x;
           o_keep[e + 1] += v.y;
           o_keep[e + 2] += v.z;
           o_keep[e + 3] += v.w;
         }
       }
-      // stage the row for coalesced stores (the K/V ring is free)
-      float *stg = reinterpret_cast<float *>(smem + C::kOffKV) + srow * C::kStage + half * (D / 2);
+      // stage the row, O then (m, l), for coalesced stores or the split
+      // merge (the K/V ring is free)
+      float *stg = reinterpret_cast<float *>(smem + C::kOffKV) + srow * C::kStage;
 #pragma unroll
       for (int e = 0; e < D / 2; e += 4)
-        *reinterpret_cast<float4 *>(stg + e) = make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
-      if (half == 0) {
-        s_ml[srow][0] = ntiles > 0 ? m_used : -INFINITY;
-        s_ml[srow][1] = l_row;
-      }
+        *reinterpret_cast<float4 *>(stg + half * (D / 2) + e) =
+            make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
+      if (half == 0) *reinterpret_cast<float2 *>(stg + D) = make_float2(ntiles > 0 ? m_used : -INFINITY, l_row);
+      fence_proxy_async_smem();  // the rows may leave by bulk copy
     }
   }
 
@@ -451,7 +462,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     const int nv = rows_here * (D / 8);
     for (int idx = tid; idx < nv; idx += kTcThreads) {
       const int lr = idx / (D / 8), c8 = idx % (D / 8);
-      const float inv = 1.f / s_ml[lr][1];
+      const float inv = 1.f / stg[lr * C::kStage + D + 1];
       const float4 v0 = *reinterpret_cast<const float4 *>(stg + lr * C::kStage + c8 * 8);
       const float4 v1 = *reinterpret_cast<const float4 *>(stg + lr * C::kStage + c8 * 8 + 4);
       uint4 pk;
@@ -466,52 +477,61 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     return;
   }
-  // ---- key splits: the CTAs of this block's cluster pull each other's
-  //      staged rows through distributed shared memory; CTA `split` merges
-  //      rows [split * rpr, (split + 1) * rpr)
-  cluster_sync_all();  // every split has staged its rows
+  // ---- key splits.  CTA `split` owns rows [split * rpr, ...) of the block.
+  //      After a cluster barrier (every split has staged its rows, every K/V
+  //      ring is free), each CTA sends every owner that owner's rows with one
+  //      bulk shared-to-shared copy into the owner's receive slot [sender],
+  //      completing on the owner's barrier; each owner merges locally.
+  const int rpr = (rows_here + CS - 1) / CS;
+  auto own_range = [&](int r, int &r0, int &rn) {
+    r0 = min(rows_here, r * rpr);
+    rn = min(rows_here, r0 + rpr) - r0;
+  };
+  int own0, own_n;
+  own_range(split, own0, own_n);
+  float *recv = const_cast<float *>(stg) + rows_here * C::kStage;   // [CS][rpr][kStage]
+  cluster_sync_all();
+  if (tid == 0) {
+    if (own_n > 0) mbar_arrive_expect_tx(&bar_m, static_cast<uint32_t>((CS - 1) * own_n * C::kStage * 4));
+    for (int r = 0; r < CS; ++r) {
+      int r0, rn;
+      own_range(r, r0, rn);
+      if (r == split || rn <= 0) continue;
+      bulk_copy_s2s(peer_addr(recv + split * rpr * C::kStage, r), smem_addr(stg + r0 * C::kStage),
+                    static_cast<uint32_t>(rn * C::kStage * 4), peer_addr(&bar_m, r));
+    }
+  }
+  if (own_n > 0 && !mbar_wait(&bar_m, 0) && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
+  cluster_arrive_relaxed();  // everything addressed to this CTA has arrived
   {
-    const int rpr = (rows_here + CS - 1) / CS;
-    const int r_begin = split * rpr, r_end = min(rows_here, r_begin + rpr);
     constexpr int kE = D / 8;   // columns per task
-    const int ntask = max(0, r_end - r_begin) * 8;
+    const int ntask = own_n * 8;
     for (int task = tid; task < ntask; task += kTcThreads) {
-      const int lr = r_begin + (task >> 3);
+      const int j = task >> 3;
+      const int lr = own0 + j;
       const int col0 = (task & 7) * kE;
-      float mls[kTcMaxSplits][2];
-      float4 ov[kTcMaxSplits][kE / 4];
-      // every peer's loads are issued before any is used
-#pragma unroll
-      for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
-        if (s2 < CS) {
-          const uint32_t pml = peer_addr(&s_ml[lr][0], s2);
-          mls[s2][0] = ld_peer_f32(pml);
-          mls[s2][1] = ld_peer_f32(pml + 4);
-          const uint32_t prow = peer_addr(stg + lr * C::kStage + col0, s2);
-#pragma unroll
-          for (int q4 = 0; q4 < kE / 4; ++q4) ov[s2][q4] = ld_peer_f32x4(prow + 16 * q4);
-        }
-      }
+      auto part = [&](int q) -> const float * {
+        return q == split ? stg + lr * C::kStage : recv + (q * rpr + j) * C::kStage;
+      };
       float M = -INFINITY;
-#pragma unroll
-      for (int s2 = 0; s2 < kTcMaxSplits; ++s2)
-        if (s2 < CS) M = fmaxf(M, mls[s2][0]);
+      for (int q = 0; q < CS; ++q) M = fmaxf(M, part(q)[D]);
       float acc[kE];
 #pragma unroll
       for (int e = 0; e < kE; ++e) acc[e] = 0.f;
       float L = 0.f;
+      for (int q = 0; q < CS; ++q) {
+        const float *row = part(q);
+        const float2 ml = *reinterpret_cast<const float2 *>(row + D);
+        if (ml.x == -INFINITY) continue;
+        const float w = exp2f(ml.x - M);
+        L += w * ml.y;
 #pragma unroll
-      for (int s2 = 0; s2 < kTcMaxSplits; ++s2) {
-        if (s2 < CS && mls[s2][0] != -INFINITY) {
-          const float w = exp2f(mls[s2][0] - M);
-          L += w * mls[s2][1];
-#pragma unroll
-          for (int q4 = 0; q4 < kE / 4; ++q4) {
-            acc[4 * q4 + 0] += w * ov[s2][q4].x;
-            acc[4 * q4 + 1] += w * ov[s2][q4].y;
-            acc[4 * q4 + 2] += w * ov[s2][q4].z;
-            acc[4 * q4 + 3] += w * ov[s2][q4].w;
-          }
+        for (int q4 = 0; q4 < kE / 4; ++q4) {
+          const float4 v = *reinterpret_cast<const float4 *>(row + col0 + 4 * q4);
+          acc[4 * q4 + 0] += w * v.x;
+          acc[4 * q4 + 1] += w * v.y;
+          acc[4 * q4 + 2] += w * v.z;
+          acc[4 * q4 + 3] += w * v.w;
         }
       }
       const float inv = 1.f / L;
@@ -529,7 +549,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       }
     }
   }
-  cluster_sync_all();  // peers are done reading this CTA's shared memory
+  cluster_wait();  // no CTA leaves while a copy may still read its rows
 }
 
 // Split plan: the split count (cluster size) that minimises (waves x tiles
