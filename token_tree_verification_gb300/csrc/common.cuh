@@ -252,6 +252,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^x for x <= 0 on the FMA pipe, so that exponential-heavy loops can split
+// their work between it and the MUFU pipe (fast_exp2).  Range reduction to
+// the nearest integer, x = n + f with |f| <= 1/2, then the degree-7 Taylor
+// polynomial of e^(f ln 2) (coefficients (ln 2)^k / k!; truncation error below
+// 1e-8 relative on the interval), scaled by 2^n through the exponent field.
+// Results below 2^-126 flush to zero, as with ex2.approx.ftz.
+__device__ __forceinline__ float exp2_taylor(float x) {
+  x = fmaxf(x, -127.f);
+  const float n = rintf(x);
+  const float f = x - n;
+  float p = 1.5252733804059838e-05f;
+  p = fmaf(p, f, 1.5403530393381606e-04f);
+  p = fmaf(p, f, 1.3333558146428441e-03f);
+  p = fmaf(p, f, 9.6181291076284770e-03f);
+  p = fmaf(p, f, 5.5504108664821576e-02f);
+  p = fmaf(p, f, 2.4022650695910071e-01f);
+  p = fmaf(p, f, 6.9314718055994531e-01f);
+  p = fmaf(p, f, 1.0f);
+  return p * __int_as_float((static_cast<int>(n) + 127) << 23);
+}
+
 // ---------------------------------------------------------------- Philox
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11, "Parallel Random Numbers:
 // As Easy as 1, 2, 3").  Each round multiplies counter words 0 and 2 by the

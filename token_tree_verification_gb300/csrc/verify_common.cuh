@@ -239,11 +239,10 @@ __device__ __forceinline__ TreeLoads tree_loads(const VerifyArgs &a, int t) {
   return r;
 }
 
-// Every thread of the CTA (blockDim >= 256) calls this with its
-// tree_loads(): find node t's request, stage its parents and tokens,
-// validate them, and list u's children in index order (one warp).  Errors
-// are identical in every CTA of a group.
-static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, const TreeLoads &ld) {
+// Phase A of load_tree, called by every thread of the CTA (blockDim >= 256)
+// with its tree_loads(): stage the window and find node t's request.  One
+// barrier.
+static __device__ NodeCtx load_tree_a(const VerifyArgs &a, int t, TreeSmem &ts, const TreeLoads &ld) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int nwarps = static_cast<int>(blockDim.x >> 5);
   if (tid < kTreeWindow) {
@@ -286,6 +285,28 @@ static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, co
     if (c.n < 1 || c.n > SPEC_MAX_TREE_NODES) c.err = SPEC_ERR_TREE_TOO_LARGE;
   }
   c.u = t - c.lo;
+  return c;
+}
+
+// Whether u has a child, from the staged window (nodes t+1 .. t+127 of the
+// request whose parent is u); every warp computes it, no barrier.  Exact for
+// a valid tree; load_tree_b() validates.
+__device__ __forceinline__ bool has_children(const NodeCtx &c, int t, const TreeSmem &ts) {
+  if (c.err) return false;
+  const int lane = threadIdx.x & 31;
+  bool hit = false;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int j = lane + 32 * s;   // node t + 1 + j, window slot 128 + j
+    if (j < SPEC_MAX_TREE_NODES - 1 && t + 1 + j < c.lo + c.n) hit |= ts.wpar[SPEC_MAX_TREE_NODES + j] == c.u;
+  }
+  return __any_sync(0xffffffffu, hit);
+}
+
+// Phase B: one warp validates the request's parents and children's tokens
+// and lists u's children in index order.  One barrier.
+static __device__ NodeCtx load_tree_b(const VerifyArgs &a, int t, TreeSmem &ts, NodeCtx c) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (!c.err && w == 0) {
     bool bad_parent = false, bad_token = false;
     int k = 0;
@@ -321,6 +342,12 @@ static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, co
   }
   if (c.err) c.k = 0;
   return c;
+}
+
+// Both phases: find node t's request, stage its parents and tokens, validate
+// them, and list u's children.  Errors are identical in every CTA of a group.
+static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, const TreeLoads &ld) {
+  return load_tree_b(a, t, ts, load_tree_a(a, t, ts, ld));
 }
 
 // Called by every thread of the one CTA per node that publishes the node's

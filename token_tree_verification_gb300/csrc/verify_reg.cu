@@ -42,6 +42,14 @@ struct RegExchange {
   int last[kRWarps];                // rare path: per warp, its last entry of positive weight
 };
 
+// The node's scalars, computed once by the CTA's last warp: the children's
+// p(x), q(x) and accept uniforms, and the fallback draw's uniform.
+struct NodeScalars {
+  float P[SPEC_MAX_TREE_NODES], Q[SPEC_MAX_TREE_NODES], U[SPEC_MAX_TREE_NODES];
+  float u_fb;
+};
+constexpr int kScalarWarp = kRWarps - 1;
+
 // 32 entries of a row into registers; entries at or past `end` read as -inf.
 __device__ __forceinline__ void load_row(const float *row, int base, int end, bool vec,
                                          float4 (&x)[kRVec]) {
@@ -74,10 +82,6 @@ __device__ __forceinline__ float pick4(const float4 v, int c) {
   return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
 }
 
-__device__ __forceinline__ float pick_slot(const float (&v)[4], int s) {
-  return s == 0 ? v[0] : (s == 1 ? v[1] : (s == 2 ? v[2] : v[3]));
-}
-
 __device__ __forceinline__ float warp_scan(float v, int lane) {  // inclusive
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -93,7 +97,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
 tree_verify_reg_kernel(const VerifyArgs a) {
   __shared__ __align__(16) RegExchange ex;
   __shared__ TreeSmem ts;
+  __shared__ NodeScalars ns;
   __shared__ __align__(8) uint64_t xbar[3];   // exchange: statistics round, rounds by parity
+  __shared__ __align__(8) uint64_t nbar;      // the node's scalars are in `ns`
 
   const int CS = static_cast<int>(cluster_size());
   const int rank = static_cast<int>(cluster_rank());
@@ -110,6 +116,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   pdl_trigger();
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) mbar_init(&xbar[i], 1);
+    mbar_init(&nbar, 1);
     fence_barrier_init();
   }
   pdl_wait();
@@ -118,30 +125,39 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   float4 xp[kRVec], xq[kRVec];
   load_row(trow, base, end, vec, xp);
   if (CS > 1) cluster_arrive_relaxed();   // waited for before the first remote store
-  const NodeCtx c = load_tree(a, t, ts, tl);
-  const int k = c.k;
-  const bool need_draft = !c.err && k > 0;   // leaves never read their draft row
-  if (need_draft) {
+  const NodeCtx ca = load_tree_a(a, t, ts, tl);
+  // Internal nodes only: the draft row is requested as soon as the staged
+  // window shows a child, before the tree is validated.
+  const bool early_draft = has_children(ca, t, ts);
+  if (early_draft) {
     load_row(drow, base, end, vec, xq);
   } else {
 #pragma unroll
     for (int m = 0; m < kRVec; ++m) xq[m] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // the fallback draw's uniform (used only if the walk can stop here), and
-  // child j's raw logits and accept uniform in lane j % 32, slot j / 32 —
-  // computed while the row loads are in flight
-  const float u_fb = c.err ? 0.f : spec_uniform(a.seed, c.u, c.b, 1);
-  float cP[4], cQ[4], cU[4];
+  const NodeCtx c = load_tree_b(a, t, ts, ca);
+  const int k = c.k;
+  const bool need_draft = !c.err && k > 0;   // leaves never read their draft row
+  if (need_draft && !early_draft) load_row(drow, base, end, vec, xq);   // not expected
+  // The scalar warp draws the node's uniforms (children's accept tests, the
+  // fallback draw) and reads the children's raw logits while the rows are in
+  // flight; lane j handles child j (and lane k the fallback draw's uniform).
+  const bool scalar_warp = w_id == kScalarWarp;
+  float rawP[4], rawQ[4];
+  if (scalar_warp && !c.err) {
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int j = lane + 32 * s;
-    cP[s] = cQ[s] = cU[s] = 0.f;
-    if (!c.err && j < k) {
-      const int ch = ts.child[j];
-      const int x = ts.tok[ch];
-      cP[s] = __ldg(trow + x);
-      cQ[s] = __ldg(drow + x);
-      cU[s] = spec_uniform(a.seed, ch, c.b, 0);
+    for (int s = 0; s < 4; ++s) {
+      const int j = lane + 32 * s;
+      rawP[s] = rawQ[s] = 0.f;
+      if (j < k) {
+        const int ch = ts.child[j];
+        const int x = ts.tok[ch];
+        rawP[s] = __ldg(trow + x);
+        rawQ[s] = __ldg(drow + x);
+        ns.U[j] = spec_uniform(a.seed, ch, c.b, 0);
+      } else if (j == k) {
+        ns.u_fb = spec_uniform(a.seed, c.u, c.b, 1);
+      }
     }
   }
   if (tid == 0 && !c.err) mbar_arrive_expect_tx(&xbar[0], static_cast<uint32_t>(CS * kRWarps * 16));
@@ -166,18 +182,23 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     const float nl = ml == -INFINITY ? 0.f : -ml * l2s;
     const float nd = md == -INFINITY ? 0.f : -md * l2s;
     float sl = 0.f, sd = 0.f;
+    // half of the exponentials on the MUFU pipe, half on the FMA pipe
+    auto expo = [&](float v, float nb, int m) -> float {
+      const float z = fmaf(v, l2s, nb);
+      return m < kRVec / 2 ? fast_exp2(z) : exp2_taylor(z);
+    };
 #pragma unroll
     for (int m = 0; m < kRVec; ++m) {
-      xp[m].x = fast_exp2(fmaf(xp[m].x, l2s, nl));
-      xp[m].y = fast_exp2(fmaf(xp[m].y, l2s, nl));
-      xp[m].z = fast_exp2(fmaf(xp[m].z, l2s, nl));
-      xp[m].w = fast_exp2(fmaf(xp[m].w, l2s, nl));
+      xp[m].x = expo(xp[m].x, nl, m);
+      xp[m].y = expo(xp[m].y, nl, m);
+      xp[m].z = expo(xp[m].z, nl, m);
+      xp[m].w = expo(xp[m].w, nl, m);
       sl += (xp[m].x + xp[m].y) + (xp[m].z + xp[m].w);
       if (need_draft) {
-        xq[m].x = fast_exp2(fmaf(xq[m].x, l2s, nd));
-        xq[m].y = fast_exp2(fmaf(xq[m].y, l2s, nd));
-        xq[m].z = fast_exp2(fmaf(xq[m].z, l2s, nd));
-        xq[m].w = fast_exp2(fmaf(xq[m].w, l2s, nd));
+        xq[m].x = expo(xq[m].x, nd, m);
+        xq[m].y = expo(xq[m].y, nd, m);
+        xq[m].z = expo(xq[m].z, nd, m);
+        xq[m].w = expo(xq[m].w, nd, m);
         sd += (xq[m].x + xq[m].y) + (xq[m].z + xq[m].w);
       }
     }
@@ -222,14 +243,21 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       xp[m].x *= sc_l; xp[m].y *= sc_l; xp[m].z *= sc_l; xp[m].w *= sc_l;
       xq[m].x *= sc_d; xq[m].y *= sc_d; xq[m].z *= sc_d; xq[m].w *= sc_d;
     }
-    // the children's p and q from their raw logits
+    // the children's p and q from their raw logits (scalar warp), published
+    // with the uniforms through an mbarrier (release / acquire)
+    if (scalar_warp) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      if (lane + 32 * s < k) {
-        cP[s] = precise_prob(cP[s], Ml, a.temp, a.inv_temp, 1.f) * inv_sp;
-        cQ[s] = precise_prob(cQ[s], Md, a.temp, a.inv_temp, 1.f) * inv_sq;
+      for (int s = 0; s < 4; ++s) {
+        const int j = lane + 32 * s;
+        if (j < k) {
+          ns.P[j] = precise_prob(rawP[s], Ml, a.temp, a.inv_temp, 1.f) * inv_sp;
+          ns.Q[j] = precise_prob(rawQ[s], Md, a.temp, a.inv_temp, 1.f) * inv_sq;
+        }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&nbar);
     }
+    if (ok && !mbar_wait(&nbar, 0)) ok = false;
 
     // ---- V2: the children's accept tests in index order, stopping at the
     //      first accepted child (the walk never looks past it).  The test
@@ -238,10 +266,9 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     bool frozen = false;   // a residual that summed to zero stays as it is
     int rounds = 0;
     for (int j = 0; j < k; ++j) {
-      const int sl_ = j >> 5, src = j & 31;
-      const float P = __shfl_sync(0xffffffffu, pick_slot(cP, sl_), src);
-      const float Q = __shfl_sync(0xffffffffu, pick_slot(cQ, sl_), src);
-      const float U = __shfl_sync(0xffffffffu, pick_slot(cU, sl_), src);
+      const float P = ns.P[j];
+      const float Q = ns.Q[j];
+      const float U = ns.U[j];
       bool accept, tie;
       const float num = fmaxf(0.f, fmaf(-c_prev, Q, P));
       const float den = W_prev * Q;
@@ -311,7 +338,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         slice[r] = r < CS ? warp_sum(lane < kRWarps ? mass(r, lane) : 0.f) : 0.f;
         total += slice[r];
       }
-      const float target = u_fb * total;
+      const float target = ns.u_fb * total;
       int owner = -1;
       float prefix = 0.f, run = 0.f;
 #pragma unroll
