@@ -15,8 +15,9 @@
 //                 O  += P_i V_i            M=128, N=D,  K=64  (TMEM O)
 //               with S_{i+1} issued before P_i is ready, so the softmax of
 //               one tile overlaps the QK^T of the next.
-//   warps 2-9   two threads per TMEM lane (= query row), one per half of
-//               the tile's keys: read S from TMEM, mask with the node's
+//   warps 2+    four threads per TMEM lane (= query row), one per quarter of
+//               the tile's keys (16 softmax warps for 128-row blocks, 8 for
+//               packed blocks): read S from TMEM, mask with the node's
 //               ancestor bits, share the row max, online softmax with a
 //               lazily moved reference max (the stored O is rescaled only
 //               when a row's max grows by more than 2^8), write P as bf16
@@ -43,8 +44,6 @@
 namespace spec {
 
 constexpr int kTcRows = 128;
-constexpr int kTcSoftmaxWarps = 8;   // two warps (key halves) per TMEM lane quadrant
-constexpr int kTcThreads = 32 * (2 + kTcSoftmaxWarps);
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D, bool PACKED>
@@ -64,8 +63,13 @@ struct TcCfg {
   static constexpr int kOffKV = kQBytes;
   static constexpr int kOffP = kOffKV + kStages * kStageBytes;
   static constexpr int kSmem = kOffP + 2 * kPParts * kPBytes + 1024;
-  static constexpr int kParts = PACKED ? 4 : 2;             // threads per row (key parts)
+  // softmax warps: four threads (key quarters) per S row; packed blocks hold
+  // 64 rows twice, so 8 warps cover them, 128-row blocks take 16
+  static constexpr int kSoftmaxWarps = PACKED ? 8 : 16;
+  static constexpr int kThreads = 32 * (2 + kSoftmaxWarps);
+  static constexpr int kParts = 4;                          // threads per row (key parts)
   static constexpr int kKeysPer = kKeyTile / kParts;        // keys per thread per tile
+  static constexpr int kOCols = PACKED ? D / 2 : D / 4;     // O columns one thread reads out
   static constexpr int kStage = D + 4;                      // floats per staged output row
   static constexpr int kSBufs = 3;                          // S tiles in flight in TMEM
   static constexpr uint32_t kTmemCols = 512;
@@ -95,12 +99,65 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
       : "memory");
 }
 
+// N consecutive TMEM columns of this thread's lane into registers (N a
+// multiple of 16), and the same columns scaled in place.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&out)[N]) {
+  static_assert(N % 16 == 0, "16-column granularity");
+  if constexpr (N % 32 == 0) {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) {
+      float o[32];
+      tc::ld32(taddr + c * 32, o);
+      tc::wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) out[c * 32 + e] = o[e];
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+      float o[16];
+      tc::ld16(taddr + c * 16, o);
+      tc::wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) out[c * 16 + e] = o[e];
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float alpha) {
+  static_assert(N % 16 == 0, "16-column granularity");
+  if constexpr (N % 32 == 0) {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) {
+      float o[32];
+      tc::ld32(taddr + c * 32, o);
+      tc::wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] *= alpha;
+      tc::st32(taddr + c * 32, o);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+      float o[16];
+      tc::ld16(taddr + c * 16, o);
+      tc::wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) o[e] *= alpha;
+      tc::st16(taddr + c * 16, o);
+    }
+  }
+  tc::wait_st();
+}
+
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
 template <int D, bool PACKED>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcCfg<D, PACKED>::kThreads, 1)
 tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv) {
@@ -137,7 +194,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     mbar_init(&bar_m, 1);
     for (int j = 0; j < 3; ++j) mbar_init(&bar_s[j], 1);
     for (int j = 0; j < 2; ++j) {
-      mbar_init(&bar_p[j], kTcSoftmaxWarps);
+      mbar_init(&bar_p[j], C::kSoftmaxWarps);
       mbar_init(&bar_o[j], 1);
     }
     fence_barrier_init();
@@ -179,21 +236,25 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const int t0 = split * per;
   const int ntiles = max(0, min(t0 + per, tiles_total) - t0);
 
-  // softmax-thread geometry (warps 2..9).  TMEM lane r = 32 * quad + lane.
-  // Not packed: row r, two threads (key halves) per row.  Packed: the Q block
-  // is loaded twice, so lanes r and r + 64 hold the same S row; four threads
-  // (key quarters) per row, and lanes 64-127 accumulate the remainder part of
-  // P V.  Each thread owns one half of its lane's O columns.
+  // softmax-thread geometry (warps 2 and up).  TMEM lane r = 32 * quad +
+  // lane.  128-row blocks: row r, four threads (key quarters) per row, each
+  // reading out a quarter of the row's O.  Packed blocks: the Q block is
+  // loaded twice, so lanes r and r + 64 hold the same S row; four threads
+  // (key quarters) per row, lanes 64-127 accumulate the remainder part of
+  // P V, and each thread reads out half of its lane's O.
   const int quad = warp & 3;
-  const int half = (warp - 2) >> 2;
+  const int half = (warp - 2) >> 2;                  // packed: 0..1; otherwise 0..3
   const int part = PACKED ? ((quad >> 1) * 2 + half) : half;
   const int srow = PACKED ? ((quad & 1) * 32 + lane) : (quad * 32 + lane);
   const bool row_ok = srow < rows_here;
   const bool lanes_live = warp >= 2 && (PACKED ? (quad & 1) : quad) * 32 < rows_here;
   const bool lo_lane = PACKED && quad >= 2;          // holds the remainder part of P V
-  const bool owner = warp >= 2 && !lo_lane;          // assembles the row's final O half
+  const bool owner = warp >= 2 && !lo_lane;          // assembles the row's final O
+  const int ocol = PACKED ? half * (D / 2) : part * (D / 4);   // this thread's O columns
+  const bool tail_writer = PACKED ? half == 0 : part == 0;
+  constexpr int kOC = C::kOCols;
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-  float o_keep[D / 2];
+  float o_keep[kOC];
   float m_used = -INFINITY, l_part = 0.f, l_row = 0.f;
 
   if (warp == 0) {
@@ -232,12 +293,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
       bool ok = mbar_wait(&bar_q, 0);
       tc::fence_after_sync();
-      // S_i into TMEM buffer i % 3; buffer reuse for tile i + 3 needs P_i
-      // (the softmax has read S_i).  Order: S_0..S_2, then per tile j:
-      // P_j ready -> P_j V_j, S_{j+3}.
-      auto issue_s = [&](int i) -> bool {
+      // S_i goes into TMEM buffer i % 3 once tile i's K/V has landed and
+      // the softmax has read S_{i-3} (its P_{i-3} arrived: PV_{i-3} issued);
+      // P_j V_j goes once P_j has arrived.  Neither waits for the other: the
+      // issuer polls both conditions and issues whichever is ready, so a
+      // late K/V tile never holds back a ready P V.
+      auto issue_s = [&](int i) {
         const int st = i % NS;
-        if (!mbar_wait(&bar_full[st], (i / NS) & 1)) return false;
         tc::fence_after_sync();
         const uint32_t kb = sb + C::kOffKV + st * C::kStageBytes;
 #pragma unroll
@@ -249,12 +311,9 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
           tc::mma_bf16(tmem + C::kColS + (i % C::kSBufs) * kKeyTile, ad, bd, idS, ks > 0);
         }
         tc::commit(&bar_s[i % C::kSBufs]);
-        return true;
       };
-      for (int i = 0; ok && i < C::kSBufs && i < ntiles; ++i) ok = issue_s(i);
-      for (int j = 0; ok && j < ntiles; ++j) {
+      auto issue_pv = [&](int j) {
         const int st = j % NS;
-        if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
         const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPParts * C::kPBytes;
@@ -269,7 +328,28 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         }
         tc::commit(&bar_o[j & 1]);
         tc::commit(&bar_empty[st]);
-        if (j + C::kSBufs < ntiles) ok = issue_s(j + C::kSBufs);
+      };
+      int next_s = 0, next_pv = 0;
+      uint64_t t_idle = 0;
+      uint32_t idle = 0;
+      while (ok && next_pv < ntiles) {
+        bool issued = false;
+        if (next_s < ntiles && next_s < next_pv + C::kSBufs &&
+            mbar_poll(&bar_full[next_s % NS], (next_s / NS) & 1)) {
+          issue_s(next_s++);
+          issued = true;
+        }
+        if (next_pv < next_s && mbar_poll(&bar_p[next_pv & 1], (next_pv >> 1) & 1)) {
+          issue_pv(next_pv++);
+          issued = true;
+        }
+        if (issued) {
+          idle = 0;
+        } else if (idle++ == 0) {
+          t_idle = global_ns();
+        } else if ((idle & 255u) == 0 && global_ns() - t_idle > kWaitLimitNs) {
+          ok = false;  // bounded: no progress for the wait limit
+        }
       }
       if (!ok) s_timeout = 1;
     }
@@ -293,7 +373,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const int valid = R.keys - key0;
         const int chunks = (kKeyTile - valid) * C::kBoxes * 8;
         uint8_t *vrow = smem + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
-        for (int c = tid - 64; c < chunks; c += 32 * kTcSoftmaxWarps) {
+        for (int c = tid - 64; c < chunks; c += 32 * C::kSoftmaxWarps) {
           const int row = valid + c / (C::kBoxes * 8);
           const int rest = c % (C::kBoxes * 8);
           *reinterpret_cast<uint4 *>(vrow + (rest >> 3) * C::kKVBoxBytes + row * 128 +
@@ -324,7 +404,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       }
       // one barrier: every part's maximum is visible, and whether any row of
       // the block moves its reference max
-      const bool any_resc = named_bar_or(2, 32 * kTcSoftmaxWarps, want);
+      const bool any_resc = named_bar_or(2, 32 * C::kSoftmaxWarps, want);
       if (any_resc) {
         float mt = -INFINITY;
         if (lanes_live && row_ok) {
@@ -337,41 +417,37 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const float alpha = !resc ? 1.f : (m_used == -INFINITY ? 0.f : exp2f(m_used - m_new));
         if (i > 0 && lanes_live) {
           // O holds the products of tiles < i: wait for the last of them,
-          // then rescale this thread's half of its TMEM lane in place.
+          // then rescale this thread's columns of its TMEM lane in place.
           if (ok && !mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1)) ok = false;
           __syncwarp();
           tc::fence_after_sync();
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            float o[32];
-            tc::ld32(trow + C::kColO + half * (D / 2) + c * 32, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tc::st32(trow + C::kColO + half * (D / 2) + c * 32, o);
-          }
-          tc::wait_st();
+          tmem_scale_cols<kOC>(trow + C::kColO + ocol, alpha);
         }
         l_part *= alpha;
         m_used = m_new;
       }
       if (lanes_live) {
+        const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
+        // the tile's weights first, in place, so they are ready while the P
+        // buffer may still be busy
+        float psum = 0.f;
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+          s[j] = fast_exp2(fmaf(s[j], sl2, nbase));
+          psum += s[j];
+        }
         // the P buffer of this parity is free once the P V of tile i-2 is done
         if (ok && i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
         __syncwarp();
-        const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
         uint8_t *pbuf = smem + C::kOffP + (i & 1) * C::kPParts * C::kPBytes;
         uint8_t *prow_hi = pbuf + srow * 128;
         uint8_t *prow_lo = PACKED ? pbuf + (srow + kTcRows / 2) * 128 : pbuf + C::kPBytes + srow * 128;
-        float psum = 0.f;
 #pragma unroll
         for (int cc = 0; cc < KP / 8; ++cc) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(fmaf(s[cc * 8 + 2 * e], sl2, nbase));
-            const float p1 = fast_exp2(fmaf(s[cc * 8 + 2 * e + 1], sl2, nbase));
-            psum += p0 + p1;
+            const float p0 = s[cc * 8 + 2 * e], p1 = s[cc * 8 + 2 * e + 1];
             const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
             const float2 hf = __bfloat1622float2(h);
             hi[e] = bf16x2_bits(h);
@@ -397,37 +473,28 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       tc::fence_after_sync();
     }
 #pragma unroll
-    for (int e = 0; e < D / 2; ++e) o_keep[e] = 0.f;
-    if (lanes_live && ntiles > 0) {
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        float o[32];
-        tc::ld32(trow + C::kColO + half * (D / 2) + c * 32, o);
-        tc::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o_keep[c * 32 + e] = o[e];
-      }
-    }
+    for (int e = 0; e < kOC; ++e) o_keep[e] = 0.f;
+    if (lanes_live && ntiles > 0) tmem_load_cols<kOC>(trow + C::kColO + ocol, o_keep);
     // [64 rows][D] floats in the free P buffers; 16-byte chunks swizzled by
     // row so that eight consecutive rows hit eight different bank groups
     float *xo = reinterpret_cast<float *>(smem + C::kOffP);
     auto xo_at = [&](int e) -> float4 * {
-      const int chunk = (half * (D / 2) + e) >> 2;
+      const int chunk = (ocol + e) >> 2;
       return reinterpret_cast<float4 *>(xo + srow * D) + (chunk ^ (srow & 7));
     };
     if (PACKED && lo_lane && row_ok) {
 #pragma unroll
-      for (int e = 0; e < D / 2; e += 4)
+      for (int e = 0; e < kOC; e += 4)
         *xo_at(e) = make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
     }
     if (warp >= 2) x_l[part][srow] = l_part;
-    named_bar_sync(2, 32 * kTcSoftmaxWarps);
+    named_bar_sync(2, 32 * C::kSoftmaxWarps);
     if (owner && row_ok) {
 #pragma unroll
       for (int q = 0; q < C::kParts; ++q) l_row += x_l[q][srow];
       if (PACKED) {
 #pragma unroll
-        for (int e = 0; e < D / 2; e += 4) {
+        for (int e = 0; e < kOC; e += 4) {
           const float4 v = *xo_at(e);
           o_keep[e] += v.x;
           o_keep[e + 1] += v.y;
@@ -439,10 +506,10 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       // merge (the K/V ring is free)
       float *stg = reinterpret_cast<float *>(smem + C::kOffKV) + srow * C::kStage;
 #pragma unroll
-      for (int e = 0; e < D / 2; e += 4)
-        *reinterpret_cast<float4 *>(stg + half * (D / 2) + e) =
+      for (int e = 0; e < kOC; e += 4)
+        *reinterpret_cast<float4 *>(stg + ocol + e) =
             make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
-      if (half == 0) *reinterpret_cast<float2 *>(stg + D) = make_float2(ntiles > 0 ? m_used : -INFINITY, l_row);
+      if (tail_writer) *reinterpret_cast<float2 *>(stg + D) = make_float2(ntiles > 0 ? m_used : -INFINITY, l_row);
       fence_proxy_async_smem();  // the rows may leave by bulk copy
     }
   }
@@ -460,7 +527,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   if (CS == 1) {
     // ---- final rows, 8 bf16 per thread, consecutive threads on one row
     const int nv = rows_here * (D / 8);
-    for (int idx = tid; idx < nv; idx += kTcThreads) {
+    for (int idx = tid; idx < nv; idx += C::kThreads) {
       const int lr = idx / (D / 8), c8 = idx % (D / 8);
       const float inv = 1.f / stg[lr * C::kStage + D + 1];
       const float4 v0 = *reinterpret_cast<const float4 *>(stg + lr * C::kStage + c8 * 8);
@@ -506,7 +573,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   {
     constexpr int kE = D / 8;   // columns per task
     const int ntask = own_n * 8;
-    for (int task = tid; task < ntask; task += kTcThreads) {
+    for (int task = tid; task < ntask; task += C::kThreads) {
       const int j = task >> 3;
       const int lr = own0 + j;
       const int col0 = (task & 7) * kE;
@@ -552,8 +619,10 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   cluster_wait();  // no CTA leaves while a copy may still read its rows
 }
 
-// Split plan: the split count (cluster size) that minimises (waves x tiles
-// per CTA) at one CTA per SM.
+// Split plan: the split count (cluster size) that minimises the time of the
+// launch at one CTA per SM, in units of one key tile: waves x (tiles per CTA
+// + a CTA's fixed ramp-up and epilogue, about 4 tiles, + the split merge,
+// about 3 tiles).
 void plan_attn_tc(int B, int T, int Hkv, int G, int max_prefix, int num_sms, int *cs_out,
                   int *rowblocks_out) {
   const int max_nodes = T < SPEC_MAX_TREE_NODES ? T : SPEC_MAX_TREE_NODES;
@@ -566,7 +635,7 @@ void plan_attn_tc(int B, int T, int Hkv, int G, int max_prefix, int num_sms, int
   for (int c = 1; c <= kTcMaxSplits; c *= 2) {
     if (c > 1 && tiles_max < 2 * c) break;
     const long long waves = (units * c + num_sms - 1) / num_sms;
-    const long long cost = waves * ((tiles_max + c - 1) / c) + (c > 1 ? 2 : 0);
+    const long long cost = waves * ((tiles_max + c - 1) / c + 4 + (c > 1 ? 3 : 0));
     if (best < 0 || cost < best) {
       best = cost;
       cs = c;
@@ -590,7 +659,7 @@ static int launch_tc(const AttnArgs &args, const CUtensorMap &tmq, const CUtenso
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, rowblocks, static_cast<unsigned>(args.B * args.Hkv));
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

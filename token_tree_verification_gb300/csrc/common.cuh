@@ -75,6 +75,19 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of phase `parity` (returns at once).
+__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete; false if the time limit ran
 // out.  try_wait itself suspends the thread in hardware for a while, so the
 // loop polls without sleeping and reads the clock only every 256 polls.
@@ -252,7 +265,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 2^x for x <= 0 on the FMA pipe, so that exponential-heavy loops can split
+// 2^x for x <= 127 on the FMA pipe, so that exponential-heavy loops can split
 // their work between it and the MUFU pipe (fast_exp2).  Range reduction to
 // the nearest integer, x = n + f with |f| <= 1/2, then the degree-7 Taylor
 // polynomial of e^(f ln 2) (coefficients (ln 2)^k / k!; truncation error below
