@@ -55,6 +55,8 @@ def _load():
     lib.oracle_tree_verify.argtypes = [P, P, P, P, P, i32, i32, i32, ctypes.c_float,
                                        u64, P, P, P, P, i32, P]
     lib.oracle_tree_verify.restype = i32
+    lib.oracle_kv_compact.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, i32, P, P]
+    lib.oracle_kv_compact.restype = i32
     _lib = lib
     return lib
 
@@ -154,3 +156,22 @@ def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperatu
     if rc != 0:
         raise ValueError(f"oracle_tree_verify: status {rc}")
     return res
+
+
+def kv_compact(cache, prefix_lens, offsets, path_nodes, accept_len, status=None):
+    """Depth-first KV-cache update (oracle_kv_compact) on a copy of ``cache``
+    ([B][H][S_cap][D], any fixed-size dtype).  Returns (new_cache,
+    new_prefix_lens, status)."""
+    lib = _load()
+    c = np.array(cache, copy=True, order="C")
+    B, H, S_cap, D = c.shape
+    pn = _c(path_nodes, np.int32)
+    W = pn.shape[1]
+    st = np.zeros(B, np.int32) if status is None else _c(status, np.int32).copy()
+    newp = np.zeros(B, np.int32)
+    rc = lib.oracle_kv_compact(_ptr(c), c.dtype.itemsize, B, H, S_cap, D,
+                               _ptr(_c(prefix_lens, np.int32)), _ptr(_c(offsets, np.int32)),
+                               _ptr(pn), _ptr(_c(accept_len, np.int32)), W, _ptr(newp), _ptr(st))
+    if rc != 0:
+        raise ValueError(f"oracle_kv_compact: {rc}")
+    return c, newp, st

@@ -394,3 +394,47 @@ int oracle_tree_verify(const float *target_logits, const float *draft_logits,
   free(p); free(qd); free(r);
   return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Depth-first KV-cache update [news]: after verification request b commits  */
+/* its root (slot L_b) and the accepted path's nodes, so their keys/values   */
+/* must sit contiguously after the prefix for the next step.  Slot L_b + j   */
+/* receives the old slot L_b + path[j] for j = 1 .. acc_b (path[0] is the    */
+/* root); every other slot is unchanged, and the committed prefix becomes    */
+/* L_b + 1 + acc_b.  The copy reads the old cache: a destination slot may    */
+/* also be the source of a later path entry (path 0 -> 2 -> 3).              */
+/* cache: [B][H][S_cap][D] elements of elem_bytes bytes.  Requests whose     */
+/* status is already non-zero are skipped (new prefix = L_b).                */
+/* ------------------------------------------------------------------------ */
+int oracle_kv_compact(uint8_t *cache, int elem_bytes, int B, int H, int S_cap, int D,
+                      const int32_t *prefix_lens, const int32_t *offsets,
+                      const int32_t *path_nodes, const int32_t *accept_len, int W,
+                      int32_t *new_prefix, int32_t *status) {
+  if (B < 1 || H < 1 || S_cap < 1 || D < 1 || W < 1 || elem_bytes < 1) return OR_ERR_SHAPE;
+  const size_t row = (size_t)D * (size_t)elem_bytes;
+  uint8_t *old = (uint8_t *)malloc(row * (size_t)S_cap);
+  if (!old) return OR_ERR_SHAPE;
+  for (int b = 0; b < B; ++b) {
+    const int L = prefix_lens[b];
+    new_prefix[b] = L;
+    if (status[b] != 0) continue;
+    const int n = offsets[b + 1] - offsets[b];
+    const int acc = accept_len[b];
+    const int32_t *pn = path_nodes + (size_t)b * W;
+    if (L < 0 || L + n > S_cap) { status[b] = OR_ERR_PREFIX; continue; }
+    if (acc < 0 || acc + 1 > W) { status[b] = OR_ERR_TREE; continue; }
+    int bad = pn[0] != 0;
+    for (int j = 1; j <= acc; ++j)
+      if (pn[j] <= pn[j - 1] || pn[j] >= n) bad = 1;
+    if (bad) { status[b] = OR_ERR_PARENT; continue; }
+    for (int h = 0; h < H; ++h) {
+      uint8_t *base = cache + (((size_t)b * H + h) * (size_t)S_cap) * row;
+      memcpy(old, base, row * (size_t)S_cap);
+      for (int j = 1; j <= acc; ++j)
+        memcpy(base + (size_t)(L + j) * row, old + (size_t)(L + pn[j]) * row, row);
+    }
+    new_prefix[b] = L + 1 + acc;
+  }
+  free(old);
+  return OR_OK;
+}
