@@ -335,6 +335,7 @@ def run_native(args, rank, world, local_rank):
         "gpu_launches": 3 * K,
         "clocks": clocks, "clock_window": "timed region + 1 s soak of the same graph" if soak else "timed region",
     }
+    result["next_rows"] = {"kv_compact": time_kv_compact(st, stream, chunk)}
     if not args.no_e2e:
         result["e2e"] = run_e2e(st, w, stream, args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -352,6 +353,65 @@ def combine_over_ranks(elapsed_ms: float, units_per_step: int, steps: int, world
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     return elapsed_ms, world * units_per_step * steps / (elapsed_ms / 1e3)
+
+
+def deepest_paths(w):
+    """Per request, the root-to-leaf path of a deepest node (request-local
+    indices, -1 padded) and its length: the most a step can accept."""
+    W = w.max_depth + 1
+    pn = np.full((w.B, W), -1, np.int32)
+    acc = np.zeros(w.B, np.int32)
+    for b in range(w.B):
+        lo, hi = w.offsets[b], w.offsets[b + 1]
+        par = w.parents[lo:hi]
+        depth = np.zeros(hi - lo, np.int32)
+        for i in range(1, hi - lo):
+            depth[i] = depth[par[i]] + 1
+        x = int(np.argmax(depth))
+        path = [x]
+        while path[-1] != 0:
+            path.append(int(par[path[-1]]))
+        path = path[::-1]
+        pn[b, :len(path)] = path
+        acc[b] = len(path) - 1
+    return pn, acc
+
+
+def time_kv_compact(st, stream, n, reps=3):
+    """The depth-first KV-cache update after verification, timed alone: a graph
+    of n launches over the rotating caches, each moving the deepest accepted
+    path a step can produce (2 x acc x Hkv rows of D elements per request, each
+    read once and written once)."""
+    import torch
+    ttv, w = st.ttv, st.w
+    pn_h, acc_h = deepest_paths(w)
+    pn, acc = torch.as_tensor(pn_h).cuda(), torch.as_tensor(acc_h).cuda()
+    newp = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    kst = torch.zeros(w.B, dtype=torch.int32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            c = st.copies[i % len(st.copies)]
+            ttv.kv_compact(c["k"], c["v"], st.pl, st.off, pn, acc, kst, new_prefix_lens=newp)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        best = ms if best is None else min(best, ms)
+    if (kst.cpu().numpy() != 0).any():
+        raise RuntimeError(f"kv_compact status {kst.cpu().tolist()}")
+    moved = int(acc_h.sum()) * w.Hkv * w.D * w.k_cache.element_size() * 2 * 2
+    return {"us": best * 1e3, "accept_len": acc_h.tolist(), "bytes": moved,
+            "gbs": moved / (best * 1e-3) / 1e9,
+            "timing": f"CUDA graph of {n} launches, events on the launching stream"}
 
 
 def per_kernel_graph_times(st, stream, n, reps=3):

@@ -191,6 +191,38 @@ int spec_tree_verify(const float *target_logits, const float *draft_logits,
                      void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
+ * spec_kv_compact — the depth-first KV-cache update after verification.
+ *
+ * Source: SpecInfer news write-up, section "Token 樹驗證器": the verifier
+ * updates the KV cache depth-first, so the accepted path's keys and values
+ * become the next step's prefix without extra storage.
+ *
+ * For request b with prefix L_b, tree nodes at cache slots [L_b, L_b + N_b)
+ * and an accepted path (path_nodes / accept_len from spec_tree_verify): slot
+ * L_b + j receives the old slot L_b + path_nodes[b][j] for j = 1 .. acc_b in
+ * both caches, for every KV head; the root (slot L_b) and every other slot
+ * are unchanged; new_prefix_lens[b] = L_b + 1 + acc_b (prefix, root and the
+ * accepted tokens; the bonus token's keys and values come from the next
+ * step).  The copy reads the old slots, so a slot that is both a destination
+ * and a later source is handled.
+ *
+ *   k_cache, v_cache [B][Hkv][S_cap][D]   dtype, modified in place, 16-byte aligned
+ *   prefix_lens      [B] int32 (L_b, before the update)
+ *   tree_offsets     [B+1] int32
+ *   path_nodes       [B][max_depth_plus1] int32, accept_len [B] int32
+ *   new_prefix_lens  [B] int32 out (L_b for a skipped request)
+ *   status           [B] int32 in/out: requests whose status is already
+ *                    non-zero are skipped (caches untouched)
+ * Errors on the device: SPEC_ERR_PREFIX_RANGE (L_b + N_b > S_cap),
+ * SPEC_ERR_TREE_TOO_LARGE (acc_b + 1 > max_depth_plus1), SPEC_ERR_BAD_PARENT
+ * (the path does not start at 0 or is not increasing inside the tree).
+ */
+int spec_kv_compact(void *k_cache, void *v_cache, int dtype, int B, int Hkv, int D, int S_cap,
+                    const int32_t *prefix_lens, const int32_t *tree_offsets,
+                    const int32_t *path_nodes, const int32_t *accept_len, int max_depth_plus1,
+                    int32_t *new_prefix_lens, int32_t *status, void *stream);
+
+/*
  * spec_tree_verify_static — spec_tree_verify without a caller workspace.
  *
  * No counterpart in the paper: this is a library convenience.  It serves

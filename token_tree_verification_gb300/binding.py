@@ -56,6 +56,8 @@ def load():
     lib.spec_tree_verify_workspace_size.restype = SZ
     lib.spec_tree_verify.argtypes = [P, P, P, P, P, I, I, I, F, U64, P, P, P, P, I, P, SZ, P, P]
     lib.spec_tree_verify.restype = I
+    lib.spec_kv_compact.argtypes = [P, P, I, I, I, I, I, P, P, P, P, I, P, P, P]
+    lib.spec_kv_compact.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -186,3 +188,29 @@ def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperatu
                                 _ptr(outputs["near_ties"]), W, _ptr(workspace), workspace.numel(),
                                 _ptr(status), _stream(stream)), "spec_tree_verify")
     return outputs
+
+
+def kv_compact(k_cache, v_cache, prefix_lens, offsets, path_nodes, accept_len, status,
+               new_prefix_lens=None, stream=None):
+    """Depth-first KV-cache update after verification (in place).  Returns the
+    new prefix lengths (device int32 [B])."""
+    lib = load()
+    if k_cache.dtype != v_cache.dtype or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must match")
+    dt = {torch.bfloat16: SPEC_BF16, torch.float32: SPEC_F32}.get(k_cache.dtype)
+    if dt is None:
+        raise ValueError(f"unsupported cache dtype {k_cache.dtype}")
+    for t, name in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev(t, k_cache.dtype, name)
+    for t, name in ((prefix_lens, "prefix_lens"), (offsets, "offsets"), (path_nodes, "path_nodes"),
+                    (accept_len, "accept_len"), (status, "status")):
+        _dev(t, torch.int32, name)
+    B, H, S_cap, D = k_cache.shape
+    W = path_nodes.shape[-1]
+    if new_prefix_lens is None:
+        new_prefix_lens = torch.empty(B, dtype=torch.int32, device=k_cache.device)
+    _check(lib.spec_kv_compact(_ptr(k_cache), _ptr(v_cache), dt, B, H, D, S_cap, _ptr(prefix_lens),
+                               _ptr(offsets), _ptr(path_nodes), _ptr(accept_len), W,
+                               _ptr(new_prefix_lens), _ptr(status), _stream(stream)),
+           "spec_kv_compact")
+    return new_prefix_lens
