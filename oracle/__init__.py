@@ -57,6 +57,10 @@ def _load():
     lib.oracle_tree_verify.restype = i32
     lib.oracle_kv_compact.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, i32, P, P]
     lib.oracle_kv_compact.restype = i32
+    lib.oracle_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, ctypes.c_double, u64, P, P, P]
+    lib.oracle_tree_expand.restype = i32
+    lib.oracle_tree_prune.argtypes = [P, P, P, P, i32, i32, P, P, P, P, P]
+    lib.oracle_tree_prune.restype = i32
     _lib = lib
     return lib
 
@@ -175,3 +179,37 @@ def kv_compact(cache, prefix_lens, offsets, path_nodes, accept_len, status=None)
     if rc != 0:
         raise ValueError(f"oracle_kv_compact: {rc}")
     return c, newp, st
+
+
+def tree_expand(draft, parent_scores, node_ids, reqs, width: int, temperature: float, seed: int):
+    """One level of draft-tree expansion (oracle_tree_expand).  Returns
+    (tokens [F][width], scores [F][width], ties [F][width])."""
+    lib = _load()
+    d = _c(draft, np.float32)
+    F, V = d.shape
+    tok = np.zeros((F, width), np.int32)
+    sc = np.zeros((F, width), np.float64)
+    ties = np.zeros((F, width), np.int32)
+    rc = lib.oracle_tree_expand(_ptr(d), _ptr(_c(parent_scores, np.float64)), _ptr(_c(node_ids, np.int32)),
+                                _ptr(_c(reqs, np.int32)), F, V, width, float(temperature),
+                                int(seed) & (2**64 - 1), _ptr(tok), _ptr(sc), _ptr(ties))
+    if rc != 0:
+        raise ValueError(f"oracle_tree_expand: {rc}")
+    return tok, sc, ties
+
+
+def tree_prune(parents, tokens, scores, cand_offsets, keep: int):
+    """Pruning of candidate trees to `keep` nodes (oracle_tree_prune).  Returns
+    dict(parents, tokens, kept, n_out, status) with [B][keep] rows."""
+    lib = _load()
+    off = _c(cand_offsets, np.int32)
+    B = off.size - 1
+    out = {k: np.zeros((B, keep), np.int32) for k in ("parents", "tokens", "kept")}
+    out["n_out"] = np.zeros(B, np.int32)
+    out["status"] = np.zeros(B, np.int32)
+    rc = lib.oracle_tree_prune(_ptr(_c(parents, np.int32)), _ptr(_c(tokens, np.int32)),
+                               _ptr(_c(scores, np.float64)), _ptr(off), B, keep, _ptr(out["parents"]),
+                               _ptr(out["tokens"]), _ptr(out["kept"]), _ptr(out["n_out"]), _ptr(out["status"]))
+    if rc != 0:
+        raise ValueError(f"oracle_tree_prune: {rc}")
+    return out

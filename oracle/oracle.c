@@ -438,3 +438,113 @@ int oracle_kv_compact(uint8_t *cache, int elem_bytes, int B, int H, int S_cap, i
   free(old);
   return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Draft token-tree construction ([dev] §2.1: the speculator proposes, from  */
+/* each node's draft distribution, several candidate tokens that form the    */
+/* next level of the token tree, and each node keeps its parent pointer;     */
+/* the article's deployment configuration sets the tree width).              */
+/*                                                                           */
+/* Level expansion, per frontier row f (node u = node_ids[f] of request      */
+/* reqs[f], draft logits draft[f][V], cumulative score parent_scores[f]):    */
+/*   T > 0:  q = softmax(draft / T); child j (j < width) is the inverse-CDF  */
+/*           draw of q at the uniform of counter (u, request, 2, j);          */
+/*   T == 0: q = softmax(draft); the children are the `width` most likely    */
+/*           tokens in order (ties to the lower index).                      */
+/* score of child j = parent score + log q(token).  ties[f][j] = 1 when a    */
+/* draw lay within 1e-6 of an inverse-CDF boundary.                          */
+/* ------------------------------------------------------------------------ */
+static double oracle_uniform4(uint64_t seed, int64_t c0, int64_t c1, int64_t c2, int64_t c3) {
+  uint64_t ctr[4] = {(uint64_t)c0, (uint64_t)c1, (uint64_t)c2, (uint64_t)c3};
+  uint64_t key[2] = {seed, 0};
+  uint64_t out[4];
+  oracle_philox4x64_10(ctr, key, out);
+  return (double)(out[0] >> 40) * (1.0 / 16777216.0);
+}
+
+int oracle_tree_expand(const float *draft, const double *parent_scores, const int32_t *node_ids,
+                       const int32_t *reqs, int F, int V, int width, double temperature,
+                       uint64_t seed, int32_t *tokens, double *scores, int32_t *ties) {
+  if (F < 1 || V < 1 || width < 1 || width > V || !(temperature >= 0.0)) return OR_ERR_SHAPE;
+  const double t = temperature > 0.0 ? temperature : 1.0;
+  double *w = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!w) return OR_ERR_SHAPE;
+  for (int f = 0; f < F; ++f) {
+    const float *row = draft + (size_t)f * V;
+    double m = -INFINITY;
+    for (int x = 0; x < V; ++x) m = row[x] > m ? row[x] : m;
+    double s = 0.0;
+    for (int x = 0; x < V; ++x) {
+      w[x] = exp(((double)row[x] - m) / t);
+      s += w[x];
+    }
+    const double log_s = log(s);
+    for (int j = 0; j < width; ++j) {
+      int tok, tie = 0;
+      if (temperature > 0.0) {
+        tok = sample_inverse_cdf(w, V, oracle_uniform4(seed, node_ids[f], reqs[f], 2, j), &tie);
+      } else {
+        /* the j-th most likely token: the best one not yet taken */
+        tok = -1;
+        for (int x = 0; x < V; ++x) {
+          int taken = 0;
+          for (int i = 0; i < j; ++i) taken |= tokens[(size_t)f * width + i] == x;
+          if (!taken && (tok < 0 || row[x] > row[tok])) tok = x;
+        }
+      }
+      tokens[(size_t)f * width + j] = tok;
+      scores[(size_t)f * width + j] = parent_scores[f] + ((double)row[tok] - m) / t - log_s;
+      ties[(size_t)f * width + j] = tie;
+    }
+  }
+  free(w);
+  return OR_OK;
+}
+
+/* Pruning of a candidate tree (request b's candidates at [cand_off[b],    */
+/* cand_off[b+1]), request-local parents, breadth-first order so parent <   */
+/* index): keep the root and the keep - 1 other candidates of highest score */
+/* (ties to the lower index).  A child's score never exceeds its parent's   */
+/* (log q <= 0) and ties go to the lower index, so the kept set is closed   */
+/* under ancestors.  The kept nodes keep their relative order; outputs per  */
+/* request at stride `keep`: parents (renumbered), tokens, the kept          */
+/* candidates' indices, and n_out[b] = min(keep, n_b).                      */
+int oracle_tree_prune(const int32_t *parents, const int32_t *tokens, const double *scores,
+                      const int32_t *cand_off, int B, int keep, int32_t *out_parents,
+                      int32_t *out_tokens, int32_t *kept_index, int32_t *n_out, int32_t *status) {
+  if (B < 1 || keep < 1) return OR_ERR_SHAPE;
+  for (int b = 0; b < B; ++b) {
+    const int lo = cand_off[b], n = cand_off[b + 1] - lo;
+    n_out[b] = 0;
+    for (int i = 0; i < keep; ++i) {
+      out_parents[(size_t)b * keep + i] = -2;
+      out_tokens[(size_t)b * keep + i] = -1;
+      kept_index[(size_t)b * keep + i] = -1;
+    }
+    if (n < 1) { status[b] = OR_ERR_TREE; continue; }
+    if (check_parents(parents + lo, n) != OR_OK) { status[b] = OR_ERR_PARENT; continue; }
+    int *keepf = (int *)calloc((size_t)n, sizeof(int));
+    int *newid = (int *)malloc(sizeof(int) * (size_t)n);
+    if (!keepf || !newid) { free(keepf); free(newid); return OR_ERR_SHAPE; }
+    keepf[0] = 1;
+    for (int i = 1; i < n; ++i) {
+      int better = 0; /* non-root candidates ranked before i */
+      for (int j = 1; j < n; ++j)
+        if (scores[lo + j] > scores[lo + i] || (scores[lo + j] == scores[lo + i] && j < i)) ++better;
+      keepf[i] = better < keep - 1;
+    }
+    int c = 0;
+    for (int i = 0; i < n; ++i) newid[i] = keepf[i] ? c++ : -1;
+    for (int i = 0; i < n; ++i) {
+      if (!keepf[i]) continue;
+      const int k = newid[i];
+      out_parents[(size_t)b * keep + k] = i == 0 ? -1 : newid[parents[lo + i]];
+      out_tokens[(size_t)b * keep + k] = tokens[lo + i];
+      kept_index[(size_t)b * keep + k] = i;
+    }
+    n_out[b] = c;
+    free(keepf);
+    free(newid);
+  }
+  return OR_OK;
+}
