@@ -335,7 +335,8 @@ def run_native(args, rank, world, local_rank):
         "gpu_launches": 3 * K,
         "clocks": clocks, "clock_window": "timed region + 1 s soak of the same graph" if soak else "timed region",
     }
-    result["next_rows"] = {"kv_compact": time_kv_compact(st, stream, chunk)}
+    result["next_rows"] = {"kv_compact": time_kv_compact(st, stream, chunk),
+                           "tree_build": time_tree_build(w, stream, chunk)}
     if not args.no_e2e:
         result["e2e"] = run_e2e(st, w, stream, args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -412,6 +413,61 @@ def time_kv_compact(st, stream, n, reps=3):
     return {"us": best * 1e3, "accept_len": acc_h.tolist(), "bytes": moved,
             "gbs": moved / (best * 1e-3) / 1e9,
             "timing": f"CUDA graph of {n} launches, events on the launching stream"}
+
+
+def time_tree_build(w, stream, n, reps=3):
+    """Draft-tree construction for the workload's tree shape (width 5, depth 3,
+    pruned to 64 nodes), timed alone: the last expansion level (25 frontier
+    rows of the vocabulary, 5 i.i.d. draws each, reading 25 draft rows) and
+    the pruning of the 156 candidates."""
+    import torch
+    import token_tree_verification_gb300 as ttv
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(7)
+    Fr, width, cand = 25, 5, 156
+    rows = [torch.randn((Fr, w.V), generator=gen, device="cuda") * 3 for _ in range(8)]
+    ps = torch.zeros(Fr, device="cuda")
+    nodes = torch.arange(6, 6 + Fr, dtype=torch.int32, device="cuda")
+    reqs = torch.zeros(Fr, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(3)
+    par = np.array([-1] + [(i - 1) // width for i in range(1, cand)], np.int32)
+    sc = np.zeros(cand, np.float32)
+    for i in range(1, cand):
+        sc[i] = sc[par[i]] + np.float32(np.log(rng.uniform(1e-3, 1.0)))
+    par_d = torch.as_tensor(par).cuda()
+    tok_d = torch.as_tensor(rng.integers(0, w.V, cand).astype(np.int32)).cuda()
+    sc_d = torch.as_tensor(sc).cuda()
+    off_d = torch.tensor([0, cand], dtype=torch.int32, device="cuda")
+    pst = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = {}
+    for kind in ("expand", "prune"):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                if kind == "expand":
+                    ttv.tree_expand(rows[i % len(rows)], ps, nodes, reqs, width, 0.7, i)
+                else:
+                    ttv.tree_prune(par_d, tok_d, sc_d, off_d, 64, pst)
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            best = ms if best is None else min(best, ms)
+        out[kind + "_us"] = best * 1e3
+    if (pst.cpu().numpy() != 0).any():
+        raise RuntimeError("tree_prune status")
+    out["expand_bytes"] = Fr * w.V * 4
+    out["expand_gbs"] = out["expand_bytes"] / (out["expand_us"] * 1e-6) / 1e9
+    out["shape"] = "expand: 25 frontier rows x V, width 5, T=0.7; prune: 156 candidates -> 64"
+    return out
 
 
 def per_kernel_graph_times(st, stream, n, reps=3):

@@ -223,6 +223,53 @@ int spec_kv_compact(void *k_cache, void *v_cache, int dtype, int B, int Hkv, int
                     int32_t *new_prefix_lens, int32_t *status, void *stream);
 
 /*
+ * spec_tree_expand — one level of draft token-tree construction.
+ *
+ * Source: SpecInfer developer article §2.1 (the speculator proposes, from
+ * each node's draft distribution, the candidate tokens of the next level of
+ * the token tree; each node keeps its parent pointer) and its deployment
+ * configuration (tree width).
+ *
+ * For frontier row f (node node_ids[f] of request requests[f]; draft logits
+ * draft_logits[f][V]; cumulative score parent_scores[f]):
+ *   temperature > 0: q = softmax(draft / temperature); child j < width is the
+ *     inverse-CDF draw of q at the Philox4x64-10 uniform of counter
+ *     (node, request, 2, j), key (seed, 0) (the uniform convention of
+ *     spec_tree_verify);
+ *   temperature == 0: q = softmax(draft); the children are the width most
+ *     likely tokens in order, ties to the lower index.
+ * child_scores[f][j] = parent_scores[f] + log q(child_tokens[f][j]);
+ * near_ties[f][j] = 1 when a draw lay within 1e-6 of an inverse-CDF boundary.
+ *   width <= 16.  All arrays are device memory; no device-side errors.
+ */
+int spec_tree_expand(const float *draft_logits, const float *parent_scores,
+                     const int32_t *node_ids, const int32_t *requests, int F, int V, int width,
+                     float temperature, uint64_t seed, int32_t *child_tokens, float *child_scores,
+                     int32_t *near_ties, void *stream);
+
+/*
+ * spec_tree_prune — pruning of a candidate token tree to its best subtree.
+ *
+ * Source: SpecInfer developer article §2.1 (the token tree organises the
+ * speculated candidates; parent pointers).  For request b with candidates
+ * [cand_offsets[b], cand_offsets[b+1]) (request-local parents, parent < index,
+ * root first) keep the root and the keep - 1 other candidates of highest
+ * score, ties to the lower index.  Scores never increase along a path (each
+ * adds a log-probability <= 0), so the kept set is closed under ancestors.
+ * Outputs at stride `keep`, kept candidates in their original order:
+ *   out_parents [B][keep] renumbered parents (-2 past n_out[b])
+ *   out_tokens  [B][keep], kept_index [B][keep] (candidate index, -1 past n_out)
+ *   n_out       [B] = min(keep, candidate count)
+ *   keep <= SPEC_MAX_TREE_NODES; at most 1024 candidates per request.
+ * Errors on the device: SPEC_ERR_TREE_TOO_LARGE (no candidate, or more than
+ * 1024), SPEC_ERR_BAD_PARENT.
+ */
+int spec_tree_prune(const int32_t *parents, const int32_t *tokens, const float *scores,
+                    const int32_t *cand_offsets, int B, int keep, int32_t *out_parents,
+                    int32_t *out_tokens, int32_t *kept_index, int32_t *n_out, int32_t *status,
+                    void *stream);
+
+/*
  * spec_tree_verify_static — spec_tree_verify without a caller workspace.
  *
  * No counterpart in the paper: this is a library convenience.  It serves

@@ -58,6 +58,10 @@ def load():
     lib.spec_tree_verify.restype = I
     lib.spec_kv_compact.argtypes = [P, P, I, I, I, I, I, P, P, P, P, I, P, P, P]
     lib.spec_kv_compact.restype = I
+    lib.spec_tree_expand.argtypes = [P, P, P, P, I, I, I, F, U64, P, P, P, P]
+    lib.spec_tree_expand.restype = I
+    lib.spec_tree_prune.argtypes = [P, P, P, P, I, I, P, P, P, P, P, P]
+    lib.spec_tree_prune.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -214,3 +218,41 @@ def kv_compact(k_cache, v_cache, prefix_lens, offsets, path_nodes, accept_len, s
                                _ptr(new_prefix_lens), _ptr(status), _stream(stream)),
            "spec_kv_compact")
     return new_prefix_lens
+
+
+def tree_expand(draft_logits, parent_scores, node_ids, requests, width: int, temperature: float,
+                seed: int, stream=None):
+    """One level of draft-tree expansion.  Returns (child_tokens [F][width],
+    child_scores [F][width], near_ties [F][width]) as device tensors."""
+    lib = load()
+    _dev(draft_logits, torch.float32, "draft_logits")
+    _dev(parent_scores, torch.float32, "parent_scores")
+    _dev(node_ids, torch.int32, "node_ids")
+    _dev(requests, torch.int32, "requests")
+    F, V = draft_logits.shape
+    dev_ = draft_logits.device
+    tok = torch.empty((F, width), dtype=torch.int32, device=dev_)
+    sc = torch.empty((F, width), dtype=torch.float32, device=dev_)
+    ties = torch.empty((F, width), dtype=torch.int32, device=dev_)
+    _check(lib.spec_tree_expand(_ptr(draft_logits), _ptr(parent_scores), _ptr(node_ids), _ptr(requests),
+                                F, V, width, float(temperature), int(seed) & (2**64 - 1), _ptr(tok),
+                                _ptr(sc), _ptr(ties), _stream(stream)), "spec_tree_expand")
+    return tok, sc, ties
+
+
+def tree_prune(parents, tokens, scores, cand_offsets, keep: int, status, stream=None):
+    """Prune candidate trees to `keep` nodes.  Returns dict(parents, tokens,
+    kept, n_out) of device tensors ([B][keep] rows)."""
+    lib = load()
+    for t, name in ((parents, "parents"), (tokens, "tokens"), (cand_offsets, "cand_offsets"),
+                    (status, "status")):
+        _dev(t, torch.int32, name)
+    _dev(scores, torch.float32, "scores")
+    B = cand_offsets.numel() - 1
+    dev_ = parents.device
+    out = {k: torch.empty((B, keep), dtype=torch.int32, device=dev_) for k in ("parents", "tokens", "kept")}
+    out["n_out"] = torch.empty(B, dtype=torch.int32, device=dev_)
+    _check(lib.spec_tree_prune(_ptr(parents), _ptr(tokens), _ptr(scores), _ptr(cand_offsets), B, keep,
+                               _ptr(out["parents"]), _ptr(out["tokens"]), _ptr(out["kept"]),
+                               _ptr(out["n_out"]), _ptr(status), _stream(stream)), "spec_tree_prune")
+    return out
