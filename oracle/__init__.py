@@ -55,6 +55,9 @@ def _load():
     lib.oracle_tree_verify.argtypes = [P, P, P, P, P, i32, i32, i32, ctypes.c_float,
                                        u64, P, P, P, P, i32, P]
     lib.oracle_tree_verify.restype = i32
+    lib.oracle_tree_verify_top_p.argtypes = [P, P, P, P, P, i32, i32, i32, ctypes.c_float,
+                                             ctypes.c_double, u64, P, P, P, P, i32, P]
+    lib.oracle_tree_verify_top_p.restype = i32
     lib.oracle_kv_compact.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, i32, P, P]
     lib.oracle_kv_compact.restype = i32
     lib.oracle_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, ctypes.c_double, u64, P, P, P]
@@ -132,8 +135,9 @@ def tree_attn(q, k, v, prefix_lens, offsets, parents, scale: float = 0.0, rows=N
 
 
 def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperature: float,
-                seed: int, max_depth_plus1: int):
-    """Sequential root-to-leaf verification walk per request.
+                seed: int, max_depth_plus1: int, top_p: float = 1.0):
+    """Sequential root-to-leaf verification walk per request (with the target
+    and draft distributions filtered to their top_p nucleus when top_p < 1).
 
     Returns a dict of numpy arrays: accept_len [B], path_nodes [B, W],
     out_tokens [B, W], near_ties [B], status [B]."""
@@ -152,11 +156,18 @@ def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperatu
         near_ties=np.zeros(B, dtype=np.int32),
         status=np.zeros(B, dtype=np.int32),
     )
-    rc = _load().oracle_tree_verify(
-        _ptr(tl), _ptr(dl), _ptr(tok), _ptr(par), _ptr(off), B, T, V,
-        ctypes.c_float(temperature), seed & (2**64 - 1),
-        _ptr(res["accept_len"]), _ptr(res["path_nodes"]), _ptr(res["out_tokens"]),
-        _ptr(res["near_ties"]), W, _ptr(res["status"]))
+    if top_p >= 1.0:
+        rc = _load().oracle_tree_verify(
+            _ptr(tl), _ptr(dl), _ptr(tok), _ptr(par), _ptr(off), B, T, V,
+            ctypes.c_float(temperature), seed & (2**64 - 1),
+            _ptr(res["accept_len"]), _ptr(res["path_nodes"]), _ptr(res["out_tokens"]),
+            _ptr(res["near_ties"]), W, _ptr(res["status"]))
+    else:
+        rc = _load().oracle_tree_verify_top_p(
+            _ptr(tl), _ptr(dl), _ptr(tok), _ptr(par), _ptr(off), B, T, V,
+            ctypes.c_float(temperature), float(top_p), seed & (2**64 - 1),
+            _ptr(res["accept_len"]), _ptr(res["path_nodes"]), _ptr(res["out_tokens"]),
+            _ptr(res["near_ties"]), W, _ptr(res["status"]))
     if rc != 0:
         raise ValueError(f"oracle_tree_verify: status {rc}")
     return res

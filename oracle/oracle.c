@@ -303,12 +303,77 @@ static int sample_inverse_cdf(const double *w, int V, double u, int *tie) {
  * rejected token is replaced by a new target prediction; the residual keeps
  * the output distribution equal to the target's).  If every child is
  * rejected (or u is a leaf), draw the emitted token from r and stop. */
+/* Nucleus (top-p) filter, in place, of a distribution d[V] (developer
+ * article, deployment configuration: top_p).  tau is the largest value whose
+ * upper tail {d >= tau} holds at least top_p of the mass; every entry of that
+ * tail is kept (entries tied at tau included), the rest set to 0, and the
+ * tail renormalised.  *tie is set when either tail mass, {d >= tau} or
+ * {d > tau}, lies within 1e-5 of top_p (the boundary rounding could move). */
+static int cmp_desc(const void *a, const void *b) {
+  const double x = *(const double *)a, y = *(const double *)b;
+  return (x < y) - (x > y);
+}
+
+static void nucleus_filter(double *d, int V, double top_p, int *tie) {
+  double *sorted = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!sorted) return;
+  memcpy(sorted, d, sizeof(double) * (size_t)V);
+  qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
+  double cum = 0.0, tau = sorted[V - 1];
+  for (int i = 0; i < V; ++i) {
+    cum += sorted[i];
+    if (cum >= top_p) { tau = sorted[i]; break; }
+  }
+  free(sorted);
+  double mass = 0.0, mass_gt = 0.0;
+  for (int v = 0; v < V; ++v) {
+    if (d[v] >= tau) mass += d[v];
+    if (d[v] > tau) mass_gt += d[v];
+  }
+  if (fabs(mass - top_p) < 1e-5 || fabs(mass_gt - top_p) < 1e-5) *tie = 1;
+  for (int v = 0; v < V; ++v) d[v] = d[v] >= tau ? d[v] / mass : 0.0;
+}
+
+static int tree_verify_impl(const float *target_logits, const float *draft_logits,
+                            const int32_t *tokens, const int32_t *parents,
+                            const int32_t *offsets, int B, int T, int V, float temperature,
+                            double top_p, uint64_t seed, int32_t *accept_len,
+                            int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
+                            int max_depth_plus1, int32_t *status);
+
 int oracle_tree_verify(const float *target_logits, const float *draft_logits,
                        const int32_t *tokens, const int32_t *parents,
                        const int32_t *offsets, int B, int T, int V, float temperature,
                        uint64_t seed, int32_t *accept_len, int32_t *path_nodes,
                        int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
                        int32_t *status) {
+  return tree_verify_impl(target_logits, draft_logits, tokens, parents, offsets, B, T, V,
+                          temperature, 1.0, seed, accept_len, path_nodes, out_tokens, near_ties,
+                          max_depth_plus1, status);
+}
+
+/* The same walk with the target and draft distributions each filtered to
+ * their top_p nucleus first (top_p >= 1: no filter; greedy is unaffected).
+ * A node whose nucleus boundary is a near-tie counts one near-tie when the
+ * walk visits it. */
+int oracle_tree_verify_top_p(const float *target_logits, const float *draft_logits,
+                             const int32_t *tokens, const int32_t *parents,
+                             const int32_t *offsets, int B, int T, int V, float temperature,
+                             double top_p, uint64_t seed, int32_t *accept_len,
+                             int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
+                             int max_depth_plus1, int32_t *status) {
+  if (!(top_p > 0.0)) return OR_ERR_SHAPE;
+  return tree_verify_impl(target_logits, draft_logits, tokens, parents, offsets, B, T, V,
+                          temperature, top_p, seed, accept_len, path_nodes, out_tokens, near_ties,
+                          max_depth_plus1, status);
+}
+
+static int tree_verify_impl(const float *target_logits, const float *draft_logits,
+                            const int32_t *tokens, const int32_t *parents,
+                            const int32_t *offsets, int B, int T, int V, float temperature,
+                            double top_p, uint64_t seed, int32_t *accept_len,
+                            int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
+                            int max_depth_plus1, int32_t *status) {
   if (B < 1 || T < 1 || V < 1 || max_depth_plus1 < 1) return OR_ERR_SHAPE;
   const int greedy = !(temperature > 0.0f);
   if (!greedy && draft_logits == NULL) return OR_ERR_SHAPE;
@@ -360,6 +425,12 @@ int oracle_tree_verify(const float *target_logits, const float *draft_logits,
         const float *drow = draft_logits + (size_t)(offsets[b] + u) * V;
         softmax_t(lrow, V, temp, p);
         softmax_t(drow, V, temp, qd);
+        if (top_p < 1.0) {
+          int ntie = 0;
+          nucleus_filter(p, V, top_p, &ntie);
+          nucleus_filter(qd, V, top_p, &ntie);
+          ties += ntie;
+        }
         memcpy(r, p, sizeof(double) * (size_t)V);
         for (int c = u + 1; c < n && next < 0; ++c) {
           if (par[c] != u) continue;

@@ -102,7 +102,7 @@ def test_workspace_reuse_and_streams(gpu_lib):
     assert all((r == res[0]).all() for r in res)
 
 
-def _gpu_verify_np(tl, dl, tok, par, off, temp, seed, W):
+def _gpu_verify_np(tl, dl, tok, par, off, temp, seed, W, top_p=1.0):
     B = len(off) - 1
     T, V = tl.shape
     status = torch.zeros(B, dtype=torch.int32, device="cuda")

@@ -241,16 +241,35 @@ def lossless_tables(seed, V=8):
     return tab_t, tab_d
 
 
-def lossless_trial_batch(rng, tab_t, tab_d, ctx_pid, ctx_len, temp, V=8):
+def nucleus_np(prob, top_p):
+    """Top-p nucleus of each row of ``prob`` by sorting: the largest value tau
+    whose upper tail {prob >= tau} holds at least top_p of the mass; the tail
+    (ties at tau included) renormalised, the rest zero."""
+    prob = np.atleast_2d(np.asarray(prob, np.float64))
+    out = np.zeros_like(prob)
+    for i, row in enumerate(prob):
+        srt = np.sort(row)[::-1]
+        k = int(np.searchsorted(np.cumsum(srt), top_p))   # first index with cumsum >= top_p
+        tau = srt[min(k, srt.size - 1)]
+        keep = row >= tau
+        out[i] = np.where(keep, row, 0.0) / row[keep].sum()
+    return out
+
+
+def lossless_trial_batch(rng, tab_t, tab_d, ctx_pid, ctx_len, temp, V=8, top_p=1.0):
     """One speculated tree per trial: node logits are a function of the node's
-    token path; each child is an i.i.d. draft sample from its parent's q."""
+    token path; each child is an i.i.d. draft sample from its parent's q (its
+    top-p nucleus when top_p < 1)."""
     n_tr = ctx_pid.size
     nn = LOSSLESS_PARENTS.size
     pid = np.zeros((n_tr, nn), np.int64)
     tok = np.zeros((n_tr, nn), np.int32)
     pid[:, 0] = ctx_pid
-    qcum = np.cumsum(np.exp(tab_d.astype(np.float64) / temp
-                            - (tab_d.astype(np.float64) / temp).max(1, keepdims=True)), axis=1)
+    q = np.exp(tab_d.astype(np.float64) / temp - (tab_d.astype(np.float64) / temp).max(1, keepdims=True))
+    q /= q.sum(1, keepdims=True)
+    if top_p < 1.0:
+        q = nucleus_np(q, top_p)
+    qcum = np.cumsum(q, axis=1)
     qcum /= qcum[:, -1:]
     for c in range(1, nn):
         u = LOSSLESS_PARENTS[c]
@@ -262,7 +281,7 @@ def lossless_trial_batch(rng, tab_t, tab_d, ctx_pid, ctx_len, temp, V=8):
     return tok, tab_t[pid].reshape(-1, V), tab_d[pid].reshape(-1, V)
 
 
-def run_lossless(verify, trials, temp, seed, chunk=100000, V=8):
+def run_lossless(verify, trials, temp, seed, chunk=100000, V=8, top_p=1.0):
     """Returns counts of the first emitted token [V] and of the first two
     emitted tokens [V, V] (a second verification step, rooted after the first
     token, supplies the second token when the first step emits only one)."""
@@ -277,17 +296,18 @@ def run_lossless(verify, trials, temp, seed, chunk=100000, V=8):
         n_tr = min(chunk, trials - done)
         par = np.tile(LOSSLESS_PARENTS, n_tr)
         off = (np.arange(n_tr + 1) * nn).astype(np.int32)
-        tok, tl, dl = lossless_trial_batch(rng, tab_t, tab_d, np.zeros(n_tr, np.int64), 0, temp)
-        r = verify(tl, dl, tok.reshape(-1), par, off, temp, 1000 * seed + 2 * step, 4)
+        tok, tl, dl = lossless_trial_batch(rng, tab_t, tab_d, np.zeros(n_tr, np.int64), 0, temp, top_p=top_p)
+        r = verify(tl, dl, tok.reshape(-1), par, off, temp, 1000 * seed + 2 * step, 4, top_p=top_p)
         x1 = r["out_tokens"][:, 0]
         x2 = r["out_tokens"][:, 1].copy()
         need = r["accept_len"] == 0
         if need.any():
             m = int(need.sum())
-            tok2, tl2, dl2 = lossless_trial_batch(rng, tab_t, tab_d, 1 + x1[need].astype(np.int64), 1, temp)
+            tok2, tl2, dl2 = lossless_trial_batch(rng, tab_t, tab_d, 1 + x1[need].astype(np.int64), 1, temp,
+                                                  top_p=top_p)
             off2 = (np.arange(m + 1) * nn).astype(np.int32)
             r2 = verify(tl2, dl2, tok2.reshape(-1), np.tile(LOSSLESS_PARENTS, m), off2, temp,
-                        1000 * seed + 2 * step + 1, 4)
+                        1000 * seed + 2 * step + 1, 4, top_p=top_p)
             x2[need] = r2["out_tokens"][:, 0]
         np.add.at(c1, x1, 1)
         np.add.at(c2, (x1, x2), 1)
@@ -295,14 +315,23 @@ def run_lossless(verify, trials, temp, seed, chunk=100000, V=8):
         step += 1
     p1 = softmax64(tab_t[0], temp)
     p2 = np.stack([softmax64(tab_t[1 + x], temp) for x in range(V)])
+    if top_p < 1.0:
+        p1 = nucleus_np(p1, top_p)[0]
+        p2 = nucleus_np(p2, top_p)
     return c1, c2, p1, p1[:, None] * p2
 
 
 def chi2_ok(counts, probs):
+    """Pearson chi-square over the cells of positive probability (cells of
+    probability zero must be empty) and its 3-sigma bound."""
+    counts = counts.reshape(-1)
+    probs = probs.reshape(-1)
+    assert (counts[probs == 0] == 0).all(), "a draw landed outside the support"
+    m = probs > 0
     n = counts.sum()
-    e = n * probs.reshape(-1)
-    chi2 = float((((counts.reshape(-1) - e) ** 2) / e).sum())
-    dof = e.size - 1
+    e = n * probs[m]
+    chi2 = float((((counts[m] - e) ** 2) / e).sum())
+    dof = int(m.sum()) - 1
     return chi2, dof + 3 * math.sqrt(2 * dof)
 
 
@@ -316,6 +345,67 @@ def test_lossless_chi_square_oracle():
 
 def test_lossless_chi_square_oracle_temperature():
     c1, c2, p1, p12 = run_lossless(oracle.tree_verify, 200_000, 0.7, seed=1)
+    for c, p in ((c1, p1), (c2, p12)):
+        chi, bound = chi2_ok(c, p)
+        assert chi <= bound, (chi, bound)
+
+
+# ---------------------------------------------------------------------------
+# top-p (nucleus) filtering of p and q (developer article, deployment
+# configuration: top_p)
+# ---------------------------------------------------------------------------
+def _leaf_draws(probs, top_p, trials, seed=0):
+    """Bonus tokens of root-only trees whose target is ``probs`` (T = 1):
+    draws from the target's nucleus."""
+    logits = np.log(np.asarray(probs, np.float64)).astype(np.float32)
+    V = logits.size
+    tl = np.tile(logits, (trials, 1))
+    par = np.full(trials, -1, np.int32)
+    off = np.arange(trials + 1, dtype=np.int32)
+    r = oracle.tree_verify(tl, tl, np.zeros(trials, np.int32), par, off, 1.0, seed, 1, top_p=top_p)
+    assert (r["accept_len"] == 0).all()
+    return np.bincount(r["out_tokens"][:, 0], minlength=V), r["near_ties"]
+
+
+def test_top_p_hand_example_draws_from_the_nucleus():
+    # [0.5, 0.3, 0.2], top_p = 0.7: the tail {0.5, 0.3} holds 0.8 >= 0.7, {0.5}
+    # only 0.5 -> nucleus {0, 1}, renormalised to 5/8, 3/8
+    counts, ties = _leaf_draws([0.5, 0.3, 0.2], 0.7, 40000)
+    assert counts[2] == 0 and (ties == 0).all()
+    chi, bound = chi2_ok(counts, np.array([5 / 8, 3 / 8, 0.0]))
+    assert chi <= bound, (chi, bound)
+
+
+def test_top_p_keeps_ties_at_the_threshold():
+    # [0.4, 0.3, 0.3], top_p = 0.5: tau = 0.3 and both entries tied at 0.3 stay
+    counts, _ = _leaf_draws([0.4, 0.3, 0.3], 0.5, 40000)
+    chi, bound = chi2_ok(counts, np.array([0.4, 0.3, 0.3]))
+    assert chi <= bound, (chi, bound)
+
+
+def test_top_p_one_is_no_filter():
+    rng = np.random.default_rng(4)
+    trees = [synthetic.random_tree(rng, 10, 3, 3) for _ in range(50)]
+    par, off = pack(trees)
+    V = 30
+    tl = rng.normal(0, 2, (par.size, V)).astype(np.float32)
+    dl = (tl + rng.normal(0, 1, tl.shape)).astype(np.float32)
+    tok = rng.integers(0, V, par.size).astype(np.int32)
+    a = oracle.tree_verify(tl, dl, tok, par, off, 0.8, 9, 4)
+    b = oracle.tree_verify(tl, dl, tok, par, off, 0.8, 9, 4, top_p=1.0)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_top_p_boundary_near_tie_is_flagged():
+    # [0.5, 0.3, 0.2] with top_p = 0.8: the tail {0.5, 0.3} holds exactly 0.8
+    _, ties = _leaf_draws([0.5, 0.3, 0.2], 0.8, 50)
+    assert (ties > 0).all()
+
+
+def test_lossless_chi_square_oracle_top_p():
+    c1, c2, p1, p12 = run_lossless(oracle.tree_verify, 200_000, 1.0, seed=5, top_p=0.8)
+    assert (p1 == 0).any()            # the nucleus really removes tokens
     for c, p in ((c1, p1), (c2, p12)):
         chi, bound = chi2_ok(c, p)
         assert chi <= bound, (chi, bound)
