@@ -303,35 +303,99 @@ static int sample_inverse_cdf(const double *w, int V, double u, int *tie) {
  * rejected token is replaced by a new target prediction; the residual keeps
  * the output distribution equal to the target's).  If every child is
  * rejected (or u is a leaf), draw the emitted token from r and stop. */
-/* Nucleus (top-p) filter, in place, of a distribution d[V] (developer
- * article, deployment configuration: top_p).  tau is the largest value whose
- * upper tail {d >= tau} holds at least top_p of the mass; every entry of that
- * tail is kept (entries tied at tau included), the rest set to 0, and the
- * tail renormalised.  *tie is set when either tail mass, {d >= tau} or
- * {d > tau}, lies within 1e-5 of top_p (the boundary rounding could move). */
+/* Nucleus (top-p) of a distribution d[V] (developer article, deployment
+ * configuration: top_p).  tau is the largest value whose upper tail
+ * {d >= tau} holds at least top_p of the mass; every entry of that tail is
+ * kept (entries tied at tau included), the rest set to 0, and the tail
+ * renormalised.
+ *
+ * Which nucleus a finite-precision implementation finds can differ from the
+ * exact one where the running mass crosses top_p within its rounding: every
+ * cut {d >= t} whose tail holds at least top_p - eps while the tail above t
+ * holds less than top_p + eps is one it may find.  nucleus_cuts lists those
+ * thresholds t (the exact tau first); the walk counts a near-tie at a node
+ * only when two of them lead to different decisions there. */
 static int cmp_desc(const void *a, const void *b) {
   const double x = *(const double *)a, y = *(const double *)b;
   return (x < y) - (x > y);
 }
 
-static void nucleus_filter(double *d, int V, double top_p, int *tie) {
-  double *sorted = (double *)malloc(sizeof(double) * (size_t)V);
-  if (!sorted) return;
+#define NUCLEUS_EPS 5e-6
+#define NUCLEUS_MAX_CUTS 64
+
+/* Returns the number of plausible thresholds written to cuts[] (cuts[0] is
+ * the exact tau), or -1 when there are more than NUCLEUS_MAX_CUTS. */
+static int nucleus_cuts(const double *d, int V, double top_p, double *sorted, double *cuts) {
   memcpy(sorted, d, sizeof(double) * (size_t)V);
   qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
-  double cum = 0.0, tau = sorted[V - 1];
-  for (int i = 0; i < V; ++i) {
-    cum += sorted[i];
-    if (cum >= top_p) { tau = sorted[i]; break; }
+  /* distinct values in descending order with the tail mass above each */
+  double above = 0.0, tau = sorted[V - 1];
+  int n = 0, found = 0;
+  for (int i = 0; i < V;) {
+    const double t = sorted[i];
+    double group = 0.0;
+    int k = i;
+    while (k < V && sorted[k] == t) group += sorted[k++];
+    const double ge = above + group;  /* tail {d >= t} */
+    if (!found && ge >= top_p) { tau = t; found = 1; }
+    i = k;
+    above = ge;
   }
-  free(sorted);
-  double mass = 0.0, mass_gt = 0.0;
-  for (int v = 0; v < V; ++v) {
-    if (d[v] >= tau) mass += d[v];
-    if (d[v] > tau) mass_gt += d[v];
+  if (!found) tau = sorted[V - 1];
+  cuts[n++] = tau;
+  above = 0.0;
+  for (int i = 0; i < V;) {
+    const double t = sorted[i];
+    double group = 0.0;
+    int k = i;
+    while (k < V && sorted[k] == t) group += sorted[k++];
+    const double ge = above + group;
+    if (t != tau && ge >= top_p - NUCLEUS_EPS && above < top_p + NUCLEUS_EPS) {
+      if (n == NUCLEUS_MAX_CUTS) return -1;
+      cuts[n++] = t;
+    }
+    if (above >= top_p + NUCLEUS_EPS) break;
+    i = k;
+    above = ge;
   }
-  if (fabs(mass - top_p) < 1e-5 || fabs(mass_gt - top_p) < 1e-5) *tie = 1;
-  for (int v = 0; v < V; ++v) d[v] = d[v] >= tau ? d[v] / mass : 0.0;
+  return n;
+}
+
+/* out = d restricted to {d >= t}, renormalised */
+static void nucleus_apply(const double *d, int V, double t, double *out) {
+  double mass = 0.0;
+  for (int v = 0; v < V; ++v)
+    if (d[v] >= t) mass += d[v];
+  for (int v = 0; v < V; ++v) out[v] = d[v] >= t ? d[v] / mass : 0.0;
+}
+
+/* The stochastic decisions at node u of request b for target p and draft qd:
+ * u's children in ascending index order against the residual r (scratch,
+ * V entries), then, when every child is rejected, the inverse-CDF draw from
+ * r.  Returns the accepted child, or -1 with *token the drawn token;
+ * *ties counts decisions within 1e-6 of flipping. */
+static int node_decide(const double *p, const double *qd, double *r, int V,
+                       const int32_t *par, const int32_t *tok, int n, int u, int b,
+                       uint64_t seed, int *token, int *ties) {
+  memcpy(r, p, sizeof(double) * (size_t)V);
+  for (int c = u + 1; c < n; ++c) {
+    if (par[c] != u) continue;
+    int x = tok[c];
+    double alpha = qd[x] > 0.0 ? fmin(1.0, r[x] / qd[x]) : 1.0;
+    double uu = oracle_uniform(seed, c, b, 0);
+    if (fabs(uu - alpha) < 1e-6) ++*ties;
+    if (uu < alpha) return c;
+    /* rejected: residual r <- norm(max(0, r - q)); a zero residual
+     * (r == q up to rounding) leaves r unchanged */
+    double s = 0.0;
+    for (int y = 0; y < V; ++y) s += fmax(0.0, r[y] - qd[y]);
+    if (s > 0.0)
+      for (int y = 0; y < V; ++y) r[y] = fmax(0.0, r[y] - qd[y]) / s;
+  }
+  int tie = 0;
+  *token = sample_inverse_cdf(r, V, oracle_uniform(seed, u, b, 1), &tie);
+  *ties += tie;
+  return -1;
 }
 
 static int tree_verify_impl(const float *target_logits, const float *draft_logits,
@@ -379,10 +443,16 @@ static int tree_verify_impl(const float *target_logits, const float *draft_logit
   if (!greedy && draft_logits == NULL) return OR_ERR_SHAPE;
   const double temp = (double)temperature;
   const int W = max_depth_plus1;
-  double *p = (double *)malloc(sizeof(double) * (size_t)V);
-  double *qd = (double *)malloc(sizeof(double) * (size_t)V);
-  double *r = (double *)malloc(sizeof(double) * (size_t)V);
-  if (!p || !qd || !r) { free(p); free(qd); free(r); return OR_ERR_SHAPE; }
+  const size_t vb = sizeof(double) * (size_t)V;
+  double *p = (double *)malloc(vb), *qd = (double *)malloc(vb), *r = (double *)malloc(vb);
+  /* top-p: filtered rows, one alternative pair, sort scratch, thresholds */
+  double *fp = (double *)malloc(vb), *fq = (double *)malloc(vb);
+  double *vp = (double *)malloc(vb), *vq = (double *)malloc(vb), *sorted = (double *)malloc(vb);
+  double cuts_p[NUCLEUS_MAX_CUTS], cuts_q[NUCLEUS_MAX_CUTS];
+  if (!p || !qd || !r || !fp || !fq || !vp || !vq || !sorted) {
+    free(p); free(qd); free(r); free(fp); free(fq); free(vp); free(vq); free(sorted);
+    return OR_ERR_SHAPE;
+  }
 
   for (int b = 0; b < B; ++b) {
     int n = 0;
@@ -425,32 +495,37 @@ static int tree_verify_impl(const float *target_logits, const float *draft_logit
         const float *drow = draft_logits + (size_t)(offsets[b] + u) * V;
         softmax_t(lrow, V, temp, p);
         softmax_t(drow, V, temp, qd);
+        int token = -1;
         if (top_p < 1.0) {
-          int ntie = 0;
-          nucleus_filter(p, V, top_p, &ntie);
-          nucleus_filter(qd, V, top_p, &ntie);
-          ties += ntie;
-        }
-        memcpy(r, p, sizeof(double) * (size_t)V);
-        for (int c = u + 1; c < n && next < 0; ++c) {
-          if (par[c] != u) continue;
-          int x = tok[c];
-          double alpha = qd[x] > 0.0 ? fmin(1.0, r[x] / qd[x]) : 1.0;
-          double uu = oracle_uniform(seed, c, b, 0);
-          if (fabs(uu - alpha) < 1e-6) ++ties;
-          if (uu < alpha) { next = c; break; }
-          /* rejected: residual r <- norm(max(0, r - q)); a zero residual
-           * (r == q up to rounding) leaves r unchanged */
-          double s = 0.0;
-          for (int y = 0; y < V; ++y) s += fmax(0.0, r[y] - qd[y]);
-          if (s > 0.0)
-            for (int y = 0; y < V; ++y) r[y] = fmax(0.0, r[y] - qd[y]) / s;
+          int has_child = 0;
+          for (int c = u + 1; c < n; ++c) has_child |= par[c] == u;
+          const int np = nucleus_cuts(p, V, top_p, sorted, cuts_p);
+          const int nq = has_child ? nucleus_cuts(qd, V, top_p, sorted, cuts_q) : 1;
+          if (!has_child) cuts_q[0] = 0.0;   /* a leaf never reads q */
+          nucleus_apply(p, V, cuts_p[0], fp);
+          if (has_child) nucleus_apply(qd, V, cuts_q[0], fq);
+          next = node_decide(fp, fq, r, V, par, tok, n, u, b, seed, &token, &ties);
+          if (np < 0 || nq < 0 || np * nq > NUCLEUS_MAX_CUTS * 4) {
+            ++ties;   /* too many plausible nuclei to compare */
+          } else {
+            int differs = 0;
+            for (int i = 0; i < np && !differs; ++i)
+              for (int j = 0; j < nq && !differs; ++j) {
+                if (i == 0 && j == 0) continue;
+                int tk = -1, scratch_ties = 0;
+                nucleus_apply(p, V, cuts_p[i], vp);
+                if (has_child) nucleus_apply(qd, V, cuts_q[j], vq);
+                const int nx = node_decide(vp, has_child ? vq : fq, r, V, par, tok, n, u, b, seed,
+                                           &tk, &scratch_ties);
+                differs = nx != next || (nx < 0 && tk != token);
+              }
+            ties += differs;
+          }
+        } else {
+          next = node_decide(p, qd, r, V, par, tok, n, u, b, seed, &token, &ties);
         }
         if (next < 0) {
-          int tie = 0;
-          int x = sample_inverse_cdf(r, V, oracle_uniform(seed, u, b, 1), &tie);
-          ties += tie;
-          ot[acc] = x;
+          ot[acc] = token;
           break;
         }
       }
@@ -462,7 +537,7 @@ static int tree_verify_impl(const float *target_logits, const float *draft_logit
     accept_len[b] = acc;
     near_ties[b] = ties;
   }
-  free(p); free(qd); free(r);
+  free(p); free(qd); free(r); free(fp); free(fq); free(vp); free(vq); free(sorted);
   return OR_OK;
 }
 
