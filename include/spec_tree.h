@@ -191,6 +191,38 @@ int spec_tree_verify(const float *target_logits, const float *draft_logits,
                      void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
+ * spec_tree_verify_top_p — spec_tree_verify with the target and draft
+ * distributions of every node filtered to their top_p nucleus first.
+ *
+ * Source: SpecInfer developer article, deployment configuration (top_p as
+ * a sampling parameter of the serving system); the walk itself is the one
+ * of spec_tree_verify.  Reading: tau is the largest probability whose upper
+ * tail {x : p(x) >= tau} holds at least top_p of the mass; every entry of
+ * that tail is kept (entries tied at tau included), the rest drop to 0, and
+ * the tail is renormalised; q is filtered the same way with its own tau.
+ * Verification of the filtered pair is lossless for the filtered target.
+ *
+ * Arguments, layouts, workspace and errors are those of spec_tree_verify,
+ * plus top_p in (0, 1]; top_p >= 1 is spec_tree_verify; temperature 0
+ * (greedy) ignores top_p (the argmax is in every nucleus).  The nucleus is
+ * found by a radix search over the float bits of the probabilities with
+ * their mass summed in 2^-40 fixed point; its membership follows each
+ * entry's float value.  Near-ties (in near_ties) are counted, besides those
+ * of spec_tree_verify, for a child whose probability is within 128 ulps of
+ * tau, or a drawn token whose is, at a node where another entry lies that
+ * close to tau (their exact order may differ).  Host errors: SPEC_ERR_SHAPE
+ * for top_p <= 0 or NaN,
+ * and for top_p < 1 with V > 131072 (the nucleus search runs in the
+ * register-resident kernel only).
+ */
+int spec_tree_verify_top_p(const float *target_logits, const float *draft_logits,
+                           const int32_t *tokens, const int32_t *parents,
+                           const int32_t *tree_offsets, int B, int T, int V, float temperature,
+                           float top_p, uint64_t seed, int32_t *accept_len, int32_t *path_nodes,
+                           int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
+                           void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
  * spec_kv_compact — the depth-first KV-cache update after verification.
  *
  * Source: SpecInfer news write-up, section "Token 樹驗證器": the verifier

@@ -84,7 +84,7 @@ def assert_attn_close(got, ref, what=""):
 
 
 def gpu_verify(w, seed, W=None, temperature=None, target=None, draft="auto", tokens=None,
-               parents=None, offsets=None):
+               parents=None, offsets=None, top_p=1.0):
     target = w.target_logits if target is None else target
     if isinstance(draft, str):
         draft = w.draft_logits
@@ -99,17 +99,18 @@ def gpu_verify(w, seed, W=None, temperature=None, target=None, draft="auto", tok
     ws = ttv.make_verify_workspace(B, T, V)
     r = ttv.tree_verify(dev(target, torch.float32), None if (draft is None or temp == 0) else dev(draft, torch.float32),
                         dev(tokens, torch.int32), dev(parents, torch.int32), dev(offsets, torch.int32),
-                        temp, seed, W, status, ws)
+                        temp, seed, W, status, ws, top_p=top_p)
     torch.cuda.synchronize()
     out = {k: v.cpu().numpy() for k, v in r.items()}
     out["status"] = status.cpu().numpy()
     return out
 
 
-def oracle_verify(w, seed, W=None, temperature=None):
+def oracle_verify(w, seed, W=None, temperature=None, top_p=1.0):
     temp = w.temperature if temperature is None else temperature
     return oracle.tree_verify(w.target_logits, w.draft_logits if temp > 0 else None, w.tokens,
-                              w.parents, w.offsets, temp, seed, (w.max_depth + 1) if W is None else W)
+                              w.parents, w.offsets, temp, seed, (w.max_depth + 1) if W is None else W,
+                              top_p=top_p)
 
 
 def assert_verify_match(g, o, parents, tokens, offsets, what=""):

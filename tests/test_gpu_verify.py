@@ -13,9 +13,9 @@ import token_tree_verification_gb300 as ttv
 pytestmark = pytest.mark.gpu
 
 
-def check(w, seed, temperature=None, W=None):
-    g = gpu_verify(w, seed, W=W, temperature=temperature)
-    o = oracle_verify(w, seed, W=W, temperature=temperature)
+def check(w, seed, temperature=None, W=None, top_p=1.0):
+    g = gpu_verify(w, seed, W=W, temperature=temperature, top_p=top_p)
+    o = oracle_verify(w, seed, W=W, temperature=temperature, top_p=top_p)
     ties = assert_verify_match(g, o, w.parents, w.tokens, w.offsets, f"{w.name} seed {seed}")
     return g, o, ties
 
@@ -107,7 +107,8 @@ def _gpu_verify_np(tl, dl, tok, par, off, temp, seed, W, top_p=1.0):
     T, V = tl.shape
     status = torch.zeros(B, dtype=torch.int32, device="cuda")
     ws = ttv.make_verify_workspace(B, T, V)
-    r = ttv.tree_verify(dev(tl), dev(dl), dev(tok), dev(par), dev(off), temp, seed, W, status, ws)
+    r = ttv.tree_verify(dev(tl), dev(dl), dev(tok), dev(par), dev(off), temp, seed, W, status, ws,
+                        top_p=top_p)
     out = {k: v.cpu().numpy() for k, v in r.items()}
     assert (status.cpu().numpy() == 0).all()
     return out
@@ -135,3 +136,61 @@ def test_lossless_trials_match_oracle(gpu_lib):
     o = oracle.tree_verify(tl, dl, tok.reshape(-1), par, off, 0.8, 77, 4)
     ties = assert_verify_match(g, o, par, tok.reshape(-1), off, "lossless trials")
     assert ties <= n * 1e-4
+
+
+# ---- top-p (nucleus) verification: the same walk on the filtered p and q
+
+@pytest.mark.parametrize("top_p", [0.9, 0.5])
+def test_top_p_llama7b(gpu_lib, top_p):
+    w = synthetic.make_workload("llama7b", seed=0, L=64)
+    total_ties = 0
+    for seed in range(6):
+        g, o, ties = check(w, seed, top_p=top_p)
+        total_ties += ties
+    assert total_ties <= 1
+
+
+def test_top_p_dynamic(gpu_lib):
+    # At T = 0.4 both nuclei are a few entries wide: near-ties are rare.
+    w = synthetic.make_workload("dynamic", seed=0, temperature=0.4)
+    g, o, ties = check(w, 3, top_p=0.9)
+    assert ties <= 2 and (g["status"] == 0).all()
+    # At T = 0.8 the draft's nucleus holds thousands of entries of mass near
+    # 1e-6: its boundary is within rounding at most internal nodes, but the
+    # nuclei a rounding may pick almost never lead to different decisions.
+    w = synthetic.make_workload("dynamic", seed=1, temperature=0.8)
+    g, o, ties = check(w, 4, top_p=0.9)
+    assert ties <= 2 and (g["status"] == 0).all()
+
+
+def test_top_p_small_and_edge_vocabularies(gpu_lib):
+    for V in (1, 3, 8, 4097, 32003, 65536, 131072):
+        w = synthetic.make_workload("tiny", seed=V % 89, V=V, B=3, N=12, depth=3, width=4)
+        for top_p in (0.3, 0.95):
+            g, o, ties = check(w, V + 1, temperature=0.9, top_p=top_p)
+            assert ties <= 1
+
+
+def test_top_p_leaves_greedy_unchanged(gpu_lib):
+    w = synthetic.make_workload("tiny", seed=4, B=4, N=10, V=300)
+    a = gpu_verify(w, 2, temperature=0.0)
+    b = gpu_verify(w, 2, temperature=0.0, top_p=0.5)
+    for k in ("accept_len", "path_nodes", "out_tokens"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_top_p_errors(gpu_lib):
+    w = synthetic.make_workload("tiny", seed=5, B=2, N=6, V=131073)
+    with pytest.raises(RuntimeError):
+        gpu_verify(w, 0, temperature=1.0, top_p=0.9)    # beyond the register-resident kernel
+    w = synthetic.make_workload("tiny", seed=5, B=2, N=6, V=100)
+    for bad in (0.0, -0.5, float("nan")):
+        with pytest.raises(RuntimeError):
+            gpu_verify(w, 0, temperature=1.0, top_p=bad)
+
+
+def test_top_p_lossless_chi_square_gpu(gpu_lib):
+    c1, c2, p1, p12 = run_lossless(_gpu_verify_np, 1_000_000, 1.0, seed=6, top_p=0.8)
+    for c, p in ((c1, p1), (c2, p12)):
+        chi, bound = chi2_ok(c, p)
+        assert chi <= bound, (chi, bound)

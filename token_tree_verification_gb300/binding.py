@@ -56,6 +56,8 @@ def load():
     lib.spec_tree_verify_workspace_size.restype = SZ
     lib.spec_tree_verify.argtypes = [P, P, P, P, P, I, I, I, F, U64, P, P, P, P, I, P, SZ, P, P]
     lib.spec_tree_verify.restype = I
+    lib.spec_tree_verify_top_p.argtypes = [P, P, P, P, P, I, I, I, F, F, U64, P, P, P, P, I, P, SZ, P, P]
+    lib.spec_tree_verify_top_p.restype = I
     lib.spec_kv_compact.argtypes = [P, P, I, I, I, I, I, P, P, P, P, I, P, P, P]
     lib.spec_kv_compact.restype = I
     lib.spec_tree_expand.argtypes = [P, P, P, P, I, I, I, F, U64, P, P, P, P]
@@ -162,9 +164,10 @@ def make_verify_workspace(B, T, V, device="cuda"):
 
 
 def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperature: float,
-                seed: int, max_depth_plus1: int, status, workspace, outputs=None, stream=None):
-    """Steps V1-V4.  Returns dict(accept_len, path_nodes, out_tokens, near_ties)
-    of device tensors."""
+                seed: int, max_depth_plus1: int, status, workspace, outputs=None, stream=None,
+                top_p: float = 1.0):
+    """Steps V1-V4 (top_p < 1: on the top_p nucleus of p and of q).  Returns
+    dict(accept_len, path_nodes, out_tokens, near_ties) of device tensors."""
     lib = load()
     _dev(target_logits, torch.float32, "target_logits")
     if draft_logits is not None:
@@ -185,12 +188,22 @@ def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperatu
             out_tokens=torch.empty((B, W), dtype=torch.int32, device=dev),
             near_ties=torch.empty(B, dtype=torch.int32, device=dev),
         )
-    _check(lib.spec_tree_verify(_ptr(target_logits), _ptr(draft_logits), _ptr(tokens),
-                                _ptr(parents), _ptr(offsets), B, T, V, float(temperature),
-                                int(seed) & (2**64 - 1), _ptr(outputs["accept_len"]),
-                                _ptr(outputs["path_nodes"]), _ptr(outputs["out_tokens"]),
-                                _ptr(outputs["near_ties"]), W, _ptr(workspace), workspace.numel(),
-                                _ptr(status), _stream(stream)), "spec_tree_verify")
+    if top_p >= 1.0:
+        _check(lib.spec_tree_verify(_ptr(target_logits), _ptr(draft_logits), _ptr(tokens),
+                                    _ptr(parents), _ptr(offsets), B, T, V, float(temperature),
+                                    int(seed) & (2**64 - 1), _ptr(outputs["accept_len"]),
+                                    _ptr(outputs["path_nodes"]), _ptr(outputs["out_tokens"]),
+                                    _ptr(outputs["near_ties"]), W, _ptr(workspace),
+                                    workspace.numel(), _ptr(status), _stream(stream)),
+               "spec_tree_verify")
+        return outputs
+    _check(lib.spec_tree_verify_top_p(_ptr(target_logits), _ptr(draft_logits), _ptr(tokens),
+                                      _ptr(parents), _ptr(offsets), B, T, V, float(temperature),
+                                      float(top_p), int(seed) & (2**64 - 1),
+                                      _ptr(outputs["accept_len"]), _ptr(outputs["path_nodes"]),
+                                      _ptr(outputs["out_tokens"]), _ptr(outputs["near_ties"]), W,
+                                      _ptr(workspace), workspace.numel(), _ptr(status),
+                                      _stream(stream)), "spec_tree_verify_top_p")
     return outputs
 
 

@@ -376,13 +376,12 @@ extern "C" size_t spec_tree_verify_workspace_size(int B, int T, int V) {
   return align256(sizeof(uint32_t) * (B + 1)) + align256(sizeof(int32_t) * T) * 2;
 }
 
-extern "C" int spec_tree_verify(const float *target_logits, const float *draft_logits,
-                                const int32_t *tokens, const int32_t *parents,
-                                const int32_t *tree_offsets, int B, int T, int V,
-                                float temperature, uint64_t seed, int32_t *accept_len,
-                                int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
-                                int max_depth_plus1, void *workspace, size_t workspace_bytes,
-                                int32_t *status, void *stream) {
+namespace {
+int verify_entry(const float *target_logits, const float *draft_logits, const int32_t *tokens,
+                 const int32_t *parents, const int32_t *tree_offsets, int B, int T, int V,
+                 float temperature, float top_p, uint64_t seed, int32_t *accept_len,
+                 int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
+                 void *workspace, size_t workspace_bytes, int32_t *status, void *stream) {
   using namespace spec;
   if (!target_logits || !tokens || !parents || !tree_offsets || !accept_len || !path_nodes ||
       !out_tokens || !near_ties || !status)
@@ -392,6 +391,9 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
   if (!(temperature >= 0.f) || temperature > 1e4f) return SPEC_ERR_SHAPE;  // rejects NaN too
   const bool greedy = temperature == 0.f;
   if (!greedy && !draft_logits) return SPEC_ERR_NULL;
+  if (!(top_p > 0.f)) return SPEC_ERR_SHAPE;   // rejects NaN too
+  const bool nucleus = !greedy && top_p < 1.f;   // the argmax is in every nucleus
+  if (nucleus && V > kMaxCS * kRegChunk) return SPEC_ERR_SHAPE;
   const size_t need = spec_tree_verify_workspace_size(B, T, V);
   if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 15) return SPEC_ERR_ALIGNMENT;
@@ -416,6 +418,7 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
   args.W = max_depth_plus1;
   args.temp = temperature;
   args.inv_temp = greedy ? 0.f : 1.0f / temperature;
+  args.top_p = nucleus ? top_p : 1.f;
   args.seed = seed;
   args.accept_len = accept_len;
   args.path_nodes = path_nodes;
@@ -431,7 +434,8 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
 
   if (greedy) return launch_verify_greedy(args, static_cast<cudaStream_t>(stream));
   if (V <= kMaxCS * kRegChunk)
-    return launch_verify_reg(args, (V + kRegChunk - 1) / kRegChunk, static_cast<cudaStream_t>(stream));
+    return launch_verify_reg(args, (V + kRegChunk - 1) / kRegChunk, nucleus,
+                             static_cast<cudaStream_t>(stream));
   const size_t smem = sizeof(float) * 2 * static_cast<size_t>(chunk);
   static int configured_smem = -1;
   if (configured_smem < static_cast<int>(smem)) {
@@ -455,4 +459,30 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
   cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, tree_verify_cluster_kernel, args) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
+}
+}  // namespace
+
+extern "C" int spec_tree_verify(const float *target_logits, const float *draft_logits,
+                                const int32_t *tokens, const int32_t *parents,
+                                const int32_t *tree_offsets, int B, int T, int V,
+                                float temperature, uint64_t seed, int32_t *accept_len,
+                                int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
+                                int max_depth_plus1, void *workspace, size_t workspace_bytes,
+                                int32_t *status, void *stream) {
+  return verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
+                      temperature, 1.f, seed, accept_len, path_nodes, out_tokens, near_ties,
+                      max_depth_plus1, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" int spec_tree_verify_top_p(const float *target_logits, const float *draft_logits,
+                                      const int32_t *tokens, const int32_t *parents,
+                                      const int32_t *tree_offsets, int B, int T, int V,
+                                      float temperature, float top_p, uint64_t seed,
+                                      int32_t *accept_len, int32_t *path_nodes,
+                                      int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
+                                      void *workspace, size_t workspace_bytes, int32_t *status,
+                                      void *stream) {
+  return verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
+                      temperature, top_p, seed, accept_len, path_nodes, out_tokens, near_ties,
+                      max_depth_plus1, workspace, workspace_bytes, status, stream);
 }

@@ -33,6 +33,7 @@ struct VerifyArgs {
   int B, T, V, chunk, W;
   float temp;     // 0 => greedy
   float inv_temp;
+  float top_p;    // nucleus mass (1: no filter)
   uint64_t seed;
   int32_t *accept_len, *path_nodes, *out_tokens, *near_ties, *status;
   int32_t *flags;      // [T] written by the parent's CTA group: accept / tie bits
@@ -385,6 +386,6 @@ int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream);
 // stochastic kernel with the rows in registers (verify_reg.cu): CTAs of
 // kRegChunk vocabulary entries, `cs` = ceil(V / kRegChunk) <= kMaxCS per node
 constexpr int kRegChunk = 16384;
-int launch_verify_reg(const VerifyArgs &args, int cs, cudaStream_t stream);
+int launch_verify_reg(const VerifyArgs &args, int cs, bool top_p, cudaStream_t stream);
 
 }  // namespace spec

@@ -47,7 +47,49 @@ struct RegExchange {
 struct NodeScalars {
   float P[SPEC_MAX_TREE_NODES], Q[SPEC_MAX_TREE_NODES], U[SPEC_MAX_TREE_NODES];
   float u_fb;
+  int near;                          // top-p: bit 0 (p) / 1 (q): an entry other than tau is near it
+  int ctie[SPEC_MAX_TREE_NODES];     // top-p: child j's entry is near tau at such a node
 };
+
+// Top-p working storage (dynamic shared memory).  Masses are fixed point,
+// value * 2^40 rounded to u64, so histogram sums are exact and independent
+// of the order of the atomic adds, and the rounding of a whole row stays
+// below V * 2^-41 of its mass.
+struct TopPSmem {
+  unsigned long long warp_hist[kRWarps][2][256];   // per warp: [row (p, q)][8-bit digit]
+  unsigned long long cta[2][2][256];               // the CTA's histogram, by pass parity
+  unsigned long long recv[2][kMaxCS][2][256];      // every CTA's histogram, by pass parity
+  unsigned long long hsum[2][256];                 // the group's histogram
+  unsigned long long state[2][4];   // per row: prefix bits, mass above, digit mass, target
+  float2 statp[kMaxCS][kRWarps];    // per warp: its mass of the filtered p, near flags
+  uint64_t bar[2], sbar;
+};
+constexpr uint32_t kHistBytes = 2 * 256 * 8;  // one CTA histogram
+constexpr float kFixedScale = 1099511627776.f;  // 2^40
+// Entries other than tau within this many ulps of it may be ordered the
+// other way round in exact arithmetic (the exponentials' rounding).
+constexpr int kTauUlps = 128;
+
+__device__ __forceinline__ unsigned long long fixed_mass(float v) {
+  return __float2ull_rn(v * kFixedScale);
+}
+// hist[bin] += fixed_mass(v), as one unit: the scaling, the conversion and
+// the shared-memory add stay together, so that an unrolled loop over a
+// thread's entries does not hold all their conversions in registers at once.
+__device__ __forceinline__ void hist_add(uint32_t saddr, float v) {
+  asm volatile(
+      "{\n\t.reg .f32 s;\n\t.reg .u64 m;\n\t"
+      "mul.rn.f32 s, %1, 0f53800000;\n\t"   // v * 2^40 (exact)
+      "cvt.rni.u64.f32 m, s;\n\t"
+      "red.shared.add.u64 [%0], m;\n\t}"
+      :
+      : "r"(saddr), "f"(v)
+      : "memory");
+}
+__device__ __forceinline__ bool near_bits(uint32_t x, uint32_t t) {
+  const int d = static_cast<int>(x - t);
+  return d >= -kTauUlps && d <= kTauUlps;
+}
 constexpr int kScalarWarp = kRWarps - 1;
 
 // 32 entries of a row into registers; entries at or past `end` read as -inf.
@@ -93,8 +135,10 @@ __device__ __forceinline__ float warp_scan(float v, int lane) {  // inclusive
 
 }  // namespace
 
+template <bool TOPP>
 __global__ void __launch_bounds__(kRThreads, 1)
 tree_verify_reg_kernel(const VerifyArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];   // TopPSmem when TOPP
   __shared__ __align__(16) RegExchange ex;
   __shared__ TreeSmem ts;
   __shared__ NodeScalars ns;
@@ -117,6 +161,12 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) mbar_init(&xbar[i], 1);
     mbar_init(&nbar, 1);
+    if constexpr (TOPP) {
+      TopPSmem &tp = *reinterpret_cast<TopPSmem *>(dyn_smem);
+      mbar_init(&tp.bar[0], 1);
+      mbar_init(&tp.bar[1], 1);
+      mbar_init(&tp.sbar, 1);
+    }
     fence_barrier_init();
   }
   pdl_wait();
@@ -167,6 +217,8 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   int stop = k;        // first accepted child, k when every child is rejected
   int my_flag = 0;     // thread j < k: the flag of child j
   int p_ok = -1;       // parity of the last reduction round that moved the residual
+  int near = 0;            // top-p: ns.near
+  uint32_t tau_kept[2] = {0u, 0u};   // top-p: tau of p and q after renormalisation
   float c_prev = 0.f, Ml = 0.f, Sp = 1.f;
   const float l2s = a.inv_temp * 1.4426950408889634f;  // exp(x / T) = 2^(x * l2s)
   if (!c.err) {
@@ -243,21 +295,211 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       xp[m].x *= sc_l; xp[m].y *= sc_l; xp[m].z *= sc_l; xp[m].w *= sc_l;
       xq[m].x *= sc_d; xq[m].y *= sc_d; xq[m].z *= sc_d; xq[m].w *= sc_d;
     }
+    // ---- top-p: the nucleus of p and of q.  tau is the largest entry whose
+    //      upper tail {x >= tau} holds at least top_p of the mass; entries of
+    //      that tail keep their mass, renormalised, the rest drop to 0.  The
+    //      float bits of non-negative entries order like the values, so tau
+    //      is found by 4 radix passes of 8 bits over them: each pass sums the
+    //      fixed-point mass of the entries still in play per 8-bit digit
+    //      (per-warp histograms, a CTA histogram, the group's by bulk copy)
+    //      and keeps the digit where the running mass from the top reaches
+    //      top_p.
+    uint32_t tau_bits[2] = {0u, 0u};
+    float inv_nuc[2] = {1.f, 1.f};
+    if constexpr (TOPP) {
+      TopPSmem &tp = *reinterpret_cast<TopPSmem *>(dyn_smem);
+      // state[r] = {prefix bits of tau, mass above the prefix's digit range,
+      // mass of the kept digit, target}; rows p (0) and q (1)
+      if (tid < 8) (&tp.state[0][0])[tid] = 0ull;
+      __syncthreads();
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        const int par = pass & 1;
+        const uint32_t hi_p = static_cast<uint32_t>(tp.state[0][0]) >> (shift + 8);
+        const uint32_t hi_q = static_cast<uint32_t>(tp.state[1][0]) >> (shift + 8);
+        unsigned long long *wh = &tp.warp_hist[w_id][0][0];
+        const uint32_t wh_addr = smem_addr(wh);
+        for (int i = lane; i < 512; i += 32) wh[i] = 0ull;
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < kRVec; ++m) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const float v = pick4(xp[m], cc);
+            const uint32_t bits = __float_as_uint(v);
+            if (bits != 0u && (pass == 0 || (bits >> (shift + 8)) == hi_p))
+              hist_add(wh_addr + 8u * ((bits >> shift) & 255u), v);
+          }
+        }
+        if (need_draft) {
+#pragma unroll
+          for (int m = 0; m < kRVec; ++m) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const float v = pick4(xq[m], cc);
+              const uint32_t bits = __float_as_uint(v);
+              if (bits != 0u && (pass == 0 || (bits >> (shift + 8)) == hi_q))
+                hist_add(wh_addr + 8u * (256u + ((bits >> shift) & 255u)), v);
+            }
+          }
+        }
+        __syncthreads();
+        {
+          const int row = tid >> 8, bin = tid & 255;   // 512 threads: 2 rows x 256 digits
+          unsigned long long h = 0ull;
+#pragma unroll
+          for (int ww = 0; ww < kRWarps; ++ww) h += tp.warp_hist[ww][row][bin];
+          tp.cta[par][row][bin] = h;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          mbar_arrive_expect_tx(&tp.bar[par], static_cast<uint32_t>(CS) * kHistBytes);
+          for (int r = 0; r < CS; ++r)
+            bulk_copy_s2s(peer_addr(&tp.recv[par][rank][0][0], r), smem_addr(&tp.cta[par][0][0]),
+                          kHistBytes, peer_addr(&tp.bar[par], r));
+        }
+        if (ok && !mbar_wait(&tp.bar[par], (pass >> 1) & 1)) ok = false;
+        {
+          const int row = tid >> 8, bin = tid & 255;
+          unsigned long long h = 0ull;
+          for (int r = 0; r < CS; ++r) h += tp.recv[par][r][row][bin];
+          tp.hsum[row][bin] = h;
+        }
+        __syncthreads();
+        if (w_id < (need_draft ? 2 : 1)) {
+          // warp r: the digit of row r where the running mass from the top
+          // reaches the target (lane l holds digits 255 - 8l .. 248 - 8l)
+          const int r = w_id;
+          const unsigned long long *hr = &tp.hsum[r][0];
+          unsigned long long lsum = 0ull;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) lsum += hr[255 - 8 * lane - i];
+          unsigned long long inc = lsum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          const unsigned long long prefix = tp.state[r][0], above = tp.state[r][1];
+          unsigned long long target = tp.state[r][3];
+          if (pass == 0) {
+            // rounding may leave the row's total below top_p (then all is
+            // kept); a top_p below the fixed-point unit keeps the top entry
+            const unsigned long long total = __shfl_sync(0xffffffffu, inc, 31);
+            target = max(1ull, min(fixed_mass(a.top_p), total));
+          }
+          const uint32_t hm = __ballot_sync(0xffffffffu, above + inc >= target);
+          const int L = hm ? __ffs(hm) - 1 : 31;
+          if (lane == L) {
+            // the crossing digit; without one (an all-zero row) the lowest
+            unsigned long long run = above + inc - lsum, new_above = above, dmass = 0ull;
+            int digit = 0;
+            bool found = false;
+            for (int i = 0; i < 8 && !found; ++i) {
+              const unsigned long long h = hr[255 - 8 * lane - i];
+              if (run + h >= target || (hm == 0u && i == 7)) {
+                found = true;
+                digit = 255 - 8 * lane - i;
+                new_above = run;
+                dmass = h;
+              }
+              run += h;
+            }
+            tp.state[r][0] = prefix | (static_cast<unsigned long long>(digit) << shift);
+            tp.state[r][1] = new_above;
+            tp.state[r][2] = dmass;
+            tp.state[r][3] = target;
+          }
+        }
+        __syncthreads();
+      }
+      // the nucleus: entries whose bits are >= tau's, renormalised.  An
+      // entry other than tau within kTauUlps of it may sit on the other side
+      // of tau in exact arithmetic: the node records that it has one, and
+      // decisions that involve an entry near tau count as near-ties.
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const unsigned long long ge = tp.state[r][1] + tp.state[r][2];
+        tau_bits[r] = static_cast<uint32_t>(tp.state[r][0]);
+        inv_nuc[r] = ge > 0ull ? kFixedScale / static_cast<float>(ge) : 0.f;
+        tau_kept[r] = __float_as_uint(__uint_as_float(tau_bits[r]) * inv_nuc[r]);
+      }
+      bool near_p = false, near_q = false;
+      auto keep = [&](float v, int r, bool &nr) -> float {
+        const uint32_t bits = __float_as_uint(v);
+        nr |= bits != tau_bits[r] && near_bits(bits, tau_bits[r]);
+        return bits >= tau_bits[r] ? v * inv_nuc[r] : 0.f;
+      };
+#pragma unroll
+      for (int m = 0; m < kRVec; ++m) {
+        xp[m].x = keep(xp[m].x, 0, near_p);
+        xp[m].y = keep(xp[m].y, 0, near_p);
+        xp[m].z = keep(xp[m].z, 0, near_p);
+        xp[m].w = keep(xp[m].w, 0, near_p);
+        if (need_draft) {
+          xq[m].x = keep(xq[m].x, 1, near_q);
+          xq[m].y = keep(xq[m].y, 1, near_q);
+          xq[m].z = keep(xq[m].z, 1, near_q);
+          xq[m].w = keep(xq[m].w, 1, near_q);
+        }
+      }
+      // every warp's mass of the filtered p and its near flag, to every CTA
+      float sf = 0.f;
+#pragma unroll
+      for (int m = 0; m < kRVec; ++m) sf += (xp[m].x + xp[m].y) + (xp[m].z + xp[m].w);
+      sf = warp_sum(sf);
+      const float nflags = (__any_sync(0xffffffffu, near_p) ? 1.f : 0.f) +
+                           (__any_sync(0xffffffffu, near_q) ? 2.f : 0.f);
+      if (tid == 0) mbar_arrive_expect_tx(&tp.sbar, static_cast<uint32_t>(CS * kRWarps * 8));
+      if (lane < CS)
+        st_async_v2_f32(peer_addr(&tp.statp[rank][w_id].x, lane), sf, nflags,
+                        peer_addr(&tp.sbar, lane));
+      if (ok && !mbar_wait(&tp.sbar, 0)) ok = false;
+    }
     // the children's p and q from their raw logits (scalar warp), published
     // with the uniforms through an mbarrier (release / acquire)
     if (scalar_warp) {
+      int nb = 0;
+      if constexpr (TOPP) {
+        const TopPSmem &tp = *reinterpret_cast<const TopPSmem *>(dyn_smem);
+        for (int i = lane; i < CS * kRWarps; i += 32) nb |= static_cast<int>((&tp.statp[0][0])[i].y);
+        nb = __reduce_or_sync(0xffffffffu, static_cast<unsigned>(nb));
+      }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const int j = lane + 32 * s;
         if (j < k) {
-          ns.P[j] = precise_prob(rawP[s], Ml, a.temp, a.inv_temp, 1.f) * inv_sp;
-          ns.Q[j] = precise_prob(rawQ[s], Md, a.temp, a.inv_temp, 1.f) * inv_sq;
+          float P = precise_prob(rawP[s], Ml, a.temp, a.inv_temp, 1.f) * inv_sp;
+          float Q = precise_prob(rawQ[s], Md, a.temp, a.inv_temp, 1.f) * inv_sq;
+          if constexpr (TOPP) {
+            // Membership follows the child's own entry of the filtered rows:
+            // the same operations on the same operands as its owner thread
+            // (warp maximum from the exchanged statistics, the same exp path).
+            const int x = ts.tok[ts.child[j]];
+            const int r = x / kRegChunk, off = x - r * kRegChunk;
+            const int wo = off / kRSpan, mo = (off % kRSpan) >> 7;
+            const float4 st = ex.stat[r][wo];
+            const float zp = fmaf(rawP[s], l2s, -st.x * l2s), zq = fmaf(rawQ[s], l2s, -st.z * l2s);
+            const float eP = (mo < kRVec / 2 ? fast_exp2(zp) : exp2_taylor(zp)) *
+                             (fast_exp2((st.x - Ml) * l2s) * inv_sp);
+            const float eQ = (mo < kRVec / 2 ? fast_exp2(zq) : exp2_taylor(zq)) *
+                             (fast_exp2((st.z - Md) * l2s) * inv_sq);
+            P = __float_as_uint(eP) >= tau_bits[0] ? P * inv_nuc[0] : 0.f;
+            Q = __float_as_uint(eQ) >= tau_bits[1] ? Q * inv_nuc[1] : 0.f;
+            ns.ctie[j] = ((nb & 1) && near_bits(__float_as_uint(eP), tau_bits[0])) ||
+                         ((nb & 2) && near_bits(__float_as_uint(eQ), tau_bits[1]));
+          }
+          ns.P[j] = P;
+          ns.Q[j] = Q;
         }
       }
+      if (lane == 0) ns.near = nb;
       __syncwarp();
       if (lane == 0) mbar_arrive(&nbar);
     }
     if (ok && !mbar_wait(&nbar, 0)) ok = false;
+    if (TOPP) near = ns.near;
 
     // ---- V2: the children's accept tests in index order, stopping at the
     //      first accepted child (the walk never looks past it).  The test
@@ -280,6 +522,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         accept = true;
         tie = 1.f - U < kTieBand;
       }
+      if (TOPP) tie |= ns.ctie[j] != 0;
       if (tid == j) my_flag = (accept ? kFlagAccept : 0) | (tie ? kFlagTie : 0);
       if (accept) {
         stop = j;
@@ -328,6 +571,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       // the mass of warp w of slice r under the final residual
       auto mass = [&](int r, int w) -> float {
         if (p_ok >= 0) return ex.part[p_ok][r][w];
+        if constexpr (TOPP) return reinterpret_cast<const TopPSmem *>(dyn_smem)->statp[r][w].x;
         const float4 e = ex.stat[r][w];
         return e.y > 0.f ? e.y * fast_exp2((e.x - Ml) * l2s) / Sp : 0.f;
       };
@@ -386,6 +630,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
             run2 += cs_;
           }
           int pick = -1;
+          bool pick_near = false;
           float cb0 = target, cb1 = target;
           if (ms >= 0) {
             // level 3: the step's lanes; level 4: the lane's four entries
@@ -408,6 +653,10 @@ tree_verify_reg_kernel(const VerifyArgs a) {
                     pick = base + 128 * ms + cc;
                     cb0 = cum;
                     cb1 = cum + wv;
+                    // top-p: a drawn entry near tau (filtered values compared
+                    // with tau filtered the same way)
+                    pick_near = ((near & 1) && near_bits(__float_as_uint(pick4(pp, cc)), tau_kept[0])) ||
+                                ((near & 2) && near_bits(__float_as_uint(pick4(qq, cc)), tau_kept[1]));
                   }
                   cum += wv;
                 }
@@ -419,6 +668,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
                 }
               }
               pick = __shfl_sync(0xffffffffu, pick, L);
+              pick_near = __shfl_sync(0xffffffffu, pick_near, L);
               cb0 = __shfl_sync(0xffffffffu, cb0, L);
               cb1 = __shfl_sync(0xffffffffu, cb1, L);
             }
@@ -436,7 +686,8 @@ tree_verify_reg_kernel(const VerifyArgs a) {
             cb0 = cb1 = target;
           }
           if (lane == 0) {
-            const bool tie = fabsf(target - cb0) < kTieBand * total || fabsf(target - cb1) < kTieBand * total;
+            const bool tie = pick_near || fabsf(target - cb0) < kTieBand * total ||
+                             fabsf(target - cb1) < kTieBand * total;
             a.fallback[t] = pick | (tie ? (1 << 31) : 0);
           }
         } else if (sw < 0) {
@@ -471,11 +722,20 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   if (CS > 1) cluster_wait();
 }
 
-int launch_verify_reg(const VerifyArgs &args, int cs, cudaStream_t stream) {
+int launch_verify_reg(const VerifyArgs &args, int cs, bool top_p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(args.T) * cs, 1, 1);
   cfg.blockDim = dim3(kRThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = top_p ? sizeof(TopPSmem) : 0;
+  if (top_p) {
+    static bool configured = false;
+    if (!configured) {
+      if (cudaFuncSetAttribute(tree_verify_reg_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sizeof(TopPSmem))) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      configured = true;
+    }
+  }
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -485,8 +745,9 @@ int launch_verify_reg(const VerifyArgs &args, int cs, cudaStream_t stream) {
   pdl_attribute(attr[1]);
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, tree_verify_reg_kernel, args) == cudaSuccess ? SPEC_OK
-                                                                              : SPEC_ERR_CUDA;
+  const cudaError_t e = top_p ? cudaLaunchKernelEx(&cfg, tree_verify_reg_kernel<true>, args)
+                              : cudaLaunchKernelEx(&cfg, tree_verify_reg_kernel<false>, args);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace spec
