@@ -336,7 +336,8 @@ def run_native(args, rank, world, local_rank):
         "clocks": clocks, "clock_window": "timed region + 1 s soak of the same graph" if soak else "timed region",
     }
     result["next_rows"] = {"kv_compact": time_kv_compact(st, stream, chunk),
-                           "tree_build": time_tree_build(w, stream, chunk)}
+                           "tree_build": time_tree_build(w, stream, chunk),
+                           "top_p": time_verify_top_p(st, stream, chunk)}
     if not args.no_e2e:
         result["e2e"] = run_e2e(st, w, stream, args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -412,6 +413,38 @@ def time_kv_compact(st, stream, n, reps=3):
     moved = int(acc_h.sum()) * w.Hkv * w.D * w.k_cache.element_size() * 2 * 2
     return {"us": best * 1e3, "accept_len": acc_h.tolist(), "bytes": moved,
             "gbs": moved / (best * 1e-3) / 1e9,
+            "timing": f"CUDA graph of {n} launches, events on the launching stream"}
+
+
+def time_verify_top_p(st, stream, n, reps=3, top_p=0.9):
+    """Stochastic verification with both distributions filtered to their
+    top_p nucleus, timed alone like the step's verify kernel: a graph of n
+    launches over the rotating logits copies."""
+    import torch
+    ttv, w = st.ttv, st.w
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            c = st.copies[i % len(st.copies)]
+            ttv.tree_verify(c["tl"], c["dl"], st.tok, st.par, st.off, w.temperature, st.seed + i,
+                            st.W, st.status, st.ws, outputs=st.outs, top_p=top_p)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        best = ms if best is None else min(best, ms)
+    if (st.status.cpu().numpy() != 0).any():
+        raise RuntimeError(f"verify status {st.status.cpu().tolist()}")
+    rows = verify_bytes(w)
+    return {"us": best * 1e3, "top_p": top_p, "bytes": rows, "gbs": rows / (best * 1e-3) / 1e9,
             "timing": f"CUDA graph of {n} launches, events on the launching stream"}
 
 
