@@ -271,8 +271,11 @@ int spec_kv_compact(void *k_cache, void *v_cache, int dtype, int B, int Hkv, int
  *   temperature == 0: q = softmax(draft); the children are the width most
  *     likely tokens in order, ties to the lower index.
  * child_scores[f][j] = parent_scores[f] + log q(child_tokens[f][j]);
- * near_ties[f][j] = 1 when a draw lay within 1e-6 of an inverse-CDF boundary.
- *   width <= 16.  All arrays are device memory; no device-side errors.
+ * near_ties[f][j] = 1 when a draw lay within 1e-6 of an inverse-CDF boundary,
+ *   -1 when an exchange between the CTAs that share row f timed out (the
+ *   row's outputs are then unreliable; not expected in normal operation).
+ *   width <= 16.  All arrays are device memory.  A row is split over
+ *   ceil(V / 8192) CTAs (at most 8) of one thread-block cluster.
  */
 int spec_tree_expand(const float *draft_logits, const float *parent_scores,
                      const int32_t *node_ids, const int32_t *requests, int F, int V, int width,

@@ -18,13 +18,17 @@ def _expand_gpu(d, ps, nodes, reqs, width, T, seed):
     return tok.cpu().numpy(), sc.cpu().numpy(), ties.cpu().numpy()
 
 
-@pytest.mark.parametrize("V,width", [(32000, 5), (1000, 16), (16, 16), (1, 1), (4097, 3)])
+@pytest.mark.parametrize("V,width", [(32000, 5), (1000, 16), (16, 16), (1, 1), (4097, 3),
+                                     (8193, 4), (100000, 7)])
 def test_greedy_expansion(V, width):
+    # V > 8192 splits each row over a cluster of CTAs (one slice each)
     rng = np.random.default_rng(V)
     F = 7
     d = (rng.standard_normal((F, V)) * 3).astype(np.float32)
     if V > 20:
         d[1, [5, 17, 3]] = d[1].max() + 2.0          # tie at the top: lower index first
+    if V > 30000:
+        d[2, [30000, 9000, 20]] = d[2].max() + 3.0   # the same across slices
     ps = rng.standard_normal(F).astype(np.float32)
     nodes, reqs = np.arange(F), np.zeros(F)
     tg, sg, _ = _expand_gpu(d, ps, nodes, reqs, width, 0.0, 1)
@@ -33,7 +37,8 @@ def test_greedy_expansion(V, width):
     np.testing.assert_allclose(sg, so, rtol=0, atol=2e-4)
 
 
-@pytest.mark.parametrize("V,width,T", [(32000, 5, 0.7), (1000, 16, 1.0), (50, 8, 2.5), (65536, 4, 0.3)])
+@pytest.mark.parametrize("V,width,T", [(32000, 5, 0.7), (1000, 16, 1.0), (50, 8, 2.5), (65536, 4, 0.3),
+                                       (8193, 6, 1.0), (131077, 3, 0.8)])
 def test_sampled_expansion(V, width, T):
     rng = np.random.default_rng(V + width)
     F = 12

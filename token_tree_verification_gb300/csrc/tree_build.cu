@@ -13,6 +13,8 @@
 // score is its parent's plus log q(token).
 // Pruning: one CTA per request; the root and the keep - 1 best other
 // candidates by (score desc, index asc) survive, renumbered in order.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace spec {
@@ -22,6 +24,8 @@ namespace {
 constexpr int kExThreads = 512;
 constexpr int kExWarps = kExThreads / 32;
 constexpr int kMaxWidth = 16;
+constexpr int kExSlice = 8192;   // vocabulary entries per CTA of an expansion cluster
+constexpr int kExMaxCS = 8;
 constexpr int kPruneThreads = 1024;
 constexpr float kDrawTieBand = 1e-6f;
 
@@ -66,29 +70,59 @@ __device__ __forceinline__ uint64_t philox_word0(uint64_t seed, uint64_t c0, uin
   return philox4x64_10(c, seed, 0).w[0];
 }
 
+// Expansion of one frontier row by a cluster of CS CTAs, CTA `rank` taking
+// the slice [v0, v1) of the vocabulary.  The slices' (max, sum) pairs go to
+// every CTA (st.async, completing on each CTA's barrier) and are combined in
+// rank order, so every CTA holds the same M and S.  Greedy: each CTA finds its
+// slice's best `width` tokens and rank 0 merges the CS lists.  Sampled: each
+// CTA scans its slice in contiguous chunks; the slice totals go to every CTA,
+// and slice r owns [P_r, P_r + T_r) of [0, S) with P_r = T_0 + ... + T_{r-1}
+// added in rank order, so the slices (and the chunks inside them) partition
+// [0, S) exactly and each draw is taken by exactly one chunk.
 __global__ void __launch_bounds__(kExThreads, 1)
 tree_expand_kernel(const ExpandArgs a) {
   __shared__ float s_m[kExWarps], s_s[kExWarps];
   __shared__ Cand s_c[kExWarps];
   __shared__ float s_scan[kExWarps];
-  __shared__ float s_pre[kExThreads];   // each chunk's exclusive prefix
-  __shared__ float s_u[kMaxWidth];
+  __shared__ float s_pre[kExThreads];   // each chunk's exclusive prefix within the slice
+  __shared__ float s_u[kMaxWidth], s_val[kMaxWidth];
   __shared__ int s_tok[kMaxWidth], s_tie[kMaxWidth], s_claim[kMaxWidth];
   __shared__ float s_M, s_S;
-  const int f = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  __shared__ __align__(16) float2 x_stat[kExMaxCS];            // every slice's (max, scaled sum)
+  __shared__ __align__(16) float x_tot[kExMaxCS];              // every slice's total (sampled)
+  __shared__ __align__(16) float2 x_cand[kExMaxCS][kMaxWidth];  // rank 0: every slice's list
+  __shared__ __align__(8) uint64_t xbar[2];
+  const int CS = static_cast<int>(cluster_size());
+  const int rank = static_cast<int>(cluster_rank());
+  const int f = blockIdx.x / CS, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int V = a.V, W = a.width;
   const bool greedy = !(a.temp > 0.f);
+  const int slice = (V + CS - 1) / CS;
+  const int v0 = min(V, rank * slice), v1 = min(V, v0 + slice);
+  if (tid == 0) {
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&xbar[0], static_cast<uint32_t>(CS * 8));
+    if (!greedy) mbar_arrive_expect_tx(&xbar[1], static_cast<uint32_t>(CS * 4));
+    else if (rank == 0) mbar_arrive_expect_tx(&xbar[1], static_cast<uint32_t>(CS * W * 8));
+  }
+  cluster_arrive_relaxed();   // barriers initialised; waited for before the first remote store
   pdl_trigger();
   pdl_wait();
   const float *row = a.draft + static_cast<size_t>(f) * V;
+  bool ok = true;
 
-  // ---- pass A: max and sum of 2^((x - max) * l2s); the greedy draft also
-  //      keeps each thread's best `width` candidates
+  // ---- pass A over the slice: max and sum of 2^((x - max) * l2s); the
+  //      greedy draft also keeps each thread's best `width` candidates
   Cand best[kMaxWidth];
 #pragma unroll
   for (int j = 0; j < kMaxWidth; ++j) best[j] = Cand{-INFINITY, 0x7fffffff};
   float m = -INFINITY, s = 0.f;
-  for (int x = tid; x < V; x += kExThreads) {
+  for (int x = v0 + tid; x < v1; x += kExThreads) {
     const float v = __ldg(row + x);
     if (v > m) {
       s = (m == -INFINITY ? 0.f : s * fast_exp2((m - v) * a.l2s)) + 1.f;
@@ -120,19 +154,31 @@ tree_expand_kernel(const ExpandArgs a) {
     if (w == 0) {
       const float pm = lane < kExWarps ? s_m[lane] : -INFINITY;
       const float ps = lane < kExWarps ? s_s[lane] : 0.f;
-      const float M = wmax(pm);
-      const float S = wsum(ps > 0.f ? ps * fast_exp2((pm - M) * a.l2s) : 0.f);
-      if (lane == 0) {
-        s_M = M;
-        s_S = S;
-      }
+      const float Mr = wmax(pm);
+      const float Sr = wsum(ps > 0.f ? ps * fast_exp2((pm - Mr) * a.l2s) : 0.f);
+      cluster_wait();
+      if (lane < CS)
+        st_async_v2_f32(peer_addr(&x_stat[rank], lane), Mr, Sr, peer_addr(&xbar[0], lane));
+    } else {
+      cluster_wait();
+    }
+    if (!mbar_wait(&xbar[0], 0)) ok = false;
+    float M = -INFINITY;
+    for (int q = 0; q < CS; ++q) M = fmaxf(M, x_stat[q].x);
+    float S = 0.f;
+    for (int q = 0; q < CS; ++q)
+      if (x_stat[q].y > 0.f) S += x_stat[q].y * fast_exp2((x_stat[q].x - M) * a.l2s);
+    if (tid == 0) {
+      s_M = M;
+      s_S = S;
     }
     __syncthreads();
   }
   const float M = s_M;
 
   if (greedy) {
-    // ---- `width` rounds of a block-wide argmax over the threads' list heads
+    // ---- the slice's best `width`: rounds of a block-wide argmax over the
+    //      threads' list heads
     int head = 0;
     for (int j = 0; j < W; ++j) {
       Cand c = head < W ? best[0] : Cand{-INFINITY, 0x7fffffff};
@@ -155,17 +201,63 @@ tree_expand_kernel(const ExpandArgs a) {
         }
         if (lane == 0) {
           s_tok[j] = b.i;
-          s_tie[j] = 0;
+          s_val[j] = b.v;
         }
       }
       __syncthreads();
-      // the owner of the winner (token x belongs to thread x % threads) pops it
-      if (s_tok[j] % kExThreads == tid && s_tok[j] >= 0 && s_tok[j] < V) ++head;
+      // the owner of the winner (token x belongs to thread (x - v0) % threads) pops it
+      const int x = s_tok[j];
+      if (x >= v0 && x < v1 && (x - v0) % kExThreads == tid) ++head;
+    }
+    // ---- rank 0 merges the CS lists
+    if (tid < W)
+      st_async_v2_f32(peer_addr(&x_cand[rank][tid], 0), s_val[tid], __int_as_float(s_tok[tid]),
+                      peer_addr(&xbar[1], 0));
+    if (rank == 0) {
+      if (!mbar_wait(&xbar[1], 0)) ok = false;
+      if (w == 0) {
+        Cand c[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int e = lane + 32 * k;   // candidate e: list e / W, entry e % W
+          c[k] = e < CS * W ? Cand{x_cand[e / W][e % W].x, __float_as_int(x_cand[e / W][e % W].y)}
+                            : Cand{-INFINITY, 0x7fffffff};
+        }
+        for (int j = 0; j < W; ++j) {
+          Cand b = c[0];
+          int kb = 0;
+#pragma unroll
+          for (int k = 1; k < 4; ++k)
+            if (cand_before(c[k], b)) {
+              b = c[k];
+              kb = k;
+            }
+          Cand g = b;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const Cand y{__shfl_xor_sync(0xffffffffu, g.v, o), __shfl_xor_sync(0xffffffffu, g.i, o)};
+            if (cand_before(y, g)) g = y;
+          }
+          if (b.i == g.i && b.v == g.v) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (k == kb) c[k] = Cand{-INFINITY, 0x7fffffff};   // the winner leaves its lane
+          }
+          if (lane == 0) {
+            const int x = min(max(g.i, 0), V - 1);
+            const float lq = (g.v - M) * (a.l2s * 0.6931471805599453f) - logf(s_S);
+            a.tokens[static_cast<size_t>(f) * W + j] = x;
+            a.scores[static_cast<size_t>(f) * W + j] = __ldg(a.parent_scores + f) + lq;
+            a.ties[static_cast<size_t>(f) * W + j] = ok ? 0 : -1;
+          }
+        }
+      }
     }
   } else {
-    // ---- inverse CDF: contiguous chunks, exclusive scan of chunk sums
-    const int C = (V + kExThreads - 1) / kExThreads;
-    const int c0 = min(V, tid * C), c1 = min(V, c0 + C);
+    // ---- inverse CDF: contiguous chunks of the slice, exclusive scan of chunk sums
+    const int len = v1 - v0;
+    const int C = (len + kExThreads - 1) / kExThreads;
+    const int c0 = v0 + min(len, tid * C), c1 = v0 + min(len, tid * C + C);
     float cs = 0.f;
     for (int x = c0; x < c1; ++x) cs += fast_exp2((__ldg(row + x) - M) * a.l2s);
     float inc = cs;
@@ -192,19 +284,30 @@ tree_expand_kernel(const ExpandArgs a) {
         if (lane >= o) x += y;
       }
       if (lane < kExWarps) s_scan[lane] = x - v;   // exclusive prefix of the warps
-      if (lane == kExWarps - 1) s_S = x;           // the total the draws are scaled to
+      const float T = __shfl_sync(0xffffffffu, x, kExWarps - 1);   // the slice's total
+      if (lane < CS) st_async_f32(peer_addr(&x_tot[rank], lane), T, peer_addr(&xbar[1], lane));
     }
     __syncthreads();
-    const float S = s_S;
-    const float prefix = s_scan[w] + inc - cs;
-    s_pre[tid] = prefix;
+    const float pre = s_scan[w] + inc - cs;
+    s_pre[tid] = pre;
+    if (!mbar_wait(&xbar[1], 0)) ok = false;
+    // the slices' offsets and the row's total, added in rank order
+    float P = 0.f, S = 0.f;
+    for (int q = 0; q < CS; ++q) {
+      if (q == rank) P = S;
+      S += x_tot[q];
+    }
+    const float T = x_tot[rank];
     __syncthreads();
-    // chunk t owns [prefix_t, prefix_{t+1}): an exact partition of [0, S)
-    const float end = tid + 1 < kExThreads ? s_pre[tid + 1] : S;
+    if (tid == 0) s_S = S;
+    // chunk t owns [P + pre_t, P + pre_{t+1}), the last one up to P + T
+    const float begin = P + pre;
+    const float end = P + (tid + 1 < kExThreads ? s_pre[tid + 1] : T);
     for (int j = 0; j < W; ++j) {
       const float target = s_u[j] * S;
-      if (prefix <= target && target < end) {
-        float run = prefix;
+      const bool last_chunk = rank == CS - 1 && tid == kExThreads - 1;
+      if (begin <= target && (target < end || (last_chunk && target >= end))) {
+        float run = begin;
         int pick = -1;
         float cb0 = target, cb1 = target;
         for (int x = c0; x < c1 && pick < 0; ++x) {
@@ -219,6 +322,7 @@ tree_expand_kernel(const ExpandArgs a) {
         if (pick < 0) {  // rounding: the chunk's last entry of positive weight, on the boundary
           for (int x = c1 - 1; x >= c0 && pick < 0; --x)
             if (fast_exp2((__ldg(row + x) - M) * a.l2s) > 0.f) pick = x;
+          if (pick < 0) pick = max(c0, min(V - 1, c1 - 1));
           cb0 = cb1 = target;
         }
         s_tok[j] = pick;
@@ -227,24 +331,13 @@ tree_expand_kernel(const ExpandArgs a) {
       }
     }
     __syncthreads();
-    if (tid < W && !s_claim[tid]) {
-      // rounding left the target past the last chunk: the row's last entry of
-      // positive weight, on the boundary
-      int pick = V - 1;
-      for (int x = V - 1; x >= 0; --x)
-        if (fast_exp2((__ldg(row + x) - M) * a.l2s) > 0.f) { pick = x; break; }
-      s_tok[tid] = pick;
-      s_tie[tid] = 1;
+    if (tid < W && s_claim[tid]) {
+      const int x = min(max(s_tok[tid], 0), V - 1);   // in range for any row contents
+      const float lq = (__ldg(row + x) - M) * (a.l2s * 0.6931471805599453f) - logf(S);
+      a.tokens[static_cast<size_t>(f) * W + tid] = x;
+      a.scores[static_cast<size_t>(f) * W + tid] = __ldg(a.parent_scores + f) + lq;
+      a.ties[static_cast<size_t>(f) * W + tid] = ok ? s_tie[tid] : -1;
     }
-    __syncthreads();
-  }
-  if (tid < W) {
-    const int x = min(max(s_tok[tid], 0), V - 1);   // in range for any row contents
-    const float S = s_S;
-    const float lq = (__ldg(row + x) - M) * (a.l2s * 0.6931471805599453f) - logf(S);
-    a.tokens[static_cast<size_t>(f) * W + tid] = x;
-    a.scores[static_cast<size_t>(f) * W + tid] = __ldg(a.parent_scores + f) + lq;
-    a.ties[static_cast<size_t>(f) * W + tid] = s_tie[tid];
   }
 }
 
@@ -354,14 +447,19 @@ extern "C" int spec_tree_expand(const float *draft_logits, const float *parent_s
   args.tokens = child_tokens;
   args.scores = child_scores;
   args.ties = near_ties;
+  const int CS = std::min(kExMaxCS, (V + kExSlice - 1) / kExSlice);   // CTAs per row
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(F), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(F) * CS, 1, 1);
   cfg.blockDim = dim3(kExThreads, 1, 1);
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  pdl_attribute(attr[0]);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  pdl_attribute(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, tree_expand_kernel, args) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
