@@ -56,7 +56,9 @@ struct NodeScalars {
 // of the order of the atomic adds, and the rounding of a whole row stays
 // below V * 2^-41 of its mass.
 struct TopPSmem {
-  unsigned long long warp_hist[kRWarps][2][256];   // per warp: [row (p, q)][8-bit digit]
+  // per warp: [row (p, q)][high, low 20 bits of the mass][8-bit digit]; a
+  // warp adds at most 1024 entries of a row, so each half stays below 2^30
+  uint32_t warp_hist[kRWarps][2][2][256];
   unsigned long long cta[2][2][256];               // the CTA's histogram, by pass parity
   unsigned long long recv[2][kMaxCS][2][256];      // every CTA's histogram, by pass parity
   unsigned long long hsum[2][256];                 // the group's histogram
@@ -73,15 +75,23 @@ constexpr int kTauUlps = 128;
 __device__ __forceinline__ unsigned long long fixed_mass(float v) {
   return __float2ull_rn(v * kFixedScale);
 }
-// hist[bin] += fixed_mass(v), as one unit: the scaling, the conversion and
-// the shared-memory add stay together, so that an unrolled loop over a
-// thread's entries does not hold all their conversions in registers at once.
+// hist[bin] += fixed_mass(v), split into its bits 20 and up (at saddr) and
+// its low 20 bits (at saddr + 1 KB), two 32-bit shared-memory adds, as one
+// unit: the scaling, the conversion and the adds stay together, so that an
+// unrolled loop over a thread's entries does not hold all their conversions
+// in registers at once.
 __device__ __forceinline__ void hist_add(uint32_t saddr, float v) {
   asm volatile(
-      "{\n\t.reg .f32 s;\n\t.reg .u64 m;\n\t"
+      "{\n\t.reg .f32 s;\n\t.reg .u64 m;\n\t.reg .u32 hi, lo;\n\t"
       "mul.rn.f32 s, %1, 0f53800000;\n\t"   // v * 2^40 (exact)
       "cvt.rni.u64.f32 m, s;\n\t"
-      "red.shared.add.u64 [%0], m;\n\t}"
+      "shr.u64 m, m, 20;\n\t"
+      "cvt.u32.u64 hi, m;\n\t"
+      "cvt.rni.u64.f32 m, s;\n\t"
+      "cvt.u32.u64 lo, m;\n\t"
+      "and.b32 lo, lo, 1048575;\n\t"
+      "red.shared.add.u32 [%0], hi;\n\t"
+      "red.shared.add.u32 [%0+1024], lo;\n\t}"
       :
       : "r"(saddr), "f"(v)
       : "memory");
@@ -317,9 +327,9 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         const int par = pass & 1;
         const uint32_t hi_p = static_cast<uint32_t>(tp.state[0][0]) >> (shift + 8);
         const uint32_t hi_q = static_cast<uint32_t>(tp.state[1][0]) >> (shift + 8);
-        unsigned long long *wh = &tp.warp_hist[w_id][0][0];
+        uint32_t *wh = &tp.warp_hist[w_id][0][0][0];
         const uint32_t wh_addr = smem_addr(wh);
-        for (int i = lane; i < 512; i += 32) wh[i] = 0ull;
+        for (int i = lane; i < 1024; i += 32) wh[i] = 0u;
         __syncwarp();
 #pragma unroll
         for (int m = 0; m < kRVec; ++m) {
@@ -328,7 +338,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
             const float v = pick4(xp[m], cc);
             const uint32_t bits = __float_as_uint(v);
             if (bits != 0u && (pass == 0 || (bits >> (shift + 8)) == hi_p))
-              hist_add(wh_addr + 8u * ((bits >> shift) & 255u), v);
+              hist_add(wh_addr + 4u * ((bits >> shift) & 255u), v);
           }
         }
         if (need_draft) {
@@ -339,7 +349,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
               const float v = pick4(xq[m], cc);
               const uint32_t bits = __float_as_uint(v);
               if (bits != 0u && (pass == 0 || (bits >> (shift + 8)) == hi_q))
-                hist_add(wh_addr + 8u * (256u + ((bits >> shift) & 255u)), v);
+                hist_add(wh_addr + 2048u + 4u * ((bits >> shift) & 255u), v);
             }
           }
         }
@@ -348,7 +358,9 @@ tree_verify_reg_kernel(const VerifyArgs a) {
           const int row = tid >> 8, bin = tid & 255;   // 512 threads: 2 rows x 256 digits
           unsigned long long h = 0ull;
 #pragma unroll
-          for (int ww = 0; ww < kRWarps; ++ww) h += tp.warp_hist[ww][row][bin];
+          for (int ww = 0; ww < kRWarps; ++ww)
+            h += (static_cast<unsigned long long>(tp.warp_hist[ww][row][0][bin]) << 20) +
+                 tp.warp_hist[ww][row][1][bin];
           tp.cta[par][row][bin] = h;
         }
         fence_proxy_async_smem();
