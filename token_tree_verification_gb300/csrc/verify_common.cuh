@@ -18,7 +18,6 @@ constexpr int kVWarps = kVThreads / 32;
 constexpr int kMaxCS = 8;          // CTAs per cluster (portable limit)
 constexpr int kChunkTarget = 16384;  // vocabulary entries per CTA the cluster size aims at
 constexpr int kMaxChunk = 27648;   // floats per CTA per row (2 rows fit in 216 KB)
-constexpr int kGreedyThreads = 1024;  // greedy per-node kernel: threads per CTA
 constexpr int kTreeWindow = 2 * SPEC_MAX_TREE_NODES - 1;   // nodes t-127 .. t+127
 constexpr int kFlagAccept = 1;
 constexpr int kFlagTie = 2;

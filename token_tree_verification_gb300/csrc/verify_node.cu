@@ -4,21 +4,23 @@
 // 三阶段工作流程详解 (stage 1 drafts greedily); SpecInfer developer article
 // §2.1 (accept the longest verified prefix).
 //
-// 1024 threads stream the node's target row (the first batch of loads is
-// issued before the tree is read) and reduce its argmax, lowest index on
+// The CTA's threads stream the node's target row (the first batch of loads
+// is issued before the tree is read) and reduce its argmax, lowest index on
 // ties; the node's children are accepted iff their token equals it, and the
-// last CTA of a request walks it.
+// last CTA of a request walks it.  Up to one node per SM: 1024 threads, one
+// CTA per SM; more nodes: 256 threads, four CTAs per SM, so one CTA's fixed
+// costs (tree, reduction, arrival) overlap the others' row loads.
 #include "verify_common.cuh"
 
 namespace spec {
 
-constexpr int kGW = kGreedyThreads / 32;
-
 // ---------------------------------------------------------------- greedy
 constexpr int kGreedyPrefetch = 8;  // float4 loads per thread issued before the tree is read
 
-__global__ void __launch_bounds__(kGreedyThreads, 1)
+template <int kGreedyThreads>
+__global__ void __launch_bounds__(kGreedyThreads, 1024 / kGreedyThreads)
 tree_verify_greedy_node_kernel(const VerifyArgs a) {
+  constexpr int kGW = kGreedyThreads / 32;
   __shared__ TreeSmem ts;
   __shared__ float rv[kGW];
   __shared__ int ri[kGW];
@@ -84,16 +86,20 @@ tree_verify_greedy_node_kernel(const VerifyArgs a) {
 }
 
 int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool wide = args.T <= sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(args.T), 1, 1);
-  cfg.blockDim = dim3(kGreedyThreads, 1, 1);
+  cfg.blockDim = dim3(wide ? 1024 : 256, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   pdl_attribute(attr[0]);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tree_verify_greedy_node_kernel, args) == cudaSuccess ? SPEC_OK
-                                                                                      : SPEC_ERR_CUDA;
+  const cudaError_t e = wide ? cudaLaunchKernelEx(&cfg, tree_verify_greedy_node_kernel<1024>, args)
+                             : cudaLaunchKernelEx(&cfg, tree_verify_greedy_node_kernel<256>, args);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace spec
