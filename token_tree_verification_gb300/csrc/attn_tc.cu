@@ -21,8 +21,10 @@
 //               ancestor bits, share the row max, online softmax with a
 //               lazily moved reference max (the stored O is rescaled only
 //               when a row's max grows by more than 2^8), write P as bf16
-//               high and remainder parts to shared memory (P V then keeps
-//               about 16 significant bits of every weight).
+//               high and remainder parts (P V then keeps about 16
+//               significant bits of every weight): into TMEM for 128-row
+//               blocks, whose P V takes its A operand from TMEM, into shared
+//               memory for packed blocks.
 // Blocks of at most 64 rows (PACKED) load their Q rows twice (rows 0-63 and
 // 64-127 of the MMA), so TMEM lanes r and r + 64 both hold S row r: four
 // threads per row spread the softmax over all four SM sub-partitions, and
@@ -48,7 +50,10 @@ constexpr float kRescaleLog2 = 8.f;
 
 template <int D, bool PACKED>
 struct TcCfg {
-  static constexpr int kStages = PACKED ? 4 : 3;
+  // packed blocks keep P in shared memory (their remainder rows come from other
+  // threads' lanes); 128-row blocks write P into TMEM, which frees room for a
+  // deeper K/V ring
+  static constexpr int kStages = PACKED ? 4 : 5;
   static constexpr int kBoxes = D / 64;
   static constexpr int kLoadRows = PACKED ? kTcRows / 2 : kTcRows;  // rows one Q load brings
   static constexpr int kQLoadBytes = kLoadRows * 128;
@@ -58,11 +63,11 @@ struct TcCfg {
   static constexpr int kTileBytes = kKeyTile * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kPBytes = kTcRows * kKeyTile * 2;   // one 128-row bf16 P operand
-  static constexpr int kPParts = PACKED ? 1 : 2;           // separate high / remainder operands
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQBytes;
   static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-  static constexpr int kSmem = kOffP + 2 * kPParts * kPBytes + 1024;
+  static constexpr int kPSmem = PACKED ? 2 * kPBytes : 0;   // P in shared memory (packed)
+  static constexpr int kSmem = kOffP + kPSmem + 1024;
   // softmax warps: four threads (key quarters) per S row; packed blocks hold
   // 64 rows twice, so 8 warps cover them, 128-row blocks take 16
   static constexpr int kSoftmaxWarps = PACKED ? 8 : 16;
@@ -75,12 +80,14 @@ struct TcCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;                      // S buffers: 3 x 64 columns
   static constexpr uint32_t kColO = 256;                    // O: D columns
-  static_assert(!PACKED || kTcRows / 2 * D * 4 <= 2 * kPParts * kPBytes,
+  static constexpr uint32_t kColP = 384;                    // 128-row P: 2 x (32 high + 32 remainder)
+  static_assert(!PACKED || kTcRows / 2 * D * 4 <= kPSmem,
                 "packed remainder exchange fits the P buffers");
+  static_assert(PACKED || kColO + D <= kColP, "O and P columns are disjoint");
   static_assert(kTcRows * kStage * 4 <= kStages * kStageBytes, "output staging fits the K/V ring");
   // staged rows plus the receive slots of the split merge, in the ring and P buffers
   static_assert((2 * (PACKED ? kTcRows / 2 : kTcRows) + 8) * kStage * 4 <=
-                    kStages * kStageBytes + 2 * kPParts * kPBytes,
+                    kStages * kStageBytes + kPSmem,
                 "split-merge buffers fit");
   static_assert(kOffP == kOffKV + kStages * kStageBytes, "ring and P buffers are contiguous");
   static_assert(kSmem <= 227 * 1024 - 8192, "shared memory budget");
@@ -316,14 +323,25 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const int st = j % NS;
         tc::fence_after_sync();
         const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
-        const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPParts * C::kPBytes;
-#pragma unroll
-        for (int pp = 0; pp < C::kPParts; ++pp) {
+        if constexpr (PACKED) {
+          const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPBytes;
 #pragma unroll
           for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-            const uint64_t ad = tc::smem_desc_sw128(pb + pp * C::kPBytes + kk * 32, 16, 1024);
+            const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
             const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
-            tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | pp | kk) != 0);
+            tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | kk) != 0);
+          }
+        } else {
+          // A = P from TMEM: high part in columns [0, 32) of the buffer, the
+          // remainder in [32, 64); eight columns per 16 keys
+          const uint32_t pt = tmem + C::kColP + (j & 1) * kKeyTile;
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp) {
+#pragma unroll
+            for (int kk = 0; kk < kKeyTile / 16; ++kk) {
+              const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
+              tc::mma_bf16_ts(tmem + C::kColO, pt + pp * 32 + kk * 8, bd, idO, (j | pp | kk) != 0);
+            }
           }
         }
         tc::commit(&bar_o[j & 1]);
@@ -439,27 +457,46 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         // the P buffer of this parity is free once the P V of tile i-2 is done
         if (ok && i >= 2 && !mbar_wait(&bar_o[i & 1], ((i - 2) >> 1) & 1)) ok = false;
         __syncwarp();
-        uint8_t *pbuf = smem + C::kOffP + (i & 1) * C::kPParts * C::kPBytes;
-        uint8_t *prow_hi = pbuf + srow * 128;
-        uint8_t *prow_lo = PACKED ? pbuf + (srow + kTcRows / 2) * 128 : pbuf + C::kPBytes + srow * 128;
+        if constexpr (PACKED) {
+          uint8_t *pbuf = smem + C::kOffP + (i & 1) * C::kPBytes;
+          uint8_t *prow_hi = pbuf + srow * 128;
+          uint8_t *prow_lo = pbuf + (srow + kTcRows / 2) * 128;
 #pragma unroll
-        for (int cc = 0; cc < KP / 8; ++cc) {
-          uint32_t hi[4], lo[4];
+          for (int cc = 0; cc < KP / 8; ++cc) {
+            uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = s[cc * 8 + 2 * e], p1 = s[cc * 8 + 2 * e + 1];
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = s[cc * 8 + 2 * e], p1 = s[cc * 8 + 2 * e + 1];
+              const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+              const float2 hf = __bfloat1622float2(h);
+              hi[e] = bf16x2_bits(h);
+              lo[e] = bf16x2_bits(__floats2bfloat162_rn(p0 - hf.x, p1 - hf.y));
+            }
+            const int off = (((KP / 8) * part + cc) ^ (srow & 7)) << 4;   // (srow + 64) & 7 == srow & 7
+            *reinterpret_cast<uint4 *>(prow_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        } else {
+          // P into this thread's TMEM lane: its 16 keys are columns
+          // [8 part, 8 part + 8) of the high and of the remainder half
+          static_assert(PACKED || KP == 16, "128-row blocks: 16 keys per thread");
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float p0 = s[2 * e], p1 = s[2 * e + 1];
             const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
             const float2 hf = __bfloat1622float2(h);
             hi[e] = bf16x2_bits(h);
             lo[e] = bf16x2_bits(__floats2bfloat162_rn(p0 - hf.x, p1 - hf.y));
           }
-          const int off = (((KP / 8) * part + cc) ^ (srow & 7)) << 4;   // (srow + 64) & 7 == srow & 7
-          *reinterpret_cast<uint4 *>(prow_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4 *>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          const uint32_t pt = trow + C::kColP + (i & 1) * kKeyTile + 8 * part;
+          tc::st8(pt, hi);
+          tc::st8(pt + 32, lo);
+          tc::wait_st();
         }
         l_part += psum;
       }
-      fence_proxy_async_smem();
+      if (PACKED) fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p[i & 1]);
