@@ -305,32 +305,35 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       // P_j V_j goes once P_j has arrived.  Neither waits for the other: the
       // issuer polls both conditions and issues whichever is ready, so a
       // late K/V tile never holds back a ready P V.
+      // Descriptors: one base per operand kind, the start address (bits
+      // [0, 14), in 16-byte units) advanced by adding the offset; every
+      // shared-memory address stays below 256 KB, so the field never carries.
+      const uint64_t qd0 = tc::smem_desc_sw128(sb + C::kOffQ, 16, 1024);
+      const uint64_t kd0 = tc::smem_desc_sw128(sb + C::kOffKV, 16, 1024);
+      const uint64_t vd0 = tc::smem_desc_sw128(sb + C::kOffKV + C::kTileBytes, C::kKVBoxBytes, 1024);
       auto issue_s = [&](int i) {
         const int st = i % NS;
         tc::fence_after_sync();
-        const uint32_t kb = sb + C::kOffKV + st * C::kStageBytes;
+        const uint64_t kd = kd0 + static_cast<uint64_t>((st * C::kStageBytes) >> 4);
+        const uint32_t sc = tmem + C::kColS + (i % C::kSBufs) * kKeyTile;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t ad = tc::smem_desc_sw128(
-              sb + C::kOffQ + (ks >> 2) * C::kQChunkBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd =
-              tc::smem_desc_sw128(kb + (ks >> 2) * C::kKVBoxBytes + (ks & 3) * 32, 16, 1024);
-          tc::mma_bf16(tmem + C::kColS + (i % C::kSBufs) * kKeyTile, ad, bd, idS, ks > 0);
+          const uint32_t off = ((ks >> 2) * C::kQChunkBytes + (ks & 3) * 32) >> 4;
+          const uint32_t koff = ((ks >> 2) * C::kKVBoxBytes + (ks & 3) * 32) >> 4;
+          tc::mma_bf16(sc, qd0 + off, kd + koff, idS, ks > 0);
         }
         tc::commit(&bar_s[i % C::kSBufs]);
       };
       auto issue_pv = [&](int j) {
         const int st = j % NS;
         tc::fence_after_sync();
-        const uint32_t vb = sb + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
+        const uint64_t vd = vd0 + static_cast<uint64_t>((st * C::kStageBytes) >> 4);
         if constexpr (PACKED) {
-          const uint32_t pb = sb + C::kOffP + (j & 1) * C::kPBytes;
+          const uint64_t pd =
+              tc::smem_desc_sw128(sb + C::kOffP, 16, 1024) + static_cast<uint64_t>(((j & 1) * C::kPBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-            const uint64_t ad = tc::smem_desc_sw128(pb + kk * 32, 16, 1024);
-            const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
-            tc::mma_bf16(tmem + C::kColO, ad, bd, idO, (j | kk) != 0);
-          }
+          for (int kk = 0; kk < kKeyTile / 16; ++kk)
+            tc::mma_bf16(tmem + C::kColO, pd + (kk * 32 >> 4), vd + (kk * 16 * 128 >> 4), idO, (j | kk) != 0);
         } else {
           // A = P from TMEM: high part in columns [0, 32) of the buffer, the
           // remainder in [32, 64); eight columns per 16 keys
@@ -338,10 +341,9 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
 #pragma unroll
           for (int pp = 0; pp < 2; ++pp) {
 #pragma unroll
-            for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-              const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, C::kKVBoxBytes, 1024);
-              tc::mma_bf16_ts(tmem + C::kColO, pt + pp * 32 + kk * 8, bd, idO, (j | pp | kk) != 0);
-            }
+            for (int kk = 0; kk < kKeyTile / 16; ++kk)
+              tc::mma_bf16_ts(tmem + C::kColO, pt + pp * 32 + kk * 8, vd + (kk * 16 * 128 >> 4), idO,
+                              (j | pp | kk) != 0);
           }
         }
         tc::commit(&bar_o[j & 1]);
