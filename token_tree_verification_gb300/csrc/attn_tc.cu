@@ -10,12 +10,14 @@
 // heads of the KV head.  Warp roles:
 //   warp 0      TMA producer: the Q block once, then 64-key K and V tiles
 //               (128-byte swizzle) into a ring of stages.
-//   warp 1      allocates TMEM; one thread issues the MMAs:
-//                 S_i = Q K_i^T            M=128, N=64, K=D   (TMEM S[i%2])
-//                 O  += P_i V_i            M=128, N=D,  K=64  (TMEM O)
-//               with S_{i+1} issued before P_i is ready, so the softmax of
-//               one tile overlaps the QK^T of the next.
-//   warps 2+    four threads per TMEM lane (= query row), one per quarter of
+//   warp 1      allocates TMEM; one thread issues S_i = Q K_i^T
+//               (M=128, N=64, K=D, into TMEM S[i%3]) as soon as K_i has
+//               landed and S[i%3] is free, so the softmax of one tile
+//               overlaps the QK^T of the next ones.
+//   warp 2      one thread issues O += P_i V_i (M=128, N=D, K=64, TMEM O)
+//               as soon as P_i is written: two issuing threads, so neither
+//               kind of MMA waits behind the other's issue.
+//   warps 3+    four threads per TMEM lane (= query row), one per quarter of
 //               the tile's keys (16 softmax warps for 128-row blocks, 8 for
 //               packed blocks): read S from TMEM, mask with the node's
 //               ancestor bits, share the row max, online softmax with a
@@ -71,7 +73,7 @@ struct TcCfg {
   // softmax warps: four threads (key quarters) per S row; packed blocks hold
   // 64 rows twice, so 8 warps cover them, 128-row blocks take 16
   static constexpr int kSoftmaxWarps = PACKED ? 8 : 16;
-  static constexpr int kThreads = 32 * (2 + kSoftmaxWarps);
+  static constexpr int kThreads = 32 * (3 + kSoftmaxWarps);   // TMA, S issuer, P V issuer, softmax
   static constexpr int kParts = 4;                          // threads per row (key parts)
   static constexpr int kKeysPer = kKeyTile / kParts;        // keys per thread per tile
   static constexpr int kOCols = PACKED ? D / 2 : D / 4;     // O columns one thread reads out
@@ -159,6 +161,15 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float alpha) {
   tc::wait_st();
 }
 
+__device__ __forceinline__ int ld_volatile_shared(const int *p) {
+  int v;
+  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_volatile_shared(int *p, int v) {
+  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
@@ -179,6 +190,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   __shared__ float x_l[C::kParts][kTcRows];
   __shared__ __align__(8) uint64_t bar_m;          // key splits: the peers' rows have arrived
   __shared__ int s_timeout;
+  __shared__ int s_pv_issued;                        // P V products issued so far (warp 2)
 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -206,6 +218,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     fence_barrier_init();
     s_timeout = 0;
+    s_pv_issued = 0;
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmq);
@@ -250,13 +263,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   // (key quarters) per row, lanes 64-127 accumulate the remainder part of
   // P V, and each thread reads out half of its lane's O.
   const int quad = warp & 3;
-  const int half = (warp - 2) >> 2;                  // packed: 0..1; otherwise 0..3
+  const int half = (warp - 3) >> 2;                  // packed: 0..1; otherwise 0..3
   const int part = PACKED ? ((quad >> 1) * 2 + half) : half;
   const int srow = PACKED ? ((quad & 1) * 32 + lane) : (quad * 32 + lane);
   const bool row_ok = srow < rows_here;
-  const bool lanes_live = warp >= 2 && (PACKED ? (quad & 1) : quad) * 32 < rows_here;
+  const bool lanes_live = warp >= 3 && (PACKED ? (quad & 1) : quad) * 32 < rows_here;
   const bool lo_lane = PACKED && quad >= 2;          // holds the remainder part of P V
-  const bool owner = warp >= 2 && !lo_lane;          // assembles the row's final O
+  const bool owner = warp >= 3 && !lo_lane;          // assembles the row's final O
   const int ocol = PACKED ? half * (D / 2) : part * (D / 4);   // this thread's O columns
   const bool tail_writer = PACKED ? half == 0 : part == 0;
   constexpr int kOC = C::kOCols;
@@ -293,13 +306,14 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1 issues S_i = Q K_i^T, warp 2 issues O += P_j V_j: two
+    // instruction streams, so neither kind waits behind the other's issue.
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kKeyTile, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
-      bool ok = mbar_wait(&bar_q, 0);
-      tc::fence_after_sync();
+      bool ok = true;
       // S_i goes into TMEM buffer i % 3 once tile i's K/V has landed and
       // the softmax has read S_{i-3} (its P_{i-3} arrived: PV_{i-3} issued);
       // P_j V_j goes once P_j has arrived.  Neither waits for the other: the
@@ -349,26 +363,32 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         tc::commit(&bar_o[j & 1]);
         tc::commit(&bar_empty[st]);
       };
-      int next_s = 0, next_pv = 0;
-      uint64_t t_idle = 0;
-      uint32_t idle = 0;
-      while (ok && next_pv < ntiles) {
-        bool issued = false;
-        if (next_s < ntiles && next_s < next_pv + C::kSBufs &&
-            mbar_poll(&bar_full[next_s % NS], (next_s / NS) & 1)) {
-          issue_s(next_s++);
-          issued = true;
+      if (warp == 1) {
+        // S_i goes into TMEM buffer i % 3 once tile i's K/V has landed and the
+        // softmax has read S_{i-3}: P V of tile i - 3 has been issued (its P
+        // arrived), which warp 2 publishes in s_pv_issued.
+        ok = ok && mbar_wait(&bar_q, 0);
+        for (int i = 0; ok && i < ntiles; ++i) {
+          if (i >= C::kSBufs) {
+            const uint64_t t0 = global_ns();
+            for (uint32_t it = 1; ld_volatile_shared(&s_pv_issued) < i - C::kSBufs + 1; ++it)
+              if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+              }
+          }
+          if (ok && !mbar_wait(&bar_full[i % NS], (i / NS) & 1)) ok = false;
+          if (ok) issue_s(i);
         }
-        if (next_pv < next_s && mbar_poll(&bar_p[next_pv & 1], (next_pv >> 1) & 1)) {
-          issue_pv(next_pv++);
-          issued = true;
-        }
-        if (issued) {
-          idle = 0;
-        } else if (idle++ == 0) {
-          t_idle = global_ns();
-        } else if ((idle & 255u) == 0 && global_ns() - t_idle > kWaitLimitNs) {
-          ok = false;  // bounded: no progress for the wait limit
+      } else {
+        // P_j V_j goes once P_j has arrived (its K/V landed before S_j)
+        for (int j = 0; ok && j < ntiles; ++j) {
+          if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          issue_pv(j);
+          st_volatile_shared(&s_pv_issued, j + 1);
         }
       }
       if (!ok) s_timeout = 1;
@@ -393,7 +413,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         const int valid = R.keys - key0;
         const int chunks = (kKeyTile - valid) * C::kBoxes * 8;
         uint8_t *vrow = smem + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
-        for (int c = tid - 64; c < chunks; c += 32 * C::kSoftmaxWarps) {
+        for (int c = tid - 96; c < chunks; c += 32 * C::kSoftmaxWarps) {
           const int row = valid + c / (C::kBoxes * 8);
           const int rest = c % (C::kBoxes * 8);
           *reinterpret_cast<uint4 *>(vrow + (rest >> 3) * C::kKVBoxBytes + row * 128 +
@@ -526,7 +546,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       for (int e = 0; e < kOC; e += 4)
         *xo_at(e) = make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
     }
-    if (warp >= 2) x_l[part][srow] = l_part;
+    if (warp >= 3) x_l[part][srow] = l_part;
     named_bar_sync(2, 32 * C::kSoftmaxWarps);
     if (owner && row_ok) {
 #pragma unroll
