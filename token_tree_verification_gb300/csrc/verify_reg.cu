@@ -126,6 +126,13 @@ __device__ __forceinline__ float resid(float p, float q, float c) {
   return c != 0.f ? fmaxf(0.f, fmaf(-c, q, p)) : p;
 }
 
+// The same for c > 0 (every rejection round): max(0, p - c q) without the
+// c == 0 case.
+__device__ __forceinline__ float sum4_resid_pos(float4 p, float4 q, float c) {
+  return (fmaxf(0.f, fmaf(-c, q.x, p.x)) + fmaxf(0.f, fmaf(-c, q.y, p.y))) +
+         (fmaxf(0.f, fmaf(-c, q.z, p.z)) + fmaxf(0.f, fmaf(-c, q.w, p.w)));
+}
+
 __device__ __forceinline__ float sum4_resid(float4 p, float4 q, float c) {
   return (resid(p.x, q.x, c) + resid(p.y, q.y, c)) + (resid(p.z, q.z, c) + resid(p.w, q.w, c));
 }
@@ -545,7 +552,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       const float c_new = c_prev + W_prev;
       float wsum = 0.f;
 #pragma unroll
-      for (int m = 0; m < kRVec; ++m) wsum += sum4_resid(xp[m], xq[m], c_new);
+      for (int m = 0; m < kRVec; ++m) wsum += sum4_resid_pos(xp[m], xq[m], c_new);   // c_new > 0
       wsum = warp_sum(wsum);
       const int p = rounds & 1;
       if (tid == 0) mbar_arrive_expect_tx(&xbar[1 + p], static_cast<uint32_t>(CS * kRWarps * 4));
