@@ -126,11 +126,40 @@ __device__ __forceinline__ float resid(float p, float q, float c) {
   return c != 0.f ? fmaxf(0.f, fmaf(-c, q, p)) : p;
 }
 
-// The same for c > 0 (every rejection round): max(0, p - c q) without the
-// c == 0 case.
-__device__ __forceinline__ float sum4_resid_pos(float4 p, float4 q, float c) {
-  return (fmaxf(0.f, fmaf(-c, q.x, p.x)) + fmaxf(0.f, fmaf(-c, q.y, p.y))) +
-         (fmaxf(0.f, fmaf(-c, q.z, p.z)) + fmaxf(0.f, fmaf(-c, q.w, p.w)));
+// The residual weight of a thread's entries for c > 0 (every rejection
+// round): the sum of max(0, p - c q) without the c == 0 case, with paired
+// fp32 FMAs and a paired accumulator (two partial sums, added at the end).
+__device__ __forceinline__ float resid_sum_pos(const float4 (&p)[kRVec], const float4 (&q)[kRVec],
+                                               float c) {
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int m = 0; m < kRVec; ++m) {
+    asm("{\n\t.reg .b64 nc, q01, q23, p01, p23, r01, r23, acc;\n\t"
+        ".reg .f32 r0, r1, r2, r3;\n\t"
+        "mov.b64 nc, {%2, %2};\n\t"
+        "mov.b64 q01, {%3, %4};\n\t"
+        "mov.b64 q23, {%5, %6};\n\t"
+        "mov.b64 p01, {%7, %8};\n\t"
+        "mov.b64 p23, {%9, %10};\n\t"
+        "fma.rn.f32x2 r01, nc, q01, p01;\n\t"
+        "fma.rn.f32x2 r23, nc, q23, p23;\n\t"
+        "mov.b64 {r0, r1}, r01;\n\t"
+        "mov.b64 {r2, r3}, r23;\n\t"
+        "max.f32 r0, r0, 0f00000000;\n\t"
+        "max.f32 r1, r1, 0f00000000;\n\t"
+        "max.f32 r2, r2, 0f00000000;\n\t"
+        "max.f32 r3, r3, 0f00000000;\n\t"
+        "mov.b64 r01, {r0, r1};\n\t"
+        "mov.b64 r23, {r2, r3};\n\t"
+        "mov.b64 acc, {%0, %1};\n\t"
+        "add.rn.f32x2 acc, acc, r01;\n\t"
+        "add.rn.f32x2 acc, acc, r23;\n\t"
+        "mov.b64 {%0, %1}, acc;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(-c), "f"(q[m].x), "f"(q[m].y), "f"(q[m].z), "f"(q[m].w), "f"(p[m].x), "f"(p[m].y),
+          "f"(p[m].z), "f"(p[m].w));
+  }
+  return a0 + a1;
 }
 
 __device__ __forceinline__ float sum4_resid(float4 p, float4 q, float c) {
@@ -550,9 +579,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       if (frozen) continue;
       // rejected: r becomes max(0, p - c q) / W(c) with c = c_prev + W_prev
       const float c_new = c_prev + W_prev;
-      float wsum = 0.f;
-#pragma unroll
-      for (int m = 0; m < kRVec; ++m) wsum += sum4_resid_pos(xp[m], xq[m], c_new);   // c_new > 0
+      float wsum = resid_sum_pos(xp, xq, c_new);   // c_new > 0
       wsum = warp_sum(wsum);
       const int p = rounds & 1;
       if (tid == 0) mbar_arrive_expect_tx(&xbar[1 + p], static_cast<uint32_t>(CS * kRWarps * 4));
