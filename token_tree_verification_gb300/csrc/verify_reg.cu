@@ -268,23 +268,20 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   float c_prev = 0.f, Ml = 0.f, Sp = 1.f;
   const float l2s = a.inv_temp * 1.4426950408889634f;  // exp(x / T) = 2^(x * l2s)
   if (!c.err) {
-    // ---- V1: the warp's maxima, exponentials in place, the warp's sums
-    float ml = -INFINITY, md = -INFINITY;
-#pragma unroll
-    for (int m = 0; m < kRVec; ++m) {
-      ml = fmaxf(ml, max4(xp[m]));
-      md = fmaxf(md, max4(xq[m]));
-    }
-    ml = warp_max(ml);
-    md = need_draft ? warp_max(md) : -INFINITY;
-    const float nl = ml == -INFINITY ? 0.f : -ml * l2s;
-    const float nd = md == -INFINITY ? 0.f : -md * l2s;
-    float sl = 0.f, sd = 0.f;
+    // ---- V1: the warp's maxima, exponentials in place, the warp's sums.
+    //      The target row first: the draft row was requested later, so its
+    //      loads are still in flight while the target's work runs.
     // half of the exponentials on the MUFU pipe, half on the FMA pipe
     auto expo = [&](float v, float nb, int m) -> float {
       const float z = fmaf(v, l2s, nb);
       return m < kRVec / 2 ? fast_exp2(z) : exp2_taylor(z);
     };
+    float ml = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < kRVec; ++m) ml = fmaxf(ml, max4(xp[m]));
+    ml = warp_max(ml);
+    const float nl = ml == -INFINITY ? 0.f : -ml * l2s;
+    float sl = 0.f;
 #pragma unroll
     for (int m = 0; m < kRVec; ++m) {
       xp[m].x = expo(xp[m].x, nl, m);
@@ -292,7 +289,16 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       xp[m].z = expo(xp[m].z, nl, m);
       xp[m].w = expo(xp[m].w, nl, m);
       sl += (xp[m].x + xp[m].y) + (xp[m].z + xp[m].w);
-      if (need_draft) {
+    }
+    float md = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < kRVec; ++m) md = fmaxf(md, max4(xq[m]));
+    md = need_draft ? warp_max(md) : -INFINITY;
+    const float nd = md == -INFINITY ? 0.f : -md * l2s;
+    float sd = 0.f;
+    if (need_draft) {
+#pragma unroll
+      for (int m = 0; m < kRVec; ++m) {
         xq[m].x = expo(xq[m].x, nd, m);
         xq[m].y = expo(xq[m].y, nd, m);
         xq[m].z = expo(xq[m].z, nd, m);
