@@ -90,10 +90,12 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// the warp's maximum (a NaN lane is ignored, as fmaxf does), one reduction
+// instruction
 __device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 
