@@ -121,13 +121,19 @@ tree_expand_kernel(const ExpandArgs a) {
   Cand best[kMaxWidth];
 #pragma unroll
   for (int j = 0; j < kMaxWidth; ++j) best[j] = Cand{-INFINITY, 0x7fffffff};
+  // greedy: strided over the slice; sampled: over this thread's contiguous
+  // chunk of the slice, whose (max, sum) then also gives the chunk's mass
+  const int len = v1 - v0;
+  const int C = (len + kExThreads - 1) / kExThreads;
+  const int c0 = v0 + min(len, tid * C), c1 = v0 + min(len, tid * C + C);
+  const int xs = greedy ? v0 + tid : c0, xe = greedy ? v1 : c1, xd = greedy ? kExThreads : 1;
   float m = -INFINITY, s = 0.f;
-  for (int x = v0 + tid; x < v1; x += kExThreads) {
+  for (int x = xs; x < xe; x += xd) {
     const float v = __ldg(row + x);
     if (v > m) {
       s = (m == -INFINITY ? 0.f : s * fast_exp2((m - v) * a.l2s)) + 1.f;
       m = v;
-    } else {
+    } else if (m != -INFINITY) {   // a -inf logit before any finite one adds nothing
       s += fast_exp2((v - m) * a.l2s);
     }
     if (greedy) {
@@ -254,12 +260,9 @@ tree_expand_kernel(const ExpandArgs a) {
       }
     }
   } else {
-    // ---- inverse CDF: contiguous chunks of the slice, exclusive scan of chunk sums
-    const int len = v1 - v0;
-    const int C = (len + kExThreads - 1) / kExThreads;
-    const int c0 = v0 + min(len, tid * C), c1 = v0 + min(len, tid * C + C);
-    float cs = 0.f;
-    for (int x = c0; x < c1; ++x) cs += fast_exp2((__ldg(row + x) - M) * a.l2s);
+    // ---- inverse CDF: contiguous chunks of the slice, exclusive scan of chunk
+    //      sums (a chunk's sum from its own (max, sum) of pass A)
+    const float cs = s > 0.f ? s * fast_exp2((m - M) * a.l2s) : 0.f;
     float inc = cs;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
