@@ -256,7 +256,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   const int t0 = split * per;
   const int ntiles = max(0, min(t0 + per, tiles_total) - t0);
 
-  // softmax-thread geometry (warps 2 and up).  TMEM lane r = 32 * quad +
+  // softmax-thread geometry (warps 3 and up).  TMEM lane r = 32 * quad +
   // lane.  128-row blocks: row r, four threads (key quarters) per row, each
   // reading out a quarter of the row's O.  Packed blocks: the Q block is
   // loaded twice, so lanes r and r + 64 hold the same S row; four threads
@@ -314,11 +314,6 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kKeyTile, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
       bool ok = true;
-      // S_i goes into TMEM buffer i % 3 once tile i's K/V has landed and
-      // the softmax has read S_{i-3} (its P_{i-3} arrived: PV_{i-3} issued);
-      // P_j V_j goes once P_j has arrived.  Neither waits for the other: the
-      // issuer polls both conditions and issues whichever is ready, so a
-      // late K/V tile never holds back a ready P V.
       // Descriptors: one base per operand kind, the start address (bits
       // [0, 14), in 16-byte units) advanced by adding the offset; every
       // shared-memory address stays below 256 KB, so the field never carries.
