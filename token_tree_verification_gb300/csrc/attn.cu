@@ -517,32 +517,33 @@ bool use_mma_kernel() {
 // SMs of the current device; 152 (GB300) when no device can be queried, so a
 // host-only caller still gets the workspace size the GPU will ask for.
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      n = 152;
+  static std::atomic<int> n[spec::kMaxDevices];
+  const int dev = spec::current_device();
+  if (dev < 0) return 152;
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return 152;
+    n[dev].store(v, std::memory_order_relaxed);
   }
-  return n;
+  return v;
 }
 
 template <int D>
 int launch_mma(const spec::AttnArgs &args, int max_prefix, int T, cudaStream_t stream) {
   using C = spec::MmaCfg<D>;
   auto kernel = spec::tree_attn_mma_kernel<D>;
-  static int configured = 0;
-  static int per_sm = 1;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-        cudaSuccess)
-      return SPEC_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, spec::kMmaThreads,
-                                                      C::kSmem) != cudaSuccess || per_sm < 1)
+  static std::atomic<size_t> granted[spec::kMaxDevices];
+  if (!spec::allow_dynamic_smem(kernel, C::kSmem, granted)) return SPEC_ERR_CUDA;
+  static std::atomic<int> occupancy[spec::kMaxDevices];   // resident CTAs per SM, per device
+  const int dev = spec::current_device();
+  int per_sm = dev >= 0 ? occupancy[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, spec::kMmaThreads, C::kSmem) !=
+            cudaSuccess ||
+        per_sm < 1)
       per_sm = 1;
-    configured = 1;
+    if (dev >= 0) occupancy[dev].store(per_sm, std::memory_order_relaxed);
   }
   CUtensorMap tmk, tmv;
   if (!encode_kv_map(&tmk, args.k, args.B, args.Hkv, args.S_cap, D) ||

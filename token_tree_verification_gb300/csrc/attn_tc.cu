@@ -704,13 +704,8 @@ static int launch_tc(const AttnArgs &args, const CUtensorMap &tmq, const CUtenso
                      const CUtensorMap &tmv, int cs, int rowblocks, cudaStream_t stream) {
   using C = TcCfg<D, PACKED>;
   auto kernel = tree_attn_tc_kernel<D, PACKED>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-        cudaSuccess)
-      return SPEC_ERR_CUDA;
-    configured = true;
-  }
+  static std::atomic<size_t> granted[kMaxDevices];
+  if (!allow_dynamic_smem(kernel, C::kSmem, granted)) return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, rowblocks, static_cast<unsigned>(args.B * args.Hkv));
   cfg.blockDim = dim3(C::kThreads, 1, 1);

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/spec_tree.h"
 
 namespace spec {
@@ -36,6 +39,35 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 inline void pdl_attribute(cudaLaunchAttribute &attr) {
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
+}
+
+// ---------------------------------------------------------------- host state
+// What a launcher caches about the GPU (a kernel's shared-memory limit, the
+// SM count) belongs to one device, so it is kept per device ordinal.
+constexpr int kMaxDevices = 256;
+
+inline int current_device() {
+  int dev = 0;
+  return (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+// A kernel needs its dynamic shared-memory limit raised before a launch with
+// more than 48 KB, on each device it runs on.  `granted[dev]` holds the
+// largest limit set on device dev; the limit only ever grows, and changes
+// are serialised, so a concurrent launch never sees it lowered.
+template <typename Kernel>
+inline bool allow_dynamic_smem(Kernel kernel, size_t bytes, std::atomic<size_t> *granted) {
+  const int dev = current_device();
+  if (dev < 0) return false;
+  if (granted[dev].load(std::memory_order_acquire) >= bytes) return true;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (granted[dev].load(std::memory_order_relaxed) >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return false;
+  granted[dev].store(bytes, std::memory_order_release);
+  return true;
 }
 
 // First error for a request sticks; kernels never write SPEC_OK.

@@ -124,13 +124,8 @@ extern "C" int spec_kv_compact(void *k_cache, void *v_cache, int dtype, int B, i
   // room for every row an accepted path can move (acc <= max_depth_plus1 - 1)
   const size_t smem = static_cast<size_t>(2) * (max_depth_plus1 - 1) * D * es;
   if (smem > 200 * 1024) return SPEC_ERR_SHAPE;
-  static size_t configured = 48 * 1024;
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(kv_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    configured = smem;
-  }
+  static std::atomic<size_t> granted[kMaxDevices];
+  if (smem > 48 * 1024 && !allow_dynamic_smem(kv_compact_kernel, smem, granted)) return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(Hkv), static_cast<unsigned>(B), 1);
   cfg.blockDim = dim3(kKvThreads, 1, 1);

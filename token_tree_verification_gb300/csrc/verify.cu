@@ -437,13 +437,8 @@ int verify_entry(const float *target_logits, const float *draft_logits, const in
     return launch_verify_reg(args, (V + kRegChunk - 1) / kRegChunk, nucleus,
                              static_cast<cudaStream_t>(stream));
   const size_t smem = sizeof(float) * 2 * static_cast<size_t>(chunk);
-  static int configured_smem = -1;
-  if (configured_smem < static_cast<int>(smem)) {
-    if (cudaFuncSetAttribute(tree_verify_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    configured_smem = static_cast<int>(smem);
-  }
+  static std::atomic<size_t> granted[kMaxDevices];
+  if (!allow_dynamic_smem(tree_verify_cluster_kernel, smem, granted)) return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(T) * CS, 1, 1);
   cfg.blockDim = dim3(kVThreads, 1, 1);

@@ -780,13 +780,9 @@ int launch_verify_reg(const VerifyArgs &args, int cs, bool top_p, cudaStream_t s
   cfg.blockDim = dim3(kRThreads, 1, 1);
   cfg.dynamicSmemBytes = top_p ? sizeof(TopPSmem) : 0;
   if (top_p) {
-    static bool configured = false;
-    if (!configured) {
-      if (cudaFuncSetAttribute(tree_verify_reg_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(sizeof(TopPSmem))) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-      configured = true;
-    }
+    static std::atomic<size_t> granted[kMaxDevices];
+    if (!allow_dynamic_smem(tree_verify_reg_kernel<true>, sizeof(TopPSmem), granted))
+      return SPEC_ERR_CUDA;
   }
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
