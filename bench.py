@@ -582,35 +582,52 @@ def run_e2e(st, w, stream, steps):
     """Same metric through the public API with host buffers: every step copies
     all of its inputs (Q, K/V caches, target and draft logits, tree arrays)
     from pinned host memory and reads the verified tokens back.  The copies of
-    step i + 1 go on two copy streams (two copy engines) into the other of two
-    device input sets while step i's kernels run, as a serving loop would
-    overlap them; the timed region spans every copy and every step."""
+    step i + 1 go on two copy streams into the other of two device input sets
+    while step i's kernels run, as a serving loop would overlap them; the
+    timed region spans every copy and every step.  The four small tree arrays
+    travel as one packed buffer and the four outputs come back as one, since
+    every copy pays a fixed start-up cost on the host-device link."""
     import torch
     ttv = st.ttv
     names = [k for k, v in st.copies[0].items() if v is not None]
     host = {k: st.copies[0][k].cpu().pin_memory() for k in names}
-    tree_host = {"par": st.par.cpu().pin_memory(), "off": st.off.cpu().pin_memory(),
-                 "tok": st.tok.cpu().pin_memory(), "pl": st.pl.cpu().pin_memory()}
+    tree_parts = [("par", st.par), ("off", st.off), ("tok", st.tok), ("pl", st.pl)]
+    tree_host = torch.cat([v.cpu() for _, v in tree_parts]).pin_memory()
+
+    def tree_views(buf):
+        out, at = {}, 0
+        for k, v in tree_parts:
+            out[k] = buf[at:at + v.numel()]
+            at += v.numel()
+        return out
+
     sets = []
     for j in range(2):
         d = {k: st.copies[j][k] for k in names}
-        d.update({k: v.cuda().clone() for k, v in tree_host.items()})
+        d["tree"] = tree_host.cuda()
+        d.update(tree_views(d["tree"]))
         sets.append(d)
-    out_host = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in st.outs.items()}
-                for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in host.values()) + \
-        sum(v.numel() * v.element_size() for v in tree_host.values())
-    d2h = sum(v.numel() * v.element_size() for v in st.outs.values())
+    # the outputs as views of one device buffer, read back with one copy
+    shapes = [(k, tuple(v.shape)) for k, v in st.outs.items()]
+    n_out = sum(int(np.prod(sh)) for _, sh in shapes)
+    out_dev = torch.empty(n_out, dtype=torch.int32, device="cuda")
+    outs, at = {}, 0
+    for k, sh in shapes:
+        n = int(np.prod(sh))
+        outs[k] = out_dev[at:at + n].view(sh)
+        at += n
+    out_host = [torch.empty(n_out, dtype=torch.int32).pin_memory() for _ in range(2)]
+    src = dict(host, tree=tree_host)
+    h2d = sum(v.numel() * v.element_size() for v in src.values())
+    d2h = out_dev.numel() * out_dev.element_size()
     cs = [torch.cuda.Stream(), torch.cuda.Stream()]
     # inputs by size, each to the copy stream with fewer bytes so far
-    src = dict(host, **tree_host)
     order = sorted(src, key=lambda k: -src[k].nbytes)
     lanes, load = {}, [0, 0]
     for k in order:
         lane = 0 if load[0] <= load[1] else 1
         lanes[k] = lane
         load[lane] += src[k].nbytes
-    ready = [torch.cuda.Event() for _ in range(2)]
     free = [torch.cuda.Event() for _ in range(2)]
 
     def copy_in(i):
@@ -633,10 +650,9 @@ def run_e2e(st, w, stream, steps):
             ttv.tree_attn(d["q"], d["k"], d["v"], d["pl"], d["off"], st.mask, st.max_prefix,
                           st.status, o=st.o, workspace=st.ws_attn, stream=stream)
             ttv.tree_verify(d["tl"], d["dl"], d["tok"], d["par"], d["off"], w.temperature,
-                            st.seed + i, st.W, st.status, st.ws, outputs=st.outs, stream=stream)
+                            st.seed + i, st.W, st.status, st.ws, outputs=outs, stream=stream)
             free[i % 2].record(stream)
-            for k, v in st.outs.items():
-                out_host[i % 2][k].copy_(v, non_blocking=True)
+            out_host[i % 2].copy_(out_dev, non_blocking=True)
 
     def run_steps(n):
         for j in range(2):
@@ -657,9 +673,20 @@ def run_e2e(st, w, stream, steps):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    # the last step's tokens, as read back, equal the device path's for its seed
+    if (st.status.cpu().numpy() != 0).any():
+        raise RuntimeError(f"device status {st.status.cpu().tolist()}")
+    last = out_host[(steps - 1) % 2].clone()
+    with torch.cuda.stream(stream):
+        st.run(steps - 1)
+    torch.cuda.synchronize()
+    ref = torch.cat([v.reshape(-1).cpu() for v in st.outs.values()])
+    if not torch.equal(last, ref):
+        raise RuntimeError("end-to-end outputs differ from the device path")
     return {"value": w.T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipeline": "two copy streams into double-buffered inputs, overlapping the previous step"}
+            "pipeline": ("two copy streams into double-buffered inputs, overlapping the previous step; "
+                         "tree arrays packed into one copy, outputs read back in one")}
 
 
 # --------------------------------------------------------------------------
