@@ -513,7 +513,10 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
         }
         l_part += psum;
       }
-      if (PACKED) fence_proxy_async_smem();
+      // P (packed blocks) and the zeroed V rows of a tail tile are generic
+      // shared-memory stores that the P V product reads through the async
+      // proxy: order them before the arrival that releases the issuer.
+      if (PACKED || key0 + kKeyTile > R.keys) fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p[i & 1]);
