@@ -83,12 +83,17 @@ def test_large_configs_sampled(gpu_lib, kernel, name):
     assert_attn_close(got.reshape(-1, w.D)[rows], ref, name)
 
 
-def test_nan_padding_never_leaks(gpu_lib, kernel):
-    w = synthetic.make_workload("llama7b", seed=3, L=100, N=10, width=3, depth=2, Hq=4, Hkv=4, V=64,
-                                S_cap=256, pad=float("nan"))
+@pytest.mark.parametrize("Hq,Hkv,N,width,depth", [
+    (4, 4, 10, 3, 2),     # 10 rows: a packed block
+    (16, 2, 40, 4, 3),    # G = 8, 320 rows: 128-row blocks, the last one partial
+])
+def test_nan_padding_never_leaks(gpu_lib, kernel, Hq, Hkv, N, width, depth):
+    w = synthetic.make_workload("llama7b", seed=3, L=100, N=N, width=width, depth=depth, Hq=Hq,
+                                Hkv=Hkv, V=64, S_cap=256, pad=float("nan"))
     got, st = gpu_attn(w)
+    assert (st == 0).all()
     assert np.isfinite(got).all()
-    assert_attn_close(got, full_oracle(w), "nan padding")
+    assert_attn_close(got, full_oracle(w), f"nan padding Hq{Hq} Hkv{Hkv} N{N}")
 
 
 def test_rescale_path(gpu_lib, kernel):
