@@ -20,6 +20,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import time
@@ -32,9 +33,22 @@ if ROOT not in sys.path:
 
 METRIC = "verified tree tokens/s; tree-attn + verify HBM GB/s as % of GB300 peak"
 UNIT = "tree tokens/s"
-WORKLOAD = "llama7b"
-WORKLOAD_DESC = ("LLaMA-7B-shaped tree verify: B1, Hq=Hkv=32, D128, bf16 KV prefix 2048, "
-                 "w5 d3 draft tree pruned to 64 nodes, V32000 fp32 logits, T=0.7 stochastic")
+WORKLOAD = "llama7b"   # the headline workload; --workload times the others the same way
+WORKLOADS = {
+    "llama7b": ("LLaMA-7B-shaped tree verify: B1, Hq=Hkv=32, D128, bf16 KV prefix 2048, "
+                "w5 d3 draft tree pruned to 64 nodes, V32000 fp32 logits, T=0.7 stochastic"),
+    "tiny": ("tiny: B1, Hq=Hkv=4, D64, fp32 Q/K/V, KV prefix 128, 8-node tree of depth 3, V1000, "
+             "T=1 stochastic"),
+    "dynamic": ("dynamic batch: B16, Hq=Hkv=32, D128, bf16 KV prefixes U[512,4096], trees of "
+                "U[16,96] nodes and depth U[2,5] in one ragged launch, V32000, greedy"),
+    "llama70b_gqa": ("LLaMA-2-70B-shaped GQA: B4, Hq=64, Hkv=8, D128, bf16 KV prefix 8192, "
+                     "128-node trees of depth 5 and width <= 8, V32000, T=0.7 stochastic"),
+    "long_chain": ("long context, chain: B8, Hq=Hkv=32, D128, bf16 KV prefix 32768, a chain of "
+                   "K=5 speculated tokens (6 nodes), V32000, T=0.7 stochastic"),
+    "long_tree": ("long context, tree: B8, Hq=Hkv=32, D128, bf16 KV prefix 32768, 128-node trees "
+                  "of depth 6 and width <= 8, V32000, T=0.7 stochastic"),
+}
+MODEL_LAYERS = {"llama70b_gqa": 80}   # 32 for the LLaMA-7B-shaped rest
 
 
 # --------------------------------------------------------------------------
@@ -64,15 +78,54 @@ def mask_bytes(w) -> int:
     return w.T * (4 + 16 + 4)
 
 
+def attn_flops(w) -> int:
+    """2 D flops for each score and 2 D for each weighted value, over the
+    keys each (node, head) row sees: its request's prefix, its ancestors and
+    itself."""
+    total = 0
+    for b in range(w.B):
+        lo, hi = w.offsets[b], w.offsets[b + 1]
+        par = w.parents[lo:hi]
+        depth = np.zeros(hi - lo, np.int64)
+        for i in range(1, hi - lo):
+            depth[i] = depth[par[i]] + 1
+        total += int((w.prefix_lens[b] + depth + 1).sum())
+    return 4 * w.D * w.Hq * total
+
+
+def describe(name: str, temperature, prefix=None) -> str:
+    desc = WORKLOADS[name]
+    if prefix is not None:
+        desc = re.sub(r"KV prefix \d+", f"KV prefix {prefix}", desc)
+    if temperature is None:
+        return desc
+    head, _, _ = desc.rpartition(", ")
+    return f"{head}, " + ("greedy" if temperature == 0 else f"T={temperature:g} stochastic")
+
+
+def prefix_override(args) -> dict:
+    """--prefix sets the KV prefix length of the workloads whose requests
+    share one (all but the dynamic batch, whose prefixes are drawn)."""
+    if args.prefix is None:
+        return {}
+    if args.workload == "dynamic":
+        raise SystemExit("--prefix does not apply to the dynamic batch (its prefixes are drawn)")
+    return {"L": args.prefix}
+
+
 # --------------------------------------------------------------------------
 # environment helpers
 # --------------------------------------------------------------------------
-def measured_peaks():
+def measured_peaks(kind: str = "hbm"):
+    """The roofline denominator: HBM copy GB/s, or dense bf16 TFLOP/s (burst:
+    each kernel is timed alone)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key, fallback = ("hbm_gbs", 6800.0) if kind == "hbm" else ("bf16_tflops", 1900.0)
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        if key in d:
+            return float(d[key]), "measured"
+    return fallback, "fallback"
 
 
 def source_hash(paths):
@@ -206,7 +259,8 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     import token_tree_verification_gb300 as ttv
     ttv.load()
-    w = synthetic.make_workload(WORKLOAD, seed=0, device="cuda", pad=0.0)
+    w = synthetic.make_workload(args.workload, seed=0, device="cuda", pad=0.0,
+                                temperature=args.temperature, **prefix_override(args))
     l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
     per_copy = (w.q.numel() + w.k_cache.numel() + w.v_cache.numel()) * w.q.element_size() \
         + w.target_logits.nbytes + (w.draft_logits.nbytes if w.draft_logits is not None else 0)
@@ -304,27 +358,42 @@ def run_native(args, rank, world, local_rank):
     achieved = ab / (attn_ms * 1e-3) / 1e9
     # the roofline block describes the kernel that takes the larger share of the step
     if ver_ms > attn_ms:
-        dom = {"kernel": ("tree_verify_reg_kernel" if w.V <= 131072 else "tree_verify_cluster_kernel")
-               if w.temperature > 0 else "tree_verify_greedy_node_kernel",
-               "bytes": vb, "ms": ver_ms, "traffic": profiled_traffic("tree_verify_llama7b")}
+        kname = (("tree_verify_reg_kernel" if w.V <= 131072 else "tree_verify_cluster_kernel")
+                 if w.temperature > 0 else "tree_verify_greedy_node_kernel")
+        roof = {"bound": "hbm", "kernel": kname, "achieved": vb / (ver_ms * 1e-3) / 1e9, "peak": peak,
+                "unit": "GB/s", "traffic": profiled_traffic(f"tree_verify_{args.workload}"),
+                "algorithmic_bytes": vb, "launch_ms": ver_ms,
+                "peak_kind": f"{peak_kind} (STREAM-style copy, burst)"}
     else:
-        dom = {"kernel": "tree_attn_tc_kernel", "bytes": ab, "ms": attn_ms,
-               "traffic": profiled_traffic("tree_attn_llama7b")}
-    dom_gbs = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+        if w.q.dtype == torch.float32:
+            kname = "tree_attn_f32_kernel"
+        elif os.environ.get("SPEC_TREE_ATTN_KERNEL") == "mma":
+            kname = "tree_attn_mma_kernel"
+        else:
+            kname = "tree_attn_tc_kernel"
+        roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "traffic": profiled_traffic(f"tree_attn_{args.workload}"), "algorithmic_bytes": ab,
+                "launch_ms": attn_ms, "peak_kind": f"{peak_kind} (STREAM-style copy, burst)"}
+        fl = attn_flops(w)
+        if fl / ab > 300:
+            # a contraction with this many flops per byte is bound by the tensor pipe
+            tpeak, tkind = measured_peaks("bf16")
+            roof.update({"bound": "tensor", "achieved": fl / (attn_ms * 1e-3) / 1e12, "peak": tpeak,
+                         "unit": "TFLOP/s", "algorithmic_flops": fl,
+                         "peak_kind": f"{tkind} (cuBLAS bf16 GEMM, burst)"})
+    roof["frac"] = roof["achieved"] / roof["peak"]
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded; no datasets or weights)",
-        "config": {"workload": WORKLOAD_DESC, "T": w.T, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+        "dtype": "f32" if w.q.dtype == torch.float32 else "bf16",
+        "data": "synthetic (seeded; no datasets or weights)",
+        "config": {"workload": describe(args.workload, args.temperature, args.prefix), "T": w.T, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "prefix": int(w.prefix_lens[0]), "V": w.V, "temperature": w.temperature,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs rotate over {copies} device copies ({copies * per_copy / 1e6:.0f} MB > 4x L2)",
                    "launch": f"CUDA graph of {chunk} steps, replayed"},
-        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom_gbs,
-                     "peak": peak, "unit": "GB/s", "frac": dom_gbs / peak, "traffic": dom["traffic"],
-                     "algorithmic_bytes": dom["bytes"], "launch_ms": dom["ms"],
-                     "peak_kind": f"{peak_kind} (STREAM-style copy, burst)"},
+        "roofline": roof,
         "kernels": {
             "mask": {"ms": mask_ms, "bytes": mb},
             "attn": {"ms": attn_ms, "bytes": ab, "gbs": achieved},
@@ -338,10 +407,13 @@ def run_native(args, rank, world, local_rank):
         "gpu_launches": 3 * K,
         "clocks": clocks, "clock_window": "timed region + 1 s soak of the same graph" if soak else "timed region",
     }
-    result.update(derived_rates(st, stream, ms_per_step, mask_ms, attn_ms, ver_ms))
-    result["next_rows"] = {"kv_compact": time_kv_compact(st, stream, chunk),
-                           "tree_build": time_tree_build(w, stream, chunk),
-                           "top_p": time_verify_top_p(st, stream, chunk)}
+    result.update(derived_rates(st, stream, ms_per_step, mask_ms, attn_ms, ver_ms,
+                                layers=MODEL_LAYERS.get(args.workload, 32)))
+    if args.workload == WORKLOAD:
+        # the rows after the hot path, on the headline workload's shapes
+        result["next_rows"] = {"kv_compact": time_kv_compact(st, stream, chunk),
+                               "tree_build": time_tree_build(w, stream, chunk),
+                               "top_p": time_verify_top_p(st, stream, chunk)}
     if not args.no_e2e:
         result["e2e"] = run_e2e(st, w, stream, args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -649,7 +721,7 @@ def run_e2e(st, w, stream, steps):
             ttv.build_tree_mask(d["par"], d["off"], st.status, mask=st.mask, depth=st.depth, stream=stream)
             ttv.tree_attn(d["q"], d["k"], d["v"], d["pl"], d["off"], st.mask, st.max_prefix,
                           st.status, o=st.o, workspace=st.ws_attn, stream=stream)
-            ttv.tree_verify(d["tl"], d["dl"], d["tok"], d["par"], d["off"], w.temperature,
+            ttv.tree_verify(d["tl"], d.get("dl"), d["tok"], d["par"], d["off"], w.temperature,
                             st.seed + i, st.W, st.status, st.ws, outputs=outs, stream=stream)
             free[i % 2].record(stream)
             out_host[i % 2].copy_(out_dev, non_blocking=True)
@@ -739,7 +811,8 @@ def run_reference(args, rank, world):
     import oracle
     from token_tree_verification_gb300 import synthetic
     oracle.build()
-    w = synthetic.make_workload(WORKLOAD, seed=0, device="cpu", pad=0.0)
+    w = synthetic.make_workload(args.workload, seed=0, device="cpu", pad=0.0,
+                                temperature=args.temperature, **prefix_override(args))
     oi = OracleInputs(w)
     n_rows = w.T * w.Hq
     # size each step's attention sample so that K + W steps take ~2 minutes
@@ -756,7 +829,8 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "parallelism": "1 host thread"},
+            "config": {"workload": describe(args.workload, args.temperature, args.prefix),
+                       "parallelism": "1 host thread"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -771,6 +845,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOADS),
+                    help="the workload to time (default: the headline LLaMA-7B-shaped step)")
+    ap.add_argument("--prefix", type=int, default=None,
+                    help="KV prefix length (every workload but the dynamic batch); default: the workload's own")
+    ap.add_argument("--temperature", type=float, default=None,
+                    help="verification temperature (0 = greedy); default: the workload's own")
     ap.add_argument("--eager", action="store_true",
                     help="plain stream launches without graphs or timing (for profilers)")
     args = ap.parse_args()
