@@ -56,8 +56,8 @@ MODEL_LAYERS = {"llama70b_gqa": 80}   # 32 for the LLaMA-7B-shaped rest
 # --------------------------------------------------------------------------
 def attn_bytes(w) -> int:
     """KV of every prefix + tree slot read once per KV head, Q read once, O
-    written once (bf16)."""
-    el = 2
+    written once, in the inputs' dtype (O takes Q's)."""
+    el = w.q.element_size()
     kv = sum(int(w.prefix_lens[b] + w.offsets[b + 1] - w.offsets[b]) for b in range(w.B)) * w.Hkv * w.D * el * 2
     return kv + 2 * w.T * w.Hq * w.D * el
 
