@@ -514,8 +514,8 @@ bool use_mma_kernel() {
   return e != nullptr && strcmp(e, "mma") == 0;
 }
 
-// SMs of the current device; 152 (GB300) when no device can be queried, so a
-// host-only caller still gets the workspace size the GPU will ask for.
+// SMs of the current device (the split plan sizes grids by it); 152 (GB300)
+// when no device can be queried.
 int sm_count() {
   static std::atomic<int> n[spec::kMaxDevices];
   const int dev = spec::current_device();
