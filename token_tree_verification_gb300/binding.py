@@ -5,6 +5,10 @@ contiguity, and their device pointers plus the current CUDA stream are passed
 to the C ABI.  Every step of the computation runs in the library's CUDA
 kernels; if the library cannot be loaded the calls raise, there is no CPU
 fallback.
+
+The library launches on the current CUDA device, so a call's tensors must
+live there (``torch.cuda.set_device`` or ``with torch.cuda.device(...)``
+around calls on another GPU).
 """
 from __future__ import annotations
 
