@@ -14,10 +14,12 @@
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL means the legacy default stream).  No call synchronises the host.
  *  - A call launches on the calling thread's current CUDA device; its
- *    pointers and stream must belong to that device.  The library is safe to
- *    call from several threads and on several devices in one process: what
- *    it caches about a device (kernel shared-memory limits, the SM count) is
- *    kept per device.
+ *    pointers and stream must belong to that device.  Calls may come from
+ *    several threads and go to several devices in one process: what the
+ *    library caches about a device (kernel shared-memory limits, the SM
+ *    count) is kept per device.  Calls whose work overlaps must not share a
+ *    workspace; spec_tree_verify_static shares one array per device among
+ *    all its calls (see there).
  *  - Host-detectable errors (null pointers, bad sizes, workspace too small)
  *    return a negative spec_status synchronously and launch nothing.
  *  - Data-dependent errors found on the device (a malformed parent array, a
