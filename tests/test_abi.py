@@ -78,3 +78,50 @@ def test_host_side_validation(lib):
                                 *outs, fake, ws, fake, None) == -1
     assert lib.spec_tree_verify(*args, ctypes.c_float(float("nan")), 0, *outs, fake, ws, fake,
                                 None) == -2
+
+
+def test_host_side_validation_of_the_other_entry_points(lib):
+    P, F32, U64, I, SZ = ctypes.c_void_p, ctypes.c_float, ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
+    fake = P(0x1000)   # never dereferenced: validation fails before any launch
+    # top-p verification: top_p must be > 0 (NaN rejected); the nucleus search
+    # covers V <= 131072
+    V = 1000
+    ws = lib.spec_tree_verify_workspace_size(1, 8, V)
+    outs = [fake, fake, fake, fake, 4]
+    f = lib.spec_tree_verify_top_p
+    assert f(fake, fake, fake, fake, fake, 1, 8, V, F32(0.7), F32(0.0), 0, *outs, fake, ws, fake, None) == -2
+    assert f(fake, fake, fake, fake, fake, 1, 8, V, F32(0.7), F32(float("nan")), 0, *outs, fake, ws, fake,
+             None) == -2
+    big = 131073
+    wsb = lib.spec_tree_verify_workspace_size(1, 8, big)
+    assert f(fake, fake, fake, fake, fake, 1, 8, big, F32(0.7), F32(0.9), 0, *outs, fake, wsb, fake, None) == -2
+    assert f(fake, None, fake, fake, fake, 1, 8, V, F32(0.7), F32(0.9), 0, *outs, fake, ws, fake, None) == -1
+    # KV compaction
+    g = lib.spec_kv_compact
+    kv = lambda k=fake, dtype=1, D=128, W=4: g(k, fake, dtype, 1, 2, D, 256, fake, fake, fake, fake, W,
+                                               fake, fake, None)
+    assert g(None, fake, 1, 1, 2, 128, 256, fake, fake, fake, fake, 4, fake, fake, None) == -1
+    assert kv(dtype=7) == -3
+    assert kv(D=4) == -2                    # D < 8
+    assert kv(W=0) == -2                    # no output row
+    assert kv(W=129) == -2                  # more rows than a tree has nodes
+    assert kv(dtype=0, D=1024, W=128) == -2  # 127 rows of 4 KB, K and V: beyond shared memory
+    assert kv(k=P(0x1008)) == -11
+    # expansion
+    e = lib.spec_tree_expand
+    ex = lambda F=4, V=64, w=5, t=0.7: e(fake, fake, fake, fake, F, V, w, F32(t), 1, fake, fake, fake, None)
+    assert e(None, fake, fake, fake, 4, 64, 5, F32(0.7), 1, fake, fake, fake, None) == -1
+    assert ex(F=0) == -2 and ex(w=0) == -2 and ex(w=17) == -2 and ex(V=4, w=5) == -2
+    assert ex(t=float("nan")) == -2 and ex(t=-1.0) == -2
+    # pruning
+    p = lib.spec_tree_prune
+    pr = lambda B=1, keep=64: p(fake, fake, fake, fake, B, keep, fake, fake, fake, fake, fake, None)
+    assert p(None, fake, fake, fake, 1, 64, fake, fake, fake, fake, fake, None) == -1
+    assert pr(B=0) == -2 and pr(keep=0) == -2 and pr(keep=129) == -2
+    # the static entry point refuses a batch beyond its fixed array before touching a device
+    s = lib.spec_tree_verify_static
+    s.argtypes = [P, P, P, P, P, I, I, I, F32, U64, P, P, P, P, I, P, P]
+    s.restype = I
+    B, T = 400, 40000
+    assert lib.spec_tree_verify_workspace_size(B, T, 32000) > 256 * 1024
+    assert s(fake, fake, fake, fake, fake, B, T, 32000, F32(0.7), 0, *outs, fake, None) == -7
