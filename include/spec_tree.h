@@ -298,6 +298,9 @@ int spec_tree_expand(const float *draft_logits, const float *parent_scores,
  * root first) keep the root and the keep - 1 other candidates of highest
  * score, ties to the lower index.  Scores never increase along a path (each
  * adds a log-probability <= 0), so the kept set is closed under ancestors.
+ * Scores from elsewhere must keep that property.  When a kept candidate's
+ * parent is not kept, its out_parent is -1: the output is then no tree, and
+ * spec_build_tree_mask rejects it with SPEC_ERR_BAD_PARENT.
  * Outputs at stride `keep`, kept candidates in their original order:
  *   out_parents [B][keep] renumbered parents (-2 past n_out[b])
  *   out_tokens  [B][keep], kept_index [B][keep] (candidate index, -1 past n_out)

@@ -102,3 +102,16 @@ def test_expand_then_prune_builds_a_valid_tree():
     out = oracle.tree_prune(parents, tokens, scores, [0, len(parents)], keep)
     par = out["parents"][0]
     assert par[0] == -1 and all(0 <= par[i] < i for i in range(1, keep))
+
+
+def test_pruning_non_monotone_scores_orphans_and_the_mask_rejects_it():
+    # a chain 0 -> 1 -> 2 whose grandchild outscores its parent: with keep 2 the
+    # root and node 2 survive, node 2's parent (1) is dropped
+    par = np.array([-1, 0, 1], np.int32)
+    sc = np.array([0.0, -3.0, -1.0])
+    out = oracle.tree_prune(par, np.array([5, 6, 7], np.int32), sc, [0, 3], 2)
+    assert out["status"].tolist() == [0]
+    assert out["kept"][0].tolist() == [0, 2]
+    assert out["parents"][0].tolist() == [-1, -1]
+    _, _, st = oracle.build_mask(out["parents"][0], np.array([0, 2], np.int32))
+    assert st.tolist() == [-5]   # bad parent
