@@ -87,10 +87,12 @@ def test_random_tree_equals_sdpa_with_networkx_mask():
         return m
     got = oracle.tree_attn(q, k, v, L, off, par)
     np.testing.assert_allclose(got, sdpa_reference(q, k, v, L, off, par, vis), rtol=1e-11, atol=1e-12)
-    # an explicit softmax scale is honoured
-    got2 = oracle.tree_attn(q, k, v, L, off, par, scale=0.3)
-    np.testing.assert_allclose(got2, sdpa_reference(q, k, v, L, off, par, vis, scale=0.3),
-                               rtol=1e-11, atol=1e-12)
+    # an explicit softmax scale is honoured, 1.0 included (the unscaled
+    # scores of the developer article's tree_attention snippet)
+    for sc in (0.3, 1.0):
+        got2 = oracle.tree_attn(q, k, v, L, off, par, scale=sc)
+        np.testing.assert_allclose(got2, sdpa_reference(q, k, v, L, off, par, vis, scale=sc),
+                                   rtol=1e-11, atol=1e-12)
 
 
 def test_each_path_alone_is_bit_identical():
