@@ -326,16 +326,18 @@ int spec_tree_prune(const int32_t *parents, const int32_t *tokens, const float *
  * library, held on every GPU that loads the library until the process exits.
  *
  * Arguments, outputs and device-side errors are those of spec_tree_verify.
- * The call allocates nothing and frees nothing; it clears the part of the
- * array it uses (an asynchronous memset on `stream`) and then runs the same
- * kernels as spec_tree_verify.
+ * The call allocates nothing and frees nothing; once every host-side check
+ * has passed it clears the part of the array it uses (an asynchronous memset
+ * on `stream`) and then runs the same kernels as spec_tree_verify.  A call
+ * that fails a host-side check enqueues nothing.
  *  - Returns SPEC_ERR_WORKSPACE, before touching the device, when
  *    spec_tree_verify_workspace_size(B, T, V) exceeds
  *    SPEC_VERIFY_STATIC_SCRATCH_BYTES (for example more than about 32000
  *    tree nodes in one batch); use spec_tree_verify with a workspace then.
  *  - The first call made with a device current looks up the array's device
- *    address on that device (cudaGetSymbolAddress).  Make that first call
- *    before any stream capture.
+ *    address on that device (cudaGetSymbolAddress), and so does the first
+ *    call after that device's context was destroyed and created again (a
+ *    device reset).  Make such a call before any stream capture.
  *  - Every call on a device shares the one array, and it keeps the last
  *    call's contents: calls whose work overlaps on the GPU (different
  *    streams, or different host threads) race and give wrong results.

@@ -60,10 +60,17 @@ def _load():
     lib.oracle_tree_verify_top_p.restype = i32
     lib.oracle_kv_compact.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, i32, P, P]
     lib.oracle_kv_compact.restype = i32
-    lib.oracle_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, ctypes.c_double, u64, P, P, P]
+    lib.oracle_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, ctypes.c_double, u64, P, P, P, P]
     lib.oracle_tree_expand.restype = i32
     lib.oracle_tree_prune.argtypes = [P, P, P, P, i32, i32, P, P, P, P, P]
     lib.oracle_tree_prune.restype = i32
+    lib.oracle_verify_nodes.argtypes = [P, P, P, P, P, i32, i32, i32, ctypes.c_float,
+                                        ctypes.c_double, u64, i32, ctypes.c_double, P, P, P, P, P, P]
+    lib.oracle_verify_nodes.restype = i32
+    lib.oracle_nucleus_alternatives.argtypes = [P, i32, ctypes.c_double, P, P]
+    lib.oracle_nucleus_alternatives.restype = i32
+    lib.oracle_nucleus_max_alternatives.argtypes = []
+    lib.oracle_nucleus_max_alternatives.restype = i32
     _lib = lib
     return lib
 
@@ -173,6 +180,51 @@ def tree_verify(target_logits, draft_logits, tokens, parents, offsets, temperatu
     return res
 
 
+def verify_nodes(target_logits, draft_logits, tokens, parents, offsets, temperature: float,
+                 seed: int, max_depth_plus1: int, top_p: float = 1.0, band: float = 1e-5,
+                 want=None):
+    """The decisions at every node (or every node with ``want[t]``) as if the
+    walk reached it: dict of next [T] (accepted child, request-local, or -1 to
+    stop; -2 when not evaluated), token [T] (the emitted token when stopping),
+    margin [T] (smallest distance of a decision from its threshold; inf for
+    greedy, 0 for a fragile top-p node), n_close [T] (decisions within
+    ``band``, top-p: plus those involving an entry near tau), status [B]."""
+    tl = _c(target_logits, np.float32)
+    T, V = tl.shape
+    dl = None if draft_logits is None else _c(draft_logits, np.float32)
+    tok = _c(tokens, np.int32)
+    par = _c(parents, np.int32)
+    off = _c(offsets, np.int32)
+    B = off.size - 1
+    wa = None if want is None else _c(want, np.uint8)
+    res = dict(next=np.zeros(T, np.int32), token=np.zeros(T, np.int32),
+               margin=np.zeros(T, np.float64), n_close=np.zeros(T, np.int32),
+               status=np.zeros(B, np.int32))
+    rc = _load().oracle_verify_nodes(
+        _ptr(tl), _ptr(dl), _ptr(tok), _ptr(par), _ptr(off), B, T, V, ctypes.c_float(temperature),
+        float(top_p), seed & (2**64 - 1), int(max_depth_plus1), float(band), _ptr(wa),
+        _ptr(res["next"]), _ptr(res["token"]), _ptr(res["margin"]), _ptr(res["n_close"]),
+        _ptr(res["status"]))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_nodes: status {rc}")
+    return res
+
+
+def nucleus_alternatives(d, top_p: float):
+    """The plausible top-p nuclei of distribution ``d`` (float64 [V]):
+    (tau, keep-flags [n][V] bool, row 0 the exact nucleus), or (tau, None)
+    when there are more than the enumeration takes."""
+    lib = _load()
+    da = _c(d, np.float64)
+    V = da.size
+    keeps = np.zeros((lib.oracle_nucleus_max_alternatives(), V), np.uint8)
+    tau = ctypes.c_double(0.0)
+    n = lib.oracle_nucleus_alternatives(_ptr(da), V, float(top_p), _ptr(keeps), ctypes.byref(tau))
+    if n < -1:
+        raise ValueError("oracle_nucleus_alternatives: allocation failed")
+    return tau.value, (None if n < 0 else keeps[:n].astype(bool))
+
+
 def kv_compact(cache, prefix_lens, offsets, path_nodes, accept_len, status=None):
     """Depth-first KV-cache update (oracle_kv_compact) on a copy of ``cache``
     ([B][H][S_cap][D], any fixed-size dtype).  Returns (new_cache,
@@ -192,21 +244,25 @@ def kv_compact(cache, prefix_lens, offsets, path_nodes, accept_len, status=None)
     return c, newp, st
 
 
-def tree_expand(draft, parent_scores, node_ids, reqs, width: int, temperature: float, seed: int):
+def tree_expand(draft, parent_scores, node_ids, reqs, width: int, temperature: float, seed: int,
+                with_gaps: bool = False):
     """One level of draft-tree expansion (oracle_tree_expand).  Returns
-    (tokens [F][width], scores [F][width], ties [F][width])."""
+    (tokens [F][width], scores [F][width], ties [F][width]), plus gaps
+    [F][width] (each draw's relative distance from the nearer inverse-CDF
+    boundary) with ``with_gaps``."""
     lib = _load()
     d = _c(draft, np.float32)
     F, V = d.shape
     tok = np.zeros((F, width), np.int32)
     sc = np.zeros((F, width), np.float64)
     ties = np.zeros((F, width), np.int32)
+    gaps = np.zeros((F, width), np.float64)
     rc = lib.oracle_tree_expand(_ptr(d), _ptr(_c(parent_scores, np.float64)), _ptr(_c(node_ids, np.int32)),
                                 _ptr(_c(reqs, np.int32)), F, V, width, float(temperature),
-                                int(seed) & (2**64 - 1), _ptr(tok), _ptr(sc), _ptr(ties))
+                                int(seed) & (2**64 - 1), _ptr(tok), _ptr(sc), _ptr(ties), _ptr(gaps))
     if rc != 0:
         raise ValueError(f"oracle_tree_expand: {rc}")
-    return tok, sc, ties
+    return (tok, sc, ties, gaps) if with_gaps else (tok, sc, ties)
 
 
 def tree_prune(parents, tokens, scores, cand_offsets, keep: int):

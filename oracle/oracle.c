@@ -257,11 +257,19 @@ static int argmax_f(const float *row, int V) {
   return best;
 }
 
+/* Two decisions the walk takes are compared against a threshold: the accept
+ * test (uniform against alpha) and the inverse-CDF draw (u * total against
+ * the running sums).  A decision whose distance from its threshold is below
+ * TIE_BAND is a near-tie: a float32 implementation may take it the other
+ * way, so it is counted ([expl] §2.2 fixes the rule, not its rounding). */
+#define TIE_BAND 1e-6
+
 /* Inverse-CDF draw from unnormalised weights w[V] >= 0 with uniform u:
  * the first x whose running sum (ascending x) exceeds u * sum(w); if rounding
- * never lets the running sum pass it, the last x with w[x] > 0.  Sets *tie
- * when u*sum lies within 1e-6*sum of the chosen interval's ends. */
-static int sample_inverse_cdf(const double *w, int V, double u, int *tie) {
+ * never lets the running sum pass it, the last x with w[x] > 0.  *gap is the
+ * distance of u * sum(w) from the nearer end of the chosen interval, relative
+ * to sum(w) (infinite for an all-zero w). */
+static int sample_inverse_cdf(const double *w, int V, double u, double *gap) {
   double total = 0.0;
   for (int x = 0; x < V; ++x) total += w[x];
   double target = u * total;
@@ -278,7 +286,7 @@ static int sample_inverse_cdf(const double *w, int V, double u, int *tie) {
     if (pick < 0) pick = 0;
     prev = run; /* boundary is the end of the cumulative sum */
   }
-  if (fabs(target - prev) < 1e-6 * total || fabs(target - run) < 1e-6 * total) *tie = 1;
+  *gap = total > 0.0 ? fmin(fabs(target - prev), fabs(target - run)) / total : INFINITY;
   return pick;
 }
 
@@ -288,7 +296,7 @@ static int sample_inverse_cdf(const double *w, int V, double u, int *tie) {
  *   accept_len[b]          number of speculated tokens accepted
  *   path_nodes[b][0..a]    request-local node ids: root, then accepted nodes
  *   out_tokens[b][0..a]    tokens of the accepted nodes, then the bonus token
- *   near_ties[b]           decisions on the walk within 1e-6 of flipping
+ *   near_ties[b]           decisions on the walk within TIE_BAND of flipping
  * unused row entries are set to -1.
  *
  * Greedy (temperature == 0): at node u accept the first child whose token is
@@ -303,88 +311,40 @@ static int sample_inverse_cdf(const double *w, int V, double u, int *tie) {
  * rejected token is replaced by a new target prediction; the residual keeps
  * the output distribution equal to the target's).  If every child is
  * rejected (or u is a leaf), draw the emitted token from r and stop. */
-/* Nucleus (top-p) of a distribution d[V] (developer article, deployment
- * configuration: top_p).  tau is the largest value whose upper tail
- * {d >= tau} holds at least top_p of the mass; every entry of that tail is
- * kept (entries tied at tau included), the rest set to 0, and the tail
- * renormalised.
- *
- * Which nucleus a finite-precision implementation finds can differ from the
- * exact one where the running mass crosses top_p within its rounding: every
- * cut {d >= t} whose tail holds at least top_p - eps while the tail above t
- * holds less than top_p + eps is one it may find.  nucleus_cuts lists those
- * thresholds t (the exact tau first); the walk counts a near-tie at a node
- * only when two of them lead to different decisions there. */
-static int cmp_desc(const void *a, const void *b) {
-  const double x = *(const double *)a, y = *(const double *)b;
-  return (x < y) - (x > y);
+
+/* What happens at one node if the walk reaches it. */
+typedef struct {
+  int next;       /* the accepted child (request-local index), or -1: stop at the node */
+  int token;      /* the emitted token when next == -1 */
+  int ties;       /* decisions within TIE_BAND of flipping */
+  double margin;  /* the smallest distance of any decision from its threshold */
+  int n_close;    /* decisions within the caller's band (and, for top-p, decisions
+                     that involve an entry near the nucleus threshold; see below) */
+} node_outcome;
+
+static void note_decision(node_outcome *o, double dist, double band) {
+  if (dist < TIE_BAND) ++o->ties;
+  if (dist < band) ++o->n_close;
+  if (dist < o->margin) o->margin = dist;
 }
 
-#define NUCLEUS_EPS 5e-6
-#define NUCLEUS_MAX_CUTS 64
-
-/* Returns the number of plausible thresholds written to cuts[] (cuts[0] is
- * the exact tau), or -1 when there are more than NUCLEUS_MAX_CUTS. */
-static int nucleus_cuts(const double *d, int V, double top_p, double *sorted, double *cuts) {
-  memcpy(sorted, d, sizeof(double) * (size_t)V);
-  qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
-  /* distinct values in descending order with the tail mass above each */
-  double above = 0.0, tau = sorted[V - 1];
-  int n = 0, found = 0;
-  for (int i = 0; i < V;) {
-    const double t = sorted[i];
-    double group = 0.0;
-    int k = i;
-    while (k < V && sorted[k] == t) group += sorted[k++];
-    const double ge = above + group;  /* tail {d >= t} */
-    if (!found && ge >= top_p) { tau = t; found = 1; }
-    i = k;
-    above = ge;
-  }
-  if (!found) tau = sorted[V - 1];
-  cuts[n++] = tau;
-  above = 0.0;
-  for (int i = 0; i < V;) {
-    const double t = sorted[i];
-    double group = 0.0;
-    int k = i;
-    while (k < V && sorted[k] == t) group += sorted[k++];
-    const double ge = above + group;
-    if (t != tau && ge >= top_p - NUCLEUS_EPS && above < top_p + NUCLEUS_EPS) {
-      if (n == NUCLEUS_MAX_CUTS) return -1;
-      cuts[n++] = t;
-    }
-    if (above >= top_p + NUCLEUS_EPS) break;
-    i = k;
-    above = ge;
-  }
-  return n;
-}
-
-/* out = d restricted to {d >= t}, renormalised */
-static void nucleus_apply(const double *d, int V, double t, double *out) {
-  double mass = 0.0;
-  for (int v = 0; v < V; ++v)
-    if (d[v] >= t) mass += d[v];
-  for (int v = 0; v < V; ++v) out[v] = d[v] >= t ? d[v] / mass : 0.0;
-}
-
-/* The stochastic decisions at node u of request b for target p and draft qd:
- * u's children in ascending index order against the residual r (scratch,
- * V entries), then, when every child is rejected, the inverse-CDF draw from
- * r.  Returns the accepted child, or -1 with *token the drawn token;
- * *ties counts decisions within 1e-6 of flipping. */
-static int node_decide(const double *p, const double *qd, double *r, int V,
-                       const int32_t *par, const int32_t *tok, int n, int u, int b,
-                       uint64_t seed, int *token, int *ties) {
+/* The stochastic decisions at node u of request b for target p and draft qd
+ * (r: V entries of scratch for the running residual): u's children in
+ * ascending index order, each against r, then, when every child is
+ * rejected, the inverse-CDF draw from r.  Distances: |uniform - alpha| for a
+ * test, the draw's relative gap for the draw. */
+static node_outcome node_decide(const double *p, const double *qd, double *r, int V,
+                                const int32_t *par, const int32_t *tok, int n, int u, int b,
+                                uint64_t seed, double band) {
+  node_outcome o = {-1, -1, 0, INFINITY, 0};
   memcpy(r, p, sizeof(double) * (size_t)V);
   for (int c = u + 1; c < n; ++c) {
     if (par[c] != u) continue;
     int x = tok[c];
     double alpha = qd[x] > 0.0 ? fmin(1.0, r[x] / qd[x]) : 1.0;
     double uu = oracle_uniform(seed, c, b, 0);
-    if (fabs(uu - alpha) < 1e-6) ++*ties;
-    if (uu < alpha) return c;
+    note_decision(&o, fabs(uu - alpha), band);
+    if (uu < alpha) { o.next = c; return o; }
     /* rejected: residual r <- norm(max(0, r - q)); a zero residual
      * (r == q up to rounding) leaves r unchanged */
     double s = 0.0;
@@ -392,10 +352,238 @@ static int node_decide(const double *p, const double *qd, double *r, int V,
     if (s > 0.0)
       for (int y = 0; y < V; ++y) r[y] = fmax(0.0, r[y] - qd[y]) / s;
   }
-  int tie = 0;
-  *token = sample_inverse_cdf(r, V, oracle_uniform(seed, u, b, 1), &tie);
-  *ties += tie;
-  return -1;
+  double gap;
+  o.token = sample_inverse_cdf(r, V, oracle_uniform(seed, u, b, 1), &gap);
+  note_decision(&o, gap, band);
+  return o;
+}
+
+/* ---- top-p (developer article, deployment configuration: top_p) -------
+ * The nucleus of a distribution d[V]: tau is the largest value whose upper
+ * tail {d >= tau} holds at least top_p of the mass (the smallest value when
+ * rounding leaves every tail below it); every entry of that tail is kept
+ * (entries tied at tau included), the rest drop to 0, and the tail is
+ * renormalised.
+ *
+ * Which nucleus a float32 implementation finds can differ from the exact one
+ * in two ways, and each has one band:
+ *  - mass: a cut {d >= t} whose tail mass lies within NUCLEUS_MASS_BAND of
+ *    top_p on the right side (tail >= top_p - band, mass above t < top_p +
+ *    band) may be the one it finds;
+ *  - value: entries within NUCLEUS_VALUE_BAND * tau of tau (2^-16 relative,
+ *    128 float32 ulps at the bottom of a binade) may sit on either side of
+ *    tau in float32, so any subset of their distinct values may be kept.
+ * The plausible nuclei are the exact one, the mass-band cuts and the
+ * value-band subsets; a node is fragile when two plausible pairs (p's
+ * nucleus, q's nucleus) lead to different decisions there. */
+#define NUCLEUS_MASS_BAND 5e-6
+#define NUCLEUS_VALUE_BAND (1.0 / 65536.0)
+#define NUCLEUS_MAX_CUTS 16
+#define NUCLEUS_MAX_NEAR 4
+#define NUCLEUS_MAX_ALT (1 + NUCLEUS_MAX_CUTS + (1 << NUCLEUS_MAX_NEAR))
+
+static int cmp_desc(const void *a, const void *b) {
+  const double x = *(const double *)a, y = *(const double *)b;
+  return (x < y) - (x > y);
+}
+
+/* d's values sorted in descending order into sorted[V]; returns tau. */
+static double nucleus_tau(const double *d, int V, double top_p, double *sorted) {
+  memcpy(sorted, d, sizeof(double) * (size_t)V);
+  qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
+  double above = 0.0;
+  for (int i = 0; i < V;) {
+    const double t = sorted[i];
+    double group = 0.0;
+    int k = i;
+    while (k < V && sorted[k] == t) group += sorted[k++];
+    if (above + group >= top_p) return t;
+    above += group;
+    i = k;
+  }
+  return sorted[V - 1];
+}
+
+/* The plausible nuclei of d as keep-flags keeps[a][V] (a = 0: the exact
+ * nucleus).  Returns their number, or -1 when there are more cuts or
+ * near-tau values than this enumeration takes (the node is then fragile).
+ * *tau_out receives the exact tau. */
+static int nucleus_alternatives(const double *d, int V, double top_p, double *sorted,
+                                unsigned char *keeps, double *tau_out) {
+  const double tau = nucleus_tau(d, V, top_p, sorted);
+  *tau_out = tau;
+  int n = 0;
+  for (int x = 0; x < V; ++x) keeps[x] = d[x] >= tau;
+  ++n;
+  /* mass band: cuts at the other distinct values t (sorted[] descending) */
+  double above = 0.0;
+  for (int i = 0; i < V;) {
+    const double t = sorted[i];
+    double group = 0.0;
+    int k = i;
+    while (k < V && sorted[k] == t) group += sorted[k++];
+    if (t != tau && above + group >= top_p - NUCLEUS_MASS_BAND &&
+        above < top_p + NUCLEUS_MASS_BAND) {
+      if (n == 1 + NUCLEUS_MAX_CUTS) return -1;
+      unsigned char *kp = keeps + (size_t)n * V;
+      for (int x = 0; x < V; ++x) kp[x] = d[x] >= t;
+      ++n;
+    }
+    if (above >= top_p + NUCLEUS_MASS_BAND) break;
+    above += group;
+    i = k;
+  }
+  /* value band: the distinct values within NUCLEUS_VALUE_BAND * tau of tau */
+  const double lo = tau * (1.0 - NUCLEUS_VALUE_BAND), hi = tau * (1.0 + NUCLEUS_VALUE_BAND);
+  double near[NUCLEUS_MAX_NEAR];
+  int nn = 0;
+  for (int i = 0; i < V; ++i) {
+    const double t = sorted[i];
+    if (t < lo || t > hi || (nn > 0 && near[nn - 1] == t)) continue;
+    if (nn == NUCLEUS_MAX_NEAR) return -1;
+    near[nn++] = t;
+  }
+  if (nn > 1) {
+    for (int s = 0; s < (1 << nn); ++s) {
+      unsigned char *kp = keeps + (size_t)n * V;
+      for (int x = 0; x < V; ++x) {
+        int keep = d[x] > hi;
+        for (int j = 0; j < nn; ++j)
+          if (((s >> j) & 1) && d[x] == near[j]) keep = 1;
+        kp[x] = (unsigned char)keep;
+      }
+      ++n;
+    }
+  }
+  return n;
+}
+
+/* out = d restricted to keep[], renormalised */
+static void nucleus_apply(const double *d, int V, const unsigned char *keep, double *out) {
+  double mass = 0.0;
+  for (int v = 0; v < V; ++v)
+    if (keep[v]) mass += d[v];
+  for (int v = 0; v < V; ++v) out[v] = keep[v] ? d[v] / mass : 0.0;
+}
+
+/* Scratch for node_eval: softmax rows, residual, top-p rows and nuclei. */
+typedef struct {
+  double *p, *qd, *r, *fp, *fq, *vp, *vq, *sorted;
+  unsigned char *keeps_p, *keeps_q;
+} verify_scratch;
+
+static void scratch_free(verify_scratch *s) {
+  free(s->p); free(s->qd); free(s->r); free(s->fp); free(s->fq); free(s->vp); free(s->vq);
+  free(s->sorted); free(s->keeps_p); free(s->keeps_q);
+}
+
+static int scratch_alloc(verify_scratch *s, int V) {
+  const size_t vb = sizeof(double) * (size_t)V;
+  const size_t kb = (size_t)NUCLEUS_MAX_ALT * (size_t)V;
+  s->p = (double *)malloc(vb); s->qd = (double *)malloc(vb); s->r = (double *)malloc(vb);
+  s->fp = (double *)malloc(vb); s->fq = (double *)malloc(vb);
+  s->vp = (double *)malloc(vb); s->vq = (double *)malloc(vb); s->sorted = (double *)malloc(vb);
+  s->keeps_p = (unsigned char *)malloc(kb); s->keeps_q = (unsigned char *)malloc(kb);
+  if (!s->p || !s->qd || !s->r || !s->fp || !s->fq || !s->vp || !s->vq || !s->sorted ||
+      !s->keeps_p || !s->keeps_q) {
+    scratch_free(s);
+    return 0;
+  }
+  return 1;
+}
+
+/* An entry within twice the value band of tau, at a node where d has a value
+ * other than tau that close: a float32 implementation that decides
+ * membership by the entry's own float value may see the two in either order,
+ * so a decision that involves the entry is close. */
+static int near_tau(const double *d, int V, double tau, int x) {
+  const double w = 2.0 * NUCLEUS_VALUE_BAND * tau;
+  if (fabs(d[x] - tau) > w) return 0;
+  for (int y = 0; y < V; ++y)
+    if (d[y] != tau && fabs(d[y] - tau) <= w) return 1;
+  return 0;
+}
+
+/* The decisions at node u (request-local) of request b: greedy, stochastic,
+ * or stochastic on the top_p nuclei (top_p < 1). */
+static node_outcome node_eval(const float *lrow, const float *drow, int V, int greedy,
+                              double temp, double top_p, const int32_t *par, const int32_t *tok,
+                              int n, int u, int b, uint64_t seed, double band,
+                              verify_scratch *s) {
+  if (greedy) {
+    node_outcome o = {-1, argmax_f(lrow, V), 0, INFINITY, 0};
+    for (int c = u + 1; c < n; ++c)
+      if (par[c] == u && tok[c] == o.token) { o.next = c; break; }
+    return o;
+  }
+  softmax_t(lrow, V, temp, s->p);
+  softmax_t(drow, V, temp, s->qd);
+  if (!(top_p < 1.0)) return node_decide(s->p, s->qd, s->r, V, par, tok, n, u, b, seed, band);
+
+  int has_child = 0;
+  for (int c = u + 1; c < n; ++c) has_child |= par[c] == u;
+  double tau_p = 0.0, tau_q = 0.0;
+  const int np = nucleus_alternatives(s->p, V, top_p, s->sorted, s->keeps_p, &tau_p);
+  int nq = 1;
+  if (has_child) {
+    nq = nucleus_alternatives(s->qd, V, top_p, s->sorted, s->keeps_q, &tau_q);
+  } else {
+    memset(s->keeps_q, 1, (size_t)V);   /* a leaf never reads q */
+  }
+  nucleus_apply(s->p, V, s->keeps_p, s->fp);
+  nucleus_apply(s->qd, V, s->keeps_q, s->fq);
+  node_outcome o = node_decide(s->fp, s->fq, s->r, V, par, tok, n, u, b, seed, band);
+
+  /* fragile: too many plausible nuclei to compare, or two that decide differently */
+  int fragile = np < 0 || nq < 0 || np * nq > 256;
+  for (int i = 0; i < np && !fragile; ++i)
+    for (int j = 0; j < nq && !fragile; ++j) {
+      if (i == 0 && j == 0) continue;
+      nucleus_apply(s->p, V, s->keeps_p + (size_t)i * V, s->vp);
+      nucleus_apply(s->qd, V, s->keeps_q + (size_t)j * V, s->vq);
+      const node_outcome alt = node_decide(s->vp, s->vq, s->r, V, par, tok, n, u, b, seed, band);
+      fragile = alt.next != o.next || (alt.next < 0 && alt.token != o.token);
+    }
+  if (fragile) {
+    ++o.ties;
+    ++o.n_close;
+    o.margin = 0.0;
+  }
+  /* decisions that involve an entry near tau (tested children, the drawn token) */
+  for (int c = u + 1; c < n; ++c) {
+    if (par[c] != u) continue;
+    const int x = tok[c];
+    o.n_close += near_tau(s->p, V, tau_p, x) || (has_child && near_tau(s->qd, V, tau_q, x));
+    if (c == o.next) break;
+  }
+  if (o.next < 0)
+    o.n_close += near_tau(s->p, V, tau_p, o.token) || (has_child && near_tau(s->qd, V, tau_q, o.token));
+  return o;
+}
+
+/* Validation of request b for verification; *n_out receives its node count. */
+static int verify_request_status(const int32_t *tokens, const int32_t *parents,
+                                 const int32_t *offsets, int B, int T, int V, int W, int b,
+                                 int *n_out) {
+  int n = 0;
+  int st = check_request(offsets, B, T, b, &n);
+  if (st != OR_OK) return st;
+  const int32_t *par = parents + offsets[b];
+  const int32_t *tok = tokens + offsets[b];
+  st = check_parents(par, n);
+  if (st != OR_OK) return st;
+  for (int i = 1; i < n; ++i)
+    if (tok[i] < 0 || tok[i] >= V) return OR_ERR_TOKEN;
+  /* the output rows must hold the deepest possible path */
+  int maxd = 0;
+  for (int i = 0; i < n; ++i) {
+    int d = 0;
+    for (int a = i; par[a] != -1; a = par[a]) ++d;
+    if (d > maxd) maxd = d;
+  }
+  if (maxd + 1 > W) return OR_ERR_TREE;
+  *n_out = n;
+  return OR_OK;
 }
 
 static int tree_verify_impl(const float *target_logits, const float *draft_logits,
@@ -403,7 +591,47 @@ static int tree_verify_impl(const float *target_logits, const float *draft_logit
                             const int32_t *offsets, int B, int T, int V, float temperature,
                             double top_p, uint64_t seed, int32_t *accept_len,
                             int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
-                            int max_depth_plus1, int32_t *status);
+                            int max_depth_plus1, int32_t *status) {
+  if (B < 1 || T < 1 || V < 1 || max_depth_plus1 < 1) return OR_ERR_SHAPE;
+  const int greedy = !(temperature > 0.0f);
+  if (!greedy && draft_logits == NULL) return OR_ERR_SHAPE;
+  const int W = max_depth_plus1;
+  verify_scratch s;
+  if (!scratch_alloc(&s, V)) return OR_ERR_SHAPE;
+
+  for (int b = 0; b < B; ++b) {
+    int n = 0;
+    const int st = verify_request_status(tokens, parents, offsets, B, T, V, W, b, &n);
+    status[b] = st;
+    if (st != OR_OK) continue;
+    const int32_t *par = parents + offsets[b];
+    const int32_t *tok = tokens + offsets[b];
+    int32_t *pn = path_nodes + (size_t)b * W;
+    int32_t *ot = out_tokens + (size_t)b * W;
+    for (int j = 0; j < W; ++j) pn[j] = ot[j] = -1;
+    int ties = 0, acc = 0, u = 0;
+    pn[0] = 0;
+    for (;;) {
+      const size_t row = (size_t)(offsets[b] + u) * V;
+      const node_outcome o =
+          node_eval(target_logits + row, greedy ? NULL : draft_logits + row, V, greedy,
+                    (double)temperature, top_p, par, tok, n, u, b, seed, TIE_BAND, &s);
+      ties += o.ties;
+      if (o.next < 0) {
+        ot[acc] = o.token;
+        break;
+      }
+      ot[acc] = tok[o.next];
+      ++acc;
+      pn[acc] = o.next;
+      u = o.next;
+    }
+    accept_len[b] = acc;
+    near_ties[b] = ties;
+  }
+  scratch_free(&s);
+  return OR_OK;
+}
 
 int oracle_tree_verify(const float *target_logits, const float *draft_logits,
                        const int32_t *tokens, const int32_t *parents,
@@ -418,8 +646,7 @@ int oracle_tree_verify(const float *target_logits, const float *draft_logits,
 
 /* The same walk with the target and draft distributions each filtered to
  * their top_p nucleus first (top_p >= 1: no filter; greedy is unaffected).
- * A node whose nucleus boundary is a near-tie counts one near-tie when the
- * walk visits it. */
+ * A visited node that is fragile (see above) counts one near-tie. */
 int oracle_tree_verify_top_p(const float *target_logits, const float *draft_logits,
                              const int32_t *tokens, const int32_t *parents,
                              const int32_t *offsets, int B, int T, int V, float temperature,
@@ -432,114 +659,68 @@ int oracle_tree_verify_top_p(const float *target_logits, const float *draft_logi
                           max_depth_plus1, status);
 }
 
-static int tree_verify_impl(const float *target_logits, const float *draft_logits,
-                            const int32_t *tokens, const int32_t *parents,
-                            const int32_t *offsets, int B, int T, int V, float temperature,
-                            double top_p, uint64_t seed, int32_t *accept_len,
-                            int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
-                            int max_depth_plus1, int32_t *status) {
-  if (B < 1 || T < 1 || V < 1 || max_depth_plus1 < 1) return OR_ERR_SHAPE;
+/* Per-node decisions, for the parity tests.  Every decision at a node
+ * depends only on that node's rows, its children and its own uniforms, not
+ * on how the walk reached it, so each node can be evaluated alone.  For every
+ * global node t of a valid request with want[t] != 0 (want may be NULL: all
+ * nodes): next[t] = the accepted child (request-local) or -1, token[t] = the
+ * emitted token when next[t] == -1, margin[t] = the smallest distance of a
+ * decision there from its threshold (infinite for greedy; 0 for a fragile
+ * top-p node), n_close[t] = its decisions within `band` (top-p: plus those
+ * that involve an entry near tau).  Nodes not evaluated get next = -2.
+ * status[b] as oracle_tree_verify (max_depth_plus1 = W). */
+int oracle_verify_nodes(const float *target_logits, const float *draft_logits,
+                        const int32_t *tokens, const int32_t *parents, const int32_t *offsets,
+                        int B, int T, int V, float temperature, double top_p, uint64_t seed,
+                        int max_depth_plus1, double band, const uint8_t *want, int32_t *next,
+                        int32_t *token, double *margin, int32_t *n_close, int32_t *status) {
+  if (B < 1 || T < 1 || V < 1 || max_depth_plus1 < 1 || !(top_p > 0.0)) return OR_ERR_SHAPE;
   const int greedy = !(temperature > 0.0f);
   if (!greedy && draft_logits == NULL) return OR_ERR_SHAPE;
-  const double temp = (double)temperature;
-  const int W = max_depth_plus1;
-  const size_t vb = sizeof(double) * (size_t)V;
-  double *p = (double *)malloc(vb), *qd = (double *)malloc(vb), *r = (double *)malloc(vb);
-  /* top-p: filtered rows, one alternative pair, sort scratch, thresholds */
-  double *fp = (double *)malloc(vb), *fq = (double *)malloc(vb);
-  double *vp = (double *)malloc(vb), *vq = (double *)malloc(vb), *sorted = (double *)malloc(vb);
-  double cuts_p[NUCLEUS_MAX_CUTS], cuts_q[NUCLEUS_MAX_CUTS];
-  if (!p || !qd || !r || !fp || !fq || !vp || !vq || !sorted) {
-    free(p); free(qd); free(r); free(fp); free(fq); free(vp); free(vq); free(sorted);
-    return OR_ERR_SHAPE;
+  for (int t = 0; t < T; ++t) {
+    next[t] = -2;
+    token[t] = -1;
+    margin[t] = INFINITY;
+    n_close[t] = 0;
   }
-
+  verify_scratch s;
+  if (!scratch_alloc(&s, V)) return OR_ERR_SHAPE;
   for (int b = 0; b < B; ++b) {
     int n = 0;
-    int st = check_request(offsets, B, T, b, &n);
-    const int32_t *par = parents + (st == OR_OK ? offsets[b] : 0);
-    const int32_t *tok = tokens + (st == OR_OK ? offsets[b] : 0);
-    if (st == OR_OK) st = check_parents(par, n);
-    if (st == OR_OK) {
-      for (int i = 1; i < n; ++i)
-        if (tok[i] < 0 || tok[i] >= V) st = OR_ERR_TOKEN;
+    status[b] = verify_request_status(tokens, parents, offsets, B, T, V, max_depth_plus1, b, &n);
+    if (status[b] != OR_OK) continue;
+    const int32_t *par = parents + offsets[b];
+    const int32_t *tok = tokens + offsets[b];
+    for (int u = 0; u < n; ++u) {
+      const int t = offsets[b] + u;
+      if (want && !want[t]) continue;
+      const size_t row = (size_t)t * V;
+      const node_outcome o =
+          node_eval(target_logits + row, greedy ? NULL : draft_logits + row, V, greedy,
+                    (double)temperature, top_p, par, tok, n, u, b, seed, band, &s);
+      next[t] = o.next;
+      token[t] = o.next < 0 ? o.token : -1;
+      margin[t] = o.margin;
+      n_close[t] = o.n_close;
     }
-    if (st == OR_OK) {
-      /* the output rows must hold the deepest possible path */
-      int maxd = 0;
-      for (int i = 0; i < n; ++i) {
-        int d = 0;
-        for (int a = i; par[a] != -1; a = par[a]) ++d;
-        if (d > maxd) maxd = d;
-      }
-      if (maxd + 1 > W) st = OR_ERR_TREE;
-    }
-    status[b] = st;
-    if (st != OR_OK) continue;
-
-    int32_t *pn = path_nodes + (size_t)b * W;
-    int32_t *ot = out_tokens + (size_t)b * W;
-    for (int j = 0; j < W; ++j) pn[j] = ot[j] = -1;
-    int ties = 0, acc = 0;
-    int u = 0;
-    pn[0] = 0;
-    for (;;) {
-      const float *lrow = target_logits + (size_t)(offsets[b] + u) * V;
-      int next = -1;
-      if (greedy) {
-        int a = argmax_f(lrow, V);
-        for (int c = u + 1; c < n; ++c)
-          if (par[c] == u && tok[c] == a) { next = c; break; }
-        if (next < 0) { ot[acc] = a; break; }
-      } else {
-        const float *drow = draft_logits + (size_t)(offsets[b] + u) * V;
-        softmax_t(lrow, V, temp, p);
-        softmax_t(drow, V, temp, qd);
-        int token = -1;
-        if (top_p < 1.0) {
-          int has_child = 0;
-          for (int c = u + 1; c < n; ++c) has_child |= par[c] == u;
-          const int np = nucleus_cuts(p, V, top_p, sorted, cuts_p);
-          const int nq = has_child ? nucleus_cuts(qd, V, top_p, sorted, cuts_q) : 1;
-          if (!has_child) cuts_q[0] = 0.0;   /* a leaf never reads q */
-          nucleus_apply(p, V, cuts_p[0], fp);
-          if (has_child) nucleus_apply(qd, V, cuts_q[0], fq);
-          next = node_decide(fp, fq, r, V, par, tok, n, u, b, seed, &token, &ties);
-          if (np < 0 || nq < 0 || np * nq > NUCLEUS_MAX_CUTS * 4) {
-            ++ties;   /* too many plausible nuclei to compare */
-          } else {
-            int differs = 0;
-            for (int i = 0; i < np && !differs; ++i)
-              for (int j = 0; j < nq && !differs; ++j) {
-                if (i == 0 && j == 0) continue;
-                int tk = -1, scratch_ties = 0;
-                nucleus_apply(p, V, cuts_p[i], vp);
-                if (has_child) nucleus_apply(qd, V, cuts_q[j], vq);
-                const int nx = node_decide(vp, has_child ? vq : fq, r, V, par, tok, n, u, b, seed,
-                                           &tk, &scratch_ties);
-                differs = nx != next || (nx < 0 && tk != token);
-              }
-            ties += differs;
-          }
-        } else {
-          next = node_decide(p, qd, r, V, par, tok, n, u, b, seed, &token, &ties);
-        }
-        if (next < 0) {
-          ot[acc] = token;
-          break;
-        }
-      }
-      ot[acc] = tok[next];
-      ++acc;
-      pn[acc] = next;
-      u = next;
-    }
-    accept_len[b] = acc;
-    near_ties[b] = ties;
   }
-  free(p); free(qd); free(r); free(fp); free(fq); free(vp); free(vq); free(sorted);
+  scratch_free(&s);
   return OR_OK;
 }
+
+/* The plausible top-p nuclei of one distribution, for the tests that pin
+ * their enumeration: writes the exact tau and the keep-flags of every
+ * plausible nucleus (keeps[NUCLEUS_MAX_ALT][V]); returns their number or -1. */
+int oracle_nucleus_alternatives(const double *d, int V, double top_p, unsigned char *keeps,
+                                double *tau) {
+  double *sorted = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!sorted) return -2;
+  const int n = nucleus_alternatives(d, V, top_p, sorted, keeps, tau);
+  free(sorted);
+  return n;
+}
+
+int oracle_nucleus_max_alternatives(void) { return NUCLEUS_MAX_ALT; }
 
 /* ------------------------------------------------------------------------ */
 /* Depth-first KV-cache update [news]: after verification request b commits  */
@@ -598,7 +779,9 @@ int oracle_kv_compact(uint8_t *cache, int elem_bytes, int B, int H, int S_cap, i
 /*   T == 0: q = softmax(draft); the children are the `width` most likely    */
 /*           tokens in order (ties to the lower index).                      */
 /* score of child j = parent score + log q(token).  ties[f][j] = 1 when a    */
-/* draw lay within 1e-6 of an inverse-CDF boundary.                          */
+/* draw lay within 1e-6 of an inverse-CDF boundary; gaps[f][j] (may be NULL)  */
+/* is the draw's relative distance from the nearer boundary (infinite for a  */
+/* greedy child).                                                            */
 /* ------------------------------------------------------------------------ */
 static double oracle_uniform4(uint64_t seed, int64_t c0, int64_t c1, int64_t c2, int64_t c3) {
   uint64_t ctr[4] = {(uint64_t)c0, (uint64_t)c1, (uint64_t)c2, (uint64_t)c3};
@@ -610,7 +793,8 @@ static double oracle_uniform4(uint64_t seed, int64_t c0, int64_t c1, int64_t c2,
 
 int oracle_tree_expand(const float *draft, const double *parent_scores, const int32_t *node_ids,
                        const int32_t *reqs, int F, int V, int width, double temperature,
-                       uint64_t seed, int32_t *tokens, double *scores, int32_t *ties) {
+                       uint64_t seed, int32_t *tokens, double *scores, int32_t *ties,
+                       double *gaps) {
   if (F < 1 || V < 1 || width < 1 || width > V || !(temperature >= 0.0)) return OR_ERR_SHAPE;
   const double t = temperature > 0.0 ? temperature : 1.0;
   double *w = (double *)malloc(sizeof(double) * (size_t)V);
@@ -626,9 +810,10 @@ int oracle_tree_expand(const float *draft, const double *parent_scores, const in
     }
     const double log_s = log(s);
     for (int j = 0; j < width; ++j) {
-      int tok, tie = 0;
+      int tok;
+      double gap = INFINITY;
       if (temperature > 0.0) {
-        tok = sample_inverse_cdf(w, V, oracle_uniform4(seed, node_ids[f], reqs[f], 2, j), &tie);
+        tok = sample_inverse_cdf(w, V, oracle_uniform4(seed, node_ids[f], reqs[f], 2, j), &gap);
       } else {
         /* the j-th most likely token: the best one not yet taken */
         tok = -1;
@@ -640,7 +825,8 @@ int oracle_tree_expand(const float *draft, const double *parent_scores, const in
       }
       tokens[(size_t)f * width + j] = tok;
       scores[(size_t)f * width + j] = parent_scores[f] + ((double)row[tok] - m) / t - log_s;
-      ties[(size_t)f * width + j] = tie;
+      ties[(size_t)f * width + j] = gap < TIE_BAND;
+      if (gaps) gaps[(size_t)f * width + j] = gap;
     }
   }
   free(w);

@@ -2,9 +2,11 @@
 binding and the oracle on the same seeded inputs, and compare them with the
 bars the method's correctness statement fixes:
   * mask, depth, greedy accept length and tokens: bit-exact;
-  * stochastic decisions: bit-exact except requests where either side saw a
-    near-tie (|u - alpha| < 1e-6, or an inverse-CDF draw within 1e-6 of a
-    bucket edge), whose results must still be valid paths;
+  * stochastic decisions: every decision on the GPU's walk equals the
+    oracle's decision at that node, except where the oracle's exact (fp64)
+    margin there is below BAND; such exemptions are counted and bounded, and
+    the GPU may only report a near-tie where the oracle finds a decision
+    within BAND (the GPU's own flag exempts nothing);
   * attention: max|d| <= 1e-2 max|ref| and relative error <= 2e-2 wherever
     |ref| >= 1e-2 max|ref|."""
 import numpy as np
@@ -113,23 +115,101 @@ def oracle_verify(w, seed, W=None, temperature=None, top_p=1.0):
                               top_p=top_p)
 
 
-def assert_verify_match(g, o, parents, tokens, offsets, what=""):
-    """Bit-exact on every request without a near-tie on either side; the
-    near-tie requests must still return a valid accepted path."""
+# A float32 implementation of the accept test and the inverse-CDF draw is
+# accurate to a few 1e-6 of the exact threshold (fp32 sums over up to 1.5e5
+# entries, ~4-ulp exponentials, the closed-form residual); a decision whose
+# exact fp64 distance from its threshold is below BAND may legitimately be
+# taken the other way.  BAND is 10x the near-tie band of the method.
+BAND = 1e-5
+
+
+def walk_nodes(res, offsets):
+    """Global node ids on each request's walk: the root, the accepted nodes
+    (the last one is where the walk stopped)."""
+    out = []
+    for b in range(len(offsets) - 1):
+        if res["status"][b] != 0:
+            out.append([])
+            continue
+        a = int(res["accept_len"][b])
+        out.append([int(offsets[b]) + int(u) for u in res["path_nodes"][b][:a + 1]])
+    return out
+
+
+def assert_verify_match(g, o, parents, tokens, offsets, what="", nodes=None, max_exempt=1):
+    """Compare a GPU verification result ``g`` with the oracle's walk ``o``.
+
+    ``nodes`` is the oracle's per-node evaluation (``oracle.verify_nodes``)
+    covering every node on both walks.  Each decision on the GPU's walk must
+    equal the oracle's decision at that node unless the oracle's margin there
+    is below BAND (an exemption; at most ``max_exempt`` over the call); the
+    GPU's walk must be a valid path; the GPU's near-tie count on a request
+    must not exceed the number of decisions the oracle finds within BAND on
+    that walk.  Returns the number of exemptions."""
     np.testing.assert_array_equal(g["status"], o["status"], err_msg=what)
-    ok = o["status"] == 0
-    tie = (g["near_ties"] > 0) | (o["near_ties"] > 0)
-    exact = ok & ~tie
-    np.testing.assert_array_equal(g["accept_len"][exact], o["accept_len"][exact], err_msg=what)
-    np.testing.assert_array_equal(g["path_nodes"][exact], o["path_nodes"][exact], err_msg=what)
-    np.testing.assert_array_equal(g["out_tokens"][exact], o["out_tokens"][exact], err_msg=what)
-    for b in np.nonzero(ok & tie)[0]:
+    off = np.asarray(offsets)
+    exempt = 0
+    ow = walk_nodes(o, off)
+    gw = walk_nodes(g, off)
+    for b in np.nonzero(o["status"] == 0)[0]:
+        lo = int(off[b])
+        # the oracle's walk follows its own per-node decisions
+        for j, t in enumerate(ow[b]):
+            nxt = ow[b][j + 1] - lo if j + 1 < len(ow[b]) else -1
+            assert nodes["next"][t] == nxt, f"{what}: oracle walk / node decisions, request {b}"
+            if nxt < 0:
+                assert nodes["token"][t] == o["out_tokens"][b, j], what
         a = int(g["accept_len"][b])
-        lo = int(offsets[b])
         pn = g["path_nodes"][b]
-        assert pn[0] == 0
-        for j in range(1, a + 1):
-            assert parents[lo + pn[j]] == pn[j - 1], what
-            assert g["out_tokens"][b, j - 1] == tokens[lo + pn[j]], what
-        assert (pn[a + 1:] == -1).all() and (g["out_tokens"][b, a + 1:] == -1).all()
-    return int(tie.sum())
+        assert pn[0] == 0, what
+        assert (pn[a + 1:] == -1).all() and (g["out_tokens"][b, a + 1:] == -1).all(), what
+        support = 0
+        for j, t in enumerate(gw[b]):
+            assert nodes["next"][t] != -2, f"{what}: node {t} not evaluated"
+            if j < a:
+                nxt = int(pn[j + 1])
+                assert parents[lo + nxt] == pn[j], f"{what}: request {b} path is not a tree path"
+                assert g["out_tokens"][b, j] == tokens[lo + nxt], what
+                same = nodes["next"][t] == nxt
+            else:
+                same = nodes["next"][t] == -1 and nodes["token"][t] == g["out_tokens"][b, j]
+            if not same:
+                assert nodes["margin"][t] < BAND, (
+                    f"{what}: request {b} node {t - lo}: GPU decision differs from the oracle's, "
+                    f"oracle margin {nodes['margin'][t]:.3e} >= {BAND}")
+                exempt += 1
+                support += 1 << 20     # the GPU took other decisions at this node
+            support += int(nodes["n_close"][t])
+        assert g["near_ties"][b] <= support, (
+            f"{what}: request {b}: GPU reports {g['near_ties'][b]} near-ties, the oracle finds "
+            f"{support} decisions within {BAND} on that walk")
+    assert exempt <= max_exempt, f"{what}: {exempt} exempted decisions > {max_exempt}"
+    return exempt
+
+
+def oracle_nodes_for(g, o, target, draft, tokens, parents, offsets, temperature, seed, W, top_p=1.0):
+    """The oracle's per-node decisions on every node of both walks."""
+    want = np.zeros(np.asarray(target).shape[0], np.uint8)
+    for walk in walk_nodes(o, offsets) + walk_nodes(g, offsets):
+        want[walk] = 1
+    return oracle.verify_nodes(target, draft if temperature > 0 else None, tokens, parents, offsets,
+                               temperature, seed, W, top_p=top_p, band=BAND, want=want)
+
+
+def check_verify(w, seed, W=None, temperature=None, top_p=1.0, max_exempt=1, what=None, **kw):
+    """GPU verification of workload ``w`` against the oracle (walk and
+    per-node decisions).  Returns (gpu result, oracle result, exemptions)."""
+    temp = w.temperature if temperature is None else temperature
+    W = (w.max_depth + 1) if W is None else W
+    g = gpu_verify(w, seed, W=W, temperature=temp, top_p=top_p, **kw)
+    target = kw.get("target", w.target_logits)
+    tokens = kw.get("tokens", w.tokens)
+    parents = kw.get("parents", w.parents)
+    offsets = kw.get("offsets", w.offsets)
+    draft = w.draft_logits if kw.get("draft", "auto") == "auto" else kw["draft"]
+    o = oracle.tree_verify(target, draft if temp > 0 else None, tokens, parents, offsets, temp, seed,
+                           W, top_p=top_p)
+    nodes = oracle_nodes_for(g, o, target, draft, tokens, parents, offsets, temp, seed, W, top_p)
+    what = what or f"{w.name} seed {seed} T={temp} top_p={top_p}"
+    ex = assert_verify_match(g, o, parents, tokens, offsets, what, nodes=nodes, max_exempt=max_exempt)
+    return g, o, ex

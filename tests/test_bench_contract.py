@@ -34,3 +34,25 @@ def test_reference_arm_other_workload_and_greedy():
     d = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][0])
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["config"]["workload"].startswith("tiny:") and d["config"]["workload"].endswith("greedy")
+
+
+def test_gpus_two_starts_two_ranks():
+    """--gpus 2 without torchrun's environment starts two local ranks; the
+    reference arm runs on rank 0 only and its line reports both GPUs."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["OMP_NUM_THREADS"] = "1"
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "1", "--workload", "tiny"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_world_size_must_agree_with_gpus():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "1",
+                          "--steps", "1", "--warmup", "1"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert out.returncode != 0 and "disagrees" in out.stderr

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import token_tree_verification_gb300 as ttv
-from parity import dev
+from parity import BAND, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -46,12 +46,22 @@ def test_sampled_expansion(V, width, T):
     ps = np.zeros(F, np.float32)
     nodes, reqs = rng.integers(0, 128, F), rng.integers(0, 4, F)
     tg, sg, tiesg = _expand_gpu(d, ps, nodes, reqs, width, T, 77)
-    to, so, tieso = oracle.tree_expand(d, ps.astype(np.float64), nodes, reqs, width, T, 77)
-    exact = (tiesg == 0) & (tieso == 0)
-    assert exact.mean() > 0.9
-    np.testing.assert_array_equal(tg[exact], to[exact])
-    np.testing.assert_allclose(sg[exact], so[exact], rtol=0, atol=2e-4)
+    to, so, tieso, gap = oracle.tree_expand(d, ps.astype(np.float64), nodes, reqs, width, T, 77,
+                                            with_gaps=True)
+    assert (tiesg >= 0).all(), "an exchange between the CTAs of a row timed out"
     assert ((tg >= 0) & (tg < V)).all()
+    # A draw may differ from the oracle's only where the oracle's exact gap to
+    # the nearer inverse-CDF boundary is below BAND (at most one per case),
+    # and the GPU may flag a near-tie only where that gap is below BAND.  (A
+    # draw that lands on an entry of mass below 1e-6 of the total is a
+    # near-tie by definition; with V = 131077 at T = 0.8 such entries carry
+    # enough mass in total to be drawn now and then.)
+    differ = tg != to
+    assert (gap[differ] < BAND).all(), gap[differ]
+    assert (gap[tiesg != 0] < BAND).all(), gap[tiesg != 0]
+    assert differ.sum() <= 1
+    same = ~differ
+    np.testing.assert_allclose(sg[same], so[same], rtol=0, atol=2e-4)
 
 
 def _prune_both(par, tok, sc32, off, keep):
@@ -93,7 +103,8 @@ def test_pruning_errors():
 
 def test_build_a_pruned_tree_level_by_level():
     """Width 5, depth 3, i.i.d. draft samples, pruned to 64 nodes: the GPU and
-    the oracle build the same tree (parents, tokens) when no draw is a tie."""
+    the oracle build the same tree (parents, tokens) unless a draw differs,
+    which it may only within BAND of an inverse-CDF boundary."""
     rng = np.random.default_rng(11)
     V, w, depth, keep, T, seed = 4000, 5, 3, 64, 0.7, 5
     par_g, tok_g, sc_g = [-1], [0], [0.0]
@@ -104,9 +115,11 @@ def test_build_a_pruned_tree_level_by_level():
         d = (rng.standard_normal((len(frontier), V)) * 3).astype(np.float32)
         tg, sg, tiesg = _expand_gpu(d, np.array([sc_g[u] for u in frontier], np.float32), frontier,
                                     np.zeros(len(frontier)), w, T, seed)
-        to, so, tieso = oracle.tree_expand(d, [sc_o[u] for u in frontier], frontier,
-                                           np.zeros(len(frontier)), w, T, seed)
-        any_tie |= bool(tiesg.any() or tieso.any())
+        to, so, tieso, gap = oracle.tree_expand(d, [sc_o[u] for u in frontier], frontier,
+                                                np.zeros(len(frontier)), w, T, seed, with_gaps=True)
+        assert (tiesg >= 0).all()
+        assert (gap[tg != to] < BAND).all()
+        any_tie |= bool((tg != to).any())
         nxt = []
         for f, u in enumerate(frontier):
             for j in range(w):

@@ -5,7 +5,8 @@ outputs.
 
 It must agree exactly with spec_tree_verify (same kernels, integer outputs)
 on consecutive calls, since every call reuses the array and finds the
-previous call's contents in it.  This file is collected last so that a run
+previous call's contents in it, and with the oracle decision by decision,
+as spec_tree_verify does.  This file is collected last so that a run
 stopping at the first failure has run every other test before it."""
 import ctypes
 
@@ -13,7 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from parity import dev, gpu_verify
+import oracle
+from parity import assert_verify_match, dev, gpu_verify, oracle_nodes_for
 from token_tree_verification_gb300 import binding, synthetic
 
 SCRATCH_BYTES = 256 * 1024
@@ -79,3 +81,10 @@ def test_static_matches_workspace_entry_point_on_consecutive_calls():
         for k in ("status", "accept_len", "path_nodes", "out_tokens", "near_ties"):
             np.testing.assert_array_equal(got[k], ref[k], err_msg=f"{name} T={temp}: {k}")
         assert (got["status"] == 0).all()
+        W = w.max_depth + 1
+        draft = w.draft_logits if temp > 0 else None
+        o = oracle.tree_verify(w.target_logits, draft, w.tokens, w.parents, w.offsets, temp, seed, W)
+        nodes = oracle_nodes_for(got, o, w.target_logits, draft, w.tokens, w.parents, w.offsets,
+                                 temp, seed, W)
+        assert_verify_match(got, o, w.parents, w.tokens, w.offsets, f"static {name} T={temp}",
+                            nodes=nodes)

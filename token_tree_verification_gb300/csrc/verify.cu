@@ -376,13 +376,13 @@ extern "C" size_t spec_tree_verify_workspace_size(int B, int T, int V) {
   return align256(sizeof(uint32_t) * (B + 1)) + align256(sizeof(int32_t) * T) * 2;
 }
 
-namespace {
+namespace spec {
 int verify_entry(const float *target_logits, const float *draft_logits, const int32_t *tokens,
                  const int32_t *parents, const int32_t *tree_offsets, int B, int T, int V,
                  float temperature, float top_p, uint64_t seed, int32_t *accept_len,
                  int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
-                 void *workspace, size_t workspace_bytes, int32_t *status, void *stream) {
-  using namespace spec;
+                 void *workspace, size_t workspace_bytes, int32_t *status, void *stream,
+                 bool clear_workspace) {
   if (!target_logits || !tokens || !parents || !tree_offsets || !accept_len || !path_nodes ||
       !out_tokens || !near_ties || !status)
     return SPEC_ERR_NULL;
@@ -425,6 +425,10 @@ int verify_entry(const float *target_logits, const float *draft_logits, const in
   args.out_tokens = out_tokens;
   args.near_ties = near_ties;
   args.status = status;
+  // Every host-side check has passed: nothing was enqueued before this point.
+  if (clear_workspace &&
+      cudaMemsetAsync(workspace, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   char *ws = static_cast<char *>(workspace);
   args.done = reinterpret_cast<uint32_t *>(ws);
   ws += align256(sizeof(uint32_t) * (B + 1));
@@ -455,7 +459,7 @@ int verify_entry(const float *target_logits, const float *draft_logits, const in
   if (cudaLaunchKernelEx(&cfg, tree_verify_cluster_kernel, args) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
-}  // namespace
+}  // namespace spec
 
 extern "C" int spec_tree_verify(const float *target_logits, const float *draft_logits,
                                 const int32_t *tokens, const int32_t *parents,
@@ -464,9 +468,9 @@ extern "C" int spec_tree_verify(const float *target_logits, const float *draft_l
                                 int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties,
                                 int max_depth_plus1, void *workspace, size_t workspace_bytes,
                                 int32_t *status, void *stream) {
-  return verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
-                      temperature, 1.f, seed, accept_len, path_nodes, out_tokens, near_ties,
-                      max_depth_plus1, workspace, workspace_bytes, status, stream);
+  return spec::verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
+                            temperature, 1.f, seed, accept_len, path_nodes, out_tokens, near_ties,
+                            max_depth_plus1, workspace, workspace_bytes, status, stream, false);
 }
 
 extern "C" int spec_tree_verify_top_p(const float *target_logits, const float *draft_logits,
@@ -477,7 +481,7 @@ extern "C" int spec_tree_verify_top_p(const float *target_logits, const float *d
                                       int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
                                       void *workspace, size_t workspace_bytes, int32_t *status,
                                       void *stream) {
-  return verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
-                      temperature, top_p, seed, accept_len, path_nodes, out_tokens, near_ties,
-                      max_depth_plus1, workspace, workspace_bytes, status, stream);
+  return spec::verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
+                            temperature, top_p, seed, accept_len, path_nodes, out_tokens, near_ties,
+                            max_depth_plus1, workspace, workspace_bytes, status, stream, false);
 }

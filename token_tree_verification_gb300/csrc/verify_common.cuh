@@ -381,6 +381,17 @@ static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, Tr
   if (ts.walk && tid < 32) walk_request(a, c.b, c.lo, c.n, ts.par, ts.tok);
 }
 
+// Host entry of spec_tree_verify / spec_tree_verify_top_p (verify.cu): checks
+// every argument on the host, then, when clear_workspace is set, zero-fills
+// the workspace's used bytes on `stream`, then launches.  Nothing is enqueued
+// when a check fails.
+int verify_entry(const float *target_logits, const float *draft_logits, const int32_t *tokens,
+                 const int32_t *parents, const int32_t *tree_offsets, int B, int T, int V,
+                 float temperature, float top_p, uint64_t seed, int32_t *accept_len,
+                 int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
+                 void *workspace, size_t workspace_bytes, int32_t *status, void *stream,
+                 bool clear_workspace);
+
 // greedy per-node kernel (verify_node.cu)
 int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream);
 
