@@ -835,9 +835,24 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def relaunch_ranks(n: int, argv: list) -> int:
+    """Run this script as ``n`` local ranks (one per GPU) under
+    torch.distributed.run on 127.0.0.1 and return its exit code; rank 0
+    prints the job's line."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of this node, one independent replica each; without torchrun's "
+                         "environment the script starts the ranks itself")
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
@@ -857,9 +872,16 @@ def main():
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
 
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: start the ranks under torch.distributed.run
+        raise SystemExit(relaunch_ranks(args.gpus, sys.argv[1:]))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"WORLD_SIZE={world} disagrees with --gpus {args.gpus}")
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if res is not None:
