@@ -2,7 +2,9 @@
 
 One step = the whole hot path over one batch: ancestor mask, tree attention
 (one attention layer over the request's KV prefix + tree), and verification
-(vocab softmax, acceptance walk, bonus token).  The workload is the
+(vocab softmax, acceptance walk, bonus token).  Verification depends on none
+of the other two, so it runs on a second branch of the step's CUDA graph,
+side by side with the mask and attention.  The workload is the
 LLaMA-7B-shaped tree-verify case: 1 request, 32 heads (MHA), head dim 128,
 bf16 KV prefix 2048, a width-5 depth-3 draft tree pruned to 64 nodes, vocab
 32000, stochastic verification at temperature 0.7.  Inputs are synthetic and
@@ -242,15 +244,31 @@ class Step:
                                     dl=None if dl is None else dl.clone()))
         self.max_prefix = int(w.prefix_lens.max())
         self.seed = seed
+        self.side = torch.cuda.Stream()
 
     def run(self, i: int, stream=None):
-        """Enqueue step i: mask, attention, verification."""
-        ttv, w, c = self.ttv, self.w, self.copies[i % len(self.copies)]
-        ttv.build_tree_mask(self.par, self.off, self.status, mask=self.mask, depth=self.depth, stream=stream)
-        ttv.tree_attn(c["q"], c["k"], c["v"], self.pl, self.off, self.mask, self.max_prefix,
-                      self.status, o=self.o, workspace=self.ws_attn, stream=stream)
-        ttv.tree_verify(c["tl"], c["dl"], self.tok, self.par, self.off, w.temperature,
-                        self.seed + i, self.W, self.status, self.ws, outputs=self.outs, stream=stream)
+        """Enqueue step i on ``stream`` (default: the current stream) over
+        input copy i."""
+        c = self.copies[i % len(self.copies)]
+        self.launch(c["q"], c["k"], c["v"], c["tl"], c["dl"], self.par, self.off, self.tok, self.pl,
+                    self.seed + i, self.outs, stream)
+
+    def launch(self, q, k, v, tl, dl, par, off, tok, pl, seed, outs, stream=None):
+        """One step: the mask then tree attention on ``stream``, and
+        verification on a second stream forked from it and joined back.
+        Verification reads only the logits and the tree, attention only Q, the
+        caches and the mask, so the two run side by side (under graph capture
+        the fork and join become two branches of the graph)."""
+        torch, ttv, w = self.torch, self.ttv, self.w
+        cur = torch.cuda.current_stream() if stream is None else stream
+        self.side.wait_stream(cur)
+        ttv.build_tree_mask(par, off, self.status, mask=self.mask, depth=self.depth, stream=cur)
+        ttv.tree_attn(q, k, v, pl, off, self.mask, self.max_prefix, self.status, o=self.o,
+                      workspace=self.ws_attn, stream=cur)
+        with torch.cuda.stream(self.side):
+            ttv.tree_verify(tl, dl, tok, par, off, w.temperature, seed, self.W, self.status, self.ws,
+                            outputs=outs, stream=self.side)
+        cur.wait_stream(self.side)
 
 
 def run_native(args, rank, world, local_rank):
@@ -718,11 +736,8 @@ def run_e2e(st, w, stream, steps):
     def compute(i):
         d = sets[i % 2]
         with torch.cuda.stream(stream):
-            ttv.build_tree_mask(d["par"], d["off"], st.status, mask=st.mask, depth=st.depth, stream=stream)
-            ttv.tree_attn(d["q"], d["k"], d["v"], d["pl"], d["off"], st.mask, st.max_prefix,
-                          st.status, o=st.o, workspace=st.ws_attn, stream=stream)
-            ttv.tree_verify(d["tl"], d.get("dl"), d["tok"], d["par"], d["off"], w.temperature,
-                            st.seed + i, st.W, st.status, st.ws, outputs=outs, stream=stream)
+            st.launch(d["q"], d["k"], d["v"], d["tl"], d.get("dl"), d["par"], d["off"], d["tok"],
+                      d["pl"], st.seed + i, outs, stream)
             free[i % 2].record(stream)
             out_host[i % 2].copy_(out_dev, non_blocking=True)
 

@@ -27,8 +27,11 @@
  *    that does not fit the cache, a bounded wait that ran out) are written to
  *    the caller's `status[b]` for request b with an atomic compare-and-swap
  *    from 0, so the first error sticks.  The kernels never write 0: the caller
- *    zero-fills `status` before a step and reads it after synchronising.  The
- *    outputs of a request with an error are left untouched.
+ *    zero-fills `status` before a step and reads it after synchronising.  A
+ *    call leaves the outputs of a request untouched when it finds an error
+ *    for that request itself; codes that other calls wrote into `status`
+ *    (which may run concurrently on other streams) do not affect it.  After
+ *    SPEC_ERR_TIMEOUT (never expected) the request's outputs are unspecified.
  *  - A batch is packed ragged: request b owns global nodes
  *    [tree_offsets[b], tree_offsets[b+1]) with tree_offsets[0] = 0 and
  *    tree_offsets[B] = T.  Node indices inside a request (parents, path

@@ -622,6 +622,8 @@ extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(D));
   args.scale_log2 = scale * 1.4426950408889634f;
   args.rows_per_cta = spec::kMmaRows;
+  // a single request holds T nodes; with max_prefix exact its key count is known
+  args.prefetch_keys = B == 1 ? max_prefix + T : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == SPEC_F32) {
     spec::tree_attn_f32_kernel<<<dim3(Hq, T), spec::kF32Threads, 0, st>>>(args);

@@ -23,6 +23,8 @@ struct AttnArgs {
   int B, T, Hq, Hkv, G, D, S_cap;
   float scale_log2;        // softmax scale * log2(e)
   int rows_per_cta;        // rows of one CTA (node-major, head-minor)
+  int prefetch_keys;       // > 0: the key count the host expects for a single request
+                           // (its L2 prefetch of the first tiles may start early)
 };
 
 // Geometry of request b as one CTA sees it.  Keys [0, L) are the prefix,

@@ -99,6 +99,21 @@ constexpr int kTcMaxSplits = 8;
 
 
 
+// L2 prefetch of one tile of a tensor map (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
                                             int c1, int c2) {
   asm volatile(
@@ -224,6 +239,25 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
+    if (a.prefetch_keys > 0) {
+      // One request whose key count the host knows: this split's first
+      // tiles, and its Q rows, are prefetched into L2 while the previous
+      // kernel still runs.  A prefetch only warms L2, which every write of
+      // the previous kernel updates, so it can never serve stale data; if the
+      // request's real key count differs, the prefetched lines are unused.
+      const int tiles = (a.prefetch_keys + kKeyTile - 1) / kKeyTile;
+      const int per = (tiles + CS - 1) / CS;
+      const int t0 = split * per;
+      const int nt = min(NS, min(t0 + per, tiles) - t0);
+      for (int i = 0; i < nt; ++i)
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_prefetch_l2_4d(&tmk, bx * 64, (t0 + i) * kKeyTile, g, 0);
+          tma_prefetch_l2_4d(&tmv, bx * 64, (t0 + i) * kKeyTile, g, 0);
+        }
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx) tma_prefetch_l2_3d(&tmq, bx * 64, g * a.G, rb * kTcRows / a.G);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(&s_tmem, C::kTmemCols);
@@ -523,15 +557,20 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     }
     if (!ok) s_timeout = 1;
     // ---- epilogue: O rows out of TMEM.  Every softmax warp waits for the
-    //      last P V before any thread reuses the K/V ring or the P buffers.
+    //      last P V before any thread reuses the K/V ring or the P buffers; a
+    //      thread whose waits ran out writes no shared memory (copies may
+    //      still land there).
     if (ntiles > 0) {
-      if (ok && !mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) s_timeout = 1;
+      if (ok && !mbar_wait(&bar_o[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
+        ok = false;
+        s_timeout = 1;
+      }
       __syncwarp();
       tc::fence_after_sync();
     }
 #pragma unroll
     for (int e = 0; e < kOC; ++e) o_keep[e] = 0.f;
-    if (lanes_live && ntiles > 0) tmem_load_cols<kOC>(trow + C::kColO + ocol, o_keep);
+    if (ok && lanes_live && ntiles > 0) tmem_load_cols<kOC>(trow + C::kColO + ocol, o_keep);
     // [64 rows][D] floats in the free P buffers; 16-byte chunks swizzled by
     // row so that eight consecutive rows hit eight different bank groups
     float *xo = reinterpret_cast<float *>(smem + C::kOffP);
@@ -539,14 +578,14 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       const int chunk = (ocol + e) >> 2;
       return reinterpret_cast<float4 *>(xo + srow * D) + (chunk ^ (srow & 7));
     };
-    if (PACKED && lo_lane && row_ok) {
+    if (ok && PACKED && lo_lane && row_ok) {
 #pragma unroll
       for (int e = 0; e < kOC; e += 4)
         *xo_at(e) = make_float4(o_keep[e], o_keep[e + 1], o_keep[e + 2], o_keep[e + 3]);
     }
     if (warp >= 3) x_l[part][srow] = l_part;
     named_bar_sync(2, 32 * C::kSoftmaxWarps);
-    if (owner && row_ok) {
+    if (ok && owner && row_ok) {
 #pragma unroll
       for (int q = 0; q < C::kParts; ++q) l_row += x_l[q][srow];
       if (PACKED) {
@@ -579,9 +618,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     __syncwarp();
     tc::tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (s_timeout && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
+  // A wait that ran out anywhere in the CTA: report it and write no output
+  // row of the block (with key splits, no CTA of the cluster writes one).
+  const bool timed_out = s_timeout != 0;
+  if (timed_out && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
   const float *stg = reinterpret_cast<const float *>(smem + C::kOffKV);
   if (CS == 1) {
+    if (timed_out) return;
     // ---- final rows, 8 bf16 per thread, consecutive threads on one row
     const int nv = rows_here * (D / 8);
     for (int idx = tid; idx < nv; idx += C::kThreads) {
@@ -615,6 +658,10 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   own_range(split, own0, own_n);
   float *recv = const_cast<float *>(stg) + rows_here * C::kStage;   // [CS][rpr][kStage]
   cluster_sync_all();
+  // Every CTA sends its rows even after a timeout (the byte counts complete
+  // the owners' barriers; the rows are then unused), and reads whether any
+  // CTA of the cluster timed out: every s_timeout is final after the barrier.
+  __shared__ int s_cluster_timeout;
   if (tid == 0) {
     if (own_n > 0) mbar_arrive_expect_tx(&bar_m, static_cast<uint32_t>((CS - 1) * own_n * C::kStage * 4));
     for (int r = 0; r < CS; ++r) {
@@ -624,9 +671,21 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       bulk_copy_s2s(peer_addr(recv + split * rpr * C::kStage, r), smem_addr(stg + r0 * C::kStage),
                     static_cast<uint32_t>(rn * C::kStage * 4), peer_addr(&bar_m, r));
     }
+    int any = timed_out ? 1 : 0;
+    for (int r = 0; r < CS; ++r)
+      if (r != split) any |= ld_peer_s32(peer_addr(&s_timeout, static_cast<uint32_t>(r)));
+    s_cluster_timeout = any;
   }
-  if (own_n > 0 && !mbar_wait(&bar_m, 0) && tid == 0) report(a.status, b, SPEC_ERR_TIMEOUT);
+  if (own_n > 0 && !mbar_wait(&bar_m, 0) && tid == 0) {
+    report(a.status, b, SPEC_ERR_TIMEOUT);
+    s_cluster_timeout = 1;
+  }
+  __syncthreads();
   cluster_arrive_relaxed();  // everything addressed to this CTA has arrived
+  if (s_cluster_timeout) {
+    cluster_wait();   // no CTA leaves while a copy may still read its rows
+    return;
+  }
   {
     constexpr int kE = D / 8;   // columns per task
     const int ntask = own_n * 8;

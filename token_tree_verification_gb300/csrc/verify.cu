@@ -252,7 +252,10 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
   // No CTA touches a peer's shared memory after this point: arrive now, wait
   // before exiting, so that no CTA leaves while a peer may still store to it.
   if (CS > 1) cluster_arrive_relaxed();
-  if (!ok && tid == 0) report(a.status, c.b, SPEC_ERR_TIMEOUT);
+  if (!ok) {
+    ts.timeout = 1;
+    if (tid == 0) report(a.status, c.b, SPEC_ERR_TIMEOUT);
+  }
 
   int writer = 0;  // the CTA of the group that publishes the node's results
   if (!c.err) {
@@ -337,6 +340,7 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
           if (lane == 0) {
             const bool tie = fabsf(target - cb0) < kTieBand * total || fabsf(target - cb1) < kTieBand * total;
             a.fallback[t] = (v0 + g0 + 32 * gw + L) | (tie ? (1 << 31) : 0);
+            ts.stop_fb = (v0 + g0 + 32 * gw + L) | (tie ? (1 << 31) : 0);
           }
         } else if (gw < 0 && tid == 0) {
           // rounding: the slice's last positive weight, on the boundary
@@ -349,6 +353,7 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
           }
           if (pick < 0) pick = v0;
           a.fallback[t] = pick | (1 << 31);
+          ts.stop_fb = pick | (1 << 31);
         }
       }
     }
@@ -358,8 +363,12 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
     report(a.status, c.b, c.err);
   }
   if (rank == writer) {
-    __syncthreads();  // the node's flags and fallback are written
-    arrive_and_walk(a, c, ts);
+    // the node's flags and fallback are written; near-ties among the tested children
+    const int child_ties =
+        __syncthreads_count(!c.err && tid < k && tid <= stop && (my_flag & kFlagTie) != 0);
+    const int fb = ts.stop_fb;
+    arrive_and_walk(a, c, ts, (!c.err && stop == k) ? (fb & 0x7fffffff) : -1,
+                    child_ties + ((fb >> 31) & 1), ts.timeout != 0);
   }
   if (CS > 1) cluster_wait();
 }

@@ -55,6 +55,8 @@ struct TreeSmem {
   int meta[4];                        // error, child count, first node, node count
   float ufb;                          // the uniform of u's fallback draw
   int walk;
+  int stop_fb;                        // the node's fallback token | tie << 31, in the writer CTA
+  int timeout;                        // a bounded wait of this CTA ran out
 };
 
 struct NodeCtx {
@@ -117,23 +119,20 @@ __device__ __forceinline__ float precise_prob(float l, float M, float temp, floa
 }
 
 // ---------------------------------------------------------------- the walk
-// One warp walks request b from the root (step V4).  Node i's data sits in
-// lane i % 32, slot i / 32.
-// spar / stok: the request's parents and tokens, staged in shared memory.
-static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, const int *spar,
-                             const int *stok) {
+// Arrival word of a request (one u32 per request in the workspace): bits
+// 0-15 count the nodes that arrived, bits 16-23 the nodes whose bounded waits
+// ran out, bit 24 says the walk ended at the root and the root's CTA wrote
+// the request's outputs.
+constexpr uint32_t kArriveCount = 0xffffu;
+constexpr uint32_t kArriveErr = 1u << 16;
+constexpr uint32_t kArriveErrMask = 0xffu << 16;
+constexpr uint32_t kArriveRootDone = 1u << 24;
+
+// Whether request b's output rows hold its deepest path (one warp; spar:
+// the request's parents, staged in shared memory, already validated).
+// Reports SPEC_ERR_TREE_TOO_LARGE and returns false when they do not.
+static __device__ bool path_fits(const VerifyArgs &a, int b, int n, const int *spar) {
   const int lane = threadIdx.x & 31;
-  // the request's status, flags and fallbacks, all in one round trip
-  const int st = __ldcg(a.status + b);
-  int par[4], flg[4], fbk[4];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int i = lane + 32 * s;
-    par[s] = i < n ? spar[i] : -2;
-    flg[s] = i < n ? __ldcg(a.flags + lo + i) : 0;
-    fbk[s] = i < n ? __ldcg(a.fallback + lo + i) : 0;
-  }
-  // depth of each node (parents are validated: parent < index)
   int maxd = 0;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
@@ -146,11 +145,45 @@ static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, c
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) maxd = max(maxd, __shfl_xor_sync(0xffffffffu, maxd, o));
-  if (__shfl_sync(0xffffffffu, st, 0) != 0) return;  // an error was reported for the request
   if (maxd + 1 > a.W) {
     if (lane == 0) report(a.status, b, SPEC_ERR_TREE_TOO_LARGE);
-    return;
+    return false;
   }
+  return true;
+}
+
+// Outputs of request b when the walk ends at the root without accepting a
+// child (one warp): the emitted token alone.
+static __device__ void write_root_stop(const VerifyArgs &a, int b, int token, int ties) {
+  const int lane = threadIdx.x & 31;
+  int32_t *pn = a.path_nodes + static_cast<size_t>(b) * a.W;
+  int32_t *ot = a.out_tokens + static_cast<size_t>(b) * a.W;
+  for (int j = lane; j < a.W; j += 32) {
+    pn[j] = j == 0 ? 0 : -1;
+    ot[j] = j == 0 ? token : -1;
+  }
+  if (lane == 0) {
+    a.accept_len[b] = 0;
+    a.near_ties[b] = ties;
+  }
+}
+
+// One warp walks request b from the root (step V4).  Node i's data sits in
+// lane i % 32, slot i / 32.
+// spar / stok: the request's parents and tokens, staged in shared memory.
+static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, const int *spar,
+                             const int *stok) {
+  const int lane = threadIdx.x & 31;
+  // the request's flags and fallbacks, all in one round trip
+  int par[4], flg[4], fbk[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int i = lane + 32 * s;
+    par[s] = i < n ? spar[i] : -2;
+    flg[s] = i < n ? __ldcg(a.flags + lo + i) : 0;
+    fbk[s] = i < n ? __ldcg(a.fallback + lo + i) : 0;
+  }
+  if (!path_fits(a, b, n, spar)) return;
   int32_t *pn = a.path_nodes + static_cast<size_t>(b) * a.W;
   int32_t *ot = a.out_tokens + static_cast<size_t>(b) * a.W;
   int cur = 0, acc = 0, ties = 0;
@@ -251,6 +284,7 @@ static __device__ NodeCtx load_tree_a(const VerifyArgs &a, int t, TreeSmem &ts, 
     ts.wpar[tid] = ld.par;
     ts.wtok[tid] = ld.tok;
   }
+  if (tid == 0) ts.timeout = 0;
   // The offsets must start at 0, never decrease and end at T; then exactly
   // one request owns t.
   int match = -1;
@@ -353,24 +387,47 @@ static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, co
 }
 
 // Called by every thread of the one CTA per node that publishes the node's
-// results, once they are written.  The last node of a request to arrive
-// walks it and clears the request's counter for the next call (with valid
-// offsets every node of the request arrives exactly once).
-static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts) {
+// results, once they are written (flags of its children, its fallback).
+// `root_stop_token` >= 0 at the root when no child of the root was accepted:
+// the walk ends there, so this CTA writes the request's outputs at once (the
+// token, `root_stop_ties` near-ties) and arrives with the root-done bit,
+// needing no other node's results.  Otherwise the node arrives with release
+// semantics, and the request's last arrival (acquire) walks it, unless the
+// root already wrote the outputs or a node's wait ran out.  The last arrival
+// clears the request's counter for the next call (with valid offsets every
+// node of the request arrives exactly once).
+static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts,
+                                       int root_stop_token, int root_stop_ties, bool timed_out) {
   const int tid = threadIdx.x;
+  bool root_done = false;
+  if (tid < 32 && c.count && !c.err && !timed_out && c.u == 0 && root_stop_token >= 0 &&
+      path_fits(a, c.b, c.n, ts.par)) {
+    write_root_stop(a, c.b, root_stop_token, root_stop_ties);
+    root_done = true;
+  }
   if (tid == 0) {
     int walk = 0;
     if (c.count) {
-      // release: this CTA's results (ordered before by the caller's barrier);
-      // acquire: every earlier arrival's results
+      const uint32_t add = 1u | (timed_out ? kArriveErr : 0u) | (root_done ? kArriveRootDone : 0u);
       uint32_t prev;
-      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                   : "=r"(prev)
-                   : "l"(a.done + c.b)
-                   : "memory");
-      if (static_cast<int>(prev) == c.n - 1) {
+      if (root_done) {
+        // nothing this node wrote is read by another node: no ordering needed
+        asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;"
+                     : "=r"(prev)
+                     : "l"(a.done + c.b), "r"(add)
+                     : "memory");
+      } else {
+        // release: this CTA's results (ordered before by the caller's
+        // barrier); acquire: every earlier arrival's results
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                     : "=r"(prev)
+                     : "l"(a.done + c.b), "r"(add)
+                     : "memory");
+      }
+      if (static_cast<int>(prev & kArriveCount) == c.n - 1) {
         a.done[c.b] = 0u;
-        walk = c.err ? 0 : 1;
+        const uint32_t all = prev + add;
+        walk = (!c.err && !(all & kArriveErrMask) && !(all & kArriveRootDone)) ? 1 : 0;
       }
     }
     ts.walk = walk;

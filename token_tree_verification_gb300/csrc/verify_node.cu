@@ -74,15 +74,20 @@ tree_verify_greedy_node_kernel(const VerifyArgs a) {
       ArgMax g{rv[0], ri[0]};
       for (int i = 1; i < kGW; ++i) g = better(g, ArgMax{rv[i], ri[i]});
       a.fallback[t] = g.i;
+      bool accepted = false;
       for (int j = 0; j < c.k; ++j) {
         const int ch = ts.child[j];
-        a.flags[c.lo + ch] = (ts.tok[ch] == g.i) ? kFlagAccept : 0;
+        const bool hit = ts.tok[ch] == g.i;
+        a.flags[c.lo + ch] = hit ? kFlagAccept : 0;
+        accepted |= hit;
       }
+      ts.stop_fb = accepted ? -1 : g.i;   // -1: the walk goes on below this node
     }
   } else if (tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }
-  arrive_and_walk(a, c, ts);
+  __syncthreads();  // the node's flags and fallback are written
+  arrive_and_walk(a, c, ts, c.err ? -1 : ts.stop_fb, 0, false);
 }
 
 int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream) {
