@@ -355,6 +355,48 @@ int spec_tree_verify_static(const float *target_logits, const float *draft_logit
                             int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
                             int32_t *status, void *stream);
 
+/*
+ * spec_test_verify_timeout — a test of verification's failure path, for the
+ * test-suite; no counterpart in the pages.
+ *
+ * Runs spec_tree_verify (stochastic, V <= 131072: the register-resident
+ * kernel) with every bounded device wait limited to wait_ns nanoseconds
+ * (0 < wait_ns <= 2 s) instead of the normal 2 s, and with one CTA of every
+ * node of request drop_request withholding its share of the first
+ * statistics exchange.  Nothing else completes those waits, so they run out:
+ * the kernel returns, status[drop_request] becomes SPEC_ERR_TIMEOUT, that
+ * request's outputs are left as they were (its walk is not run), and every
+ * other request is verified exactly as by spec_tree_verify.  The workspace
+ * is left reusable.  Arguments are those of spec_tree_verify plus the two
+ * above; SPEC_ERR_SHAPE for greedy, wider vocabularies, or out-of-range
+ * wait_ns / drop_request.
+ */
+int spec_test_verify_timeout(const float *target_logits, const float *draft_logits,
+                             const int32_t *tokens, const int32_t *parents,
+                             const int32_t *tree_offsets, int B, int T, int V, float temperature,
+                             uint64_t seed, int32_t *accept_len, int32_t *path_nodes,
+                             int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
+                             void *workspace, size_t workspace_bytes, int32_t *status,
+                             void *stream, uint64_t wait_ns, int drop_request);
+
+/*
+ * spec_philox_uniforms — step R on its own: the uniform the kernels draw for
+ * each of n counters.
+ *
+ * Source: the counter-based generator the method's stochastic decisions use
+ * (a generator shared with any independent check of the decisions).
+ * Philox4x64-10 (Salmon et al., SC'11) with key (seed, 0); for counter
+ * (c0, c1, c2, c3): u = (first output word >> 40) * 2^-24, exact in float.
+ * spec_tree_verify draws with counters (node, request, 0, 0) for the accept
+ * test of child `node` and (node, request, 1, 0) for the draw at `node`;
+ * spec_tree_expand with (node, request, 2, j) for child slot j.
+ *
+ *   counters [n][4] int64 (each word taken as its uint64 bit pattern), device
+ *   u        [n] float out, device
+ * n == 0 launches nothing.
+ */
+int spec_philox_uniforms(uint64_t seed, const int64_t *counters, int n, float *u, void *stream);
+
 /* Human-readable name of a spec_status value (static storage). */
 const char *spec_status_string(int code);
 

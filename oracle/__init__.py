@@ -47,6 +47,8 @@ def _load():
     lib.oracle_philox4x64_10.restype = None
     lib.oracle_uniform.argtypes = [u64, i64, i64, i64]
     lib.oracle_uniform.restype = ctypes.c_double
+    lib.oracle_uniforms.argtypes = [u64, P, i64, P]
+    lib.oracle_uniforms.restype = None
     lib.oracle_build_mask.argtypes = [P, P, i32, i32, P, P, P]
     lib.oracle_build_mask.restype = i32
     lib.oracle_tree_attn.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32,
@@ -95,6 +97,16 @@ def philox4x64_10(counter, key) -> np.ndarray:
 def uniform(seed: int, node: int, request: int, kind: int) -> float:
     """The method's uniform for (request, node, kind), in [0, 1)."""
     return float(_load().oracle_uniform(seed & (2**64 - 1), node, request, kind))
+
+
+def uniforms(seed: int, counters) -> np.ndarray:
+    """The uniform of every counter row (c0, c1, c2, c3) of ``counters`` [n, 4]
+    (any integer dtype; words taken as uint64), key (seed, 0)."""
+    ctr = np.ascontiguousarray(np.asarray(counters).astype(np.int64).view(np.uint64))
+    n = ctr.shape[0]
+    out = np.zeros(n, np.float64)
+    _load().oracle_uniforms(seed & (2**64 - 1), _ptr(ctr), n, _ptr(out))
+    return out
 
 
 def build_mask(parents, offsets):

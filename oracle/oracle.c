@@ -104,6 +104,17 @@ double oracle_uniform(uint64_t seed, int64_t node, int64_t request, int64_t kind
   return (double)(out[0] >> 40) * (1.0 / 16777216.0);
 }
 
+/* The uniforms of n counters (c0, c1, c2, c3) [n][4], key (seed, 0), the
+ * same conversion: for checking a device implementation of the generator. */
+void oracle_uniforms(uint64_t seed, const uint64_t *ctr, int64_t n, double *u) {
+  const uint64_t key[2] = {seed, 0};
+  for (int64_t i = 0; i < n; ++i) {
+    uint64_t out[4];
+    oracle_philox4x64_10(ctr + 4 * i, key, out);
+    u[i] = (double)(out[0] >> 40) * (1.0 / 16777216.0);
+  }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Tree validation: parent[0] = -1 and 0 <= parent[i] < i for i > 0 ([dev]  */
 /* §2.1: each node keeps a parent pointer; index order is topological).      */

@@ -41,3 +41,18 @@ def test_uniform_chi_square():
     chi2 = ((h - n / bins) ** 2 / (n / bins)).sum()
     dof = bins - 1
     assert chi2 <= dof + 3 * np.sqrt(2 * dof)
+
+
+def test_batch_uniforms_match_numpy_and_the_single_counter_form():
+    rng = np.random.default_rng(3)
+    ctr = np.stack([rng.integers(0, 128, 50), rng.integers(0, 2**31 - 1, 50),
+                    rng.integers(0, 3, 50), rng.integers(0, 16, 50)], axis=1).astype(np.int64)
+    ctr[0] = (2**62, 2**40, 2, 15)
+    seed = 0x5EED
+    u = oracle.uniforms(seed, ctr)
+    for i, (c0, c1, c2, c3) in enumerate(ctr.tolist()):
+        c_int = c0 + (c1 << 64) + (c2 << 128) + (c3 << 192)
+        bg = np.random.Philox(key=seed, counter=(c_int - 1) % 2**256)
+        assert u[i] == (int(bg.random_raw(1)[0]) >> 40) / 2.0**24
+        if c3 == 0:
+            assert u[i] == oracle.uniform(seed, c0, c1, c2)

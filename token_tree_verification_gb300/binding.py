@@ -68,6 +68,8 @@ def load():
     lib.spec_tree_expand.restype = I
     lib.spec_tree_prune.argtypes = [P, P, P, P, I, I, P, P, P, P, P, P]
     lib.spec_tree_prune.restype = I
+    lib.spec_philox_uniforms.argtypes = [U64, P, I, P, P]
+    lib.spec_philox_uniforms.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -272,4 +274,19 @@ def tree_prune(parents, tokens, scores, cand_offsets, keep: int, status, stream=
     _check(lib.spec_tree_prune(_ptr(parents), _ptr(tokens), _ptr(scores), _ptr(cand_offsets), B, keep,
                                _ptr(out["parents"]), _ptr(out["tokens"]), _ptr(out["kept"]),
                                _ptr(out["n_out"]), _ptr(status), _stream(stream)), "spec_tree_prune")
+    return out
+
+
+def philox_uniforms(seed: int, counters, out=None, stream=None):
+    """Step R: the uniform for each counter row (c0, c1, c2, c3) of the int64
+    device tensor ``counters`` [n, 4].  Returns a float32 device tensor [n]."""
+    lib = load()
+    _dev(counters, torch.int64, "counters")
+    if counters.dim() != 2 or counters.shape[1] != 4:
+        raise ValueError("counters must be [n, 4]")
+    n = counters.shape[0]
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=counters.device)
+    _check(lib.spec_philox_uniforms(int(seed) & (2**64 - 1), _ptr(counters), n, _ptr(out),
+                                    _stream(stream)), "spec_philox_uniforms")
     return out

@@ -120,16 +120,20 @@ __device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete; false if the time limit ran
-// out.  try_wait itself suspends the thread in hardware for a while, so the
-// loop polls without sleeping and reads the clock only every 256 polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete; false if `limit_ns` ran out.
+// try_wait itself suspends the thread in hardware for a while, so the loop
+// polls without sleeping and reads the clock only every 256 polls.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
-    if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 __device__ __forceinline__ void fence_barrier_init() {

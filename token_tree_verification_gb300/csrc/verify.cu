@@ -226,6 +226,13 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
         break;
       }
       if (frozen) continue;
+      // After a wait ran out this thread takes part in no further exchange:
+      // an arrival on a barrier whose previous phase never completed is not
+      // allowed.  (Its request is reported and its walk not run.)
+      if (!ok) {
+        frozen = true;
+        continue;
+      }
       // rejected: r becomes max(0, p - c q) / W(c) with c = c_prev + W_prev
       const float c_new = c_prev + W_prev;
       const float cq = c_new * sc_d;
@@ -391,7 +398,7 @@ int verify_entry(const float *target_logits, const float *draft_logits, const in
                  float temperature, float top_p, uint64_t seed, int32_t *accept_len,
                  int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
                  void *workspace, size_t workspace_bytes, int32_t *status, void *stream,
-                 bool clear_workspace) {
+                 bool clear_workspace, uint64_t wait_ns, int drop_request) {
   if (!target_logits || !tokens || !parents || !tree_offsets || !accept_len || !path_nodes ||
       !out_tokens || !near_ties || !status)
     return SPEC_ERR_NULL;
@@ -429,6 +436,8 @@ int verify_entry(const float *target_logits, const float *draft_logits, const in
   args.inv_temp = greedy ? 0.f : 1.0f / temperature;
   args.top_p = nucleus ? top_p : 1.f;
   args.seed = seed;
+  args.wait_ns = wait_ns;
+  args.drop_request = drop_request;
   args.accept_len = accept_len;
   args.path_nodes = path_nodes;
   args.out_tokens = out_tokens;
@@ -493,4 +502,22 @@ extern "C" int spec_tree_verify_top_p(const float *target_logits, const float *d
   return spec::verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
                             temperature, top_p, seed, accept_len, path_nodes, out_tokens, near_ties,
                             max_depth_plus1, workspace, workspace_bytes, status, stream, false);
+}
+
+extern "C" int spec_test_verify_timeout(const float *target_logits, const float *draft_logits,
+                                        const int32_t *tokens, const int32_t *parents,
+                                        const int32_t *tree_offsets, int B, int T, int V,
+                                        float temperature, uint64_t seed, int32_t *accept_len,
+                                        int32_t *path_nodes, int32_t *out_tokens,
+                                        int32_t *near_ties, int max_depth_plus1, void *workspace,
+                                        size_t workspace_bytes, int32_t *status, void *stream,
+                                        uint64_t wait_ns, int drop_request) {
+  // the register-resident stochastic kernel only, a short positive limit
+  if (!(temperature > 0.f) || V > spec::kMaxCS * spec::kRegChunk) return SPEC_ERR_SHAPE;
+  if (wait_ns == 0 || wait_ns > spec::kWaitLimitNs || drop_request < 0 || drop_request >= B)
+    return SPEC_ERR_SHAPE;
+  return spec::verify_entry(target_logits, draft_logits, tokens, parents, tree_offsets, B, T, V,
+                            temperature, 1.f, seed, accept_len, path_nodes, out_tokens, near_ties,
+                            max_depth_plus1, workspace, workspace_bytes, status, stream, false,
+                            wait_ns, drop_request);
 }

@@ -38,6 +38,8 @@ struct VerifyArgs {
   int32_t *flags;      // [T] written by the parent's CTA group: accept / tie bits
   int32_t *fallback;   // [T] token emitted on stopping at the node | tie << 31
   uint32_t *done;      // [B] arrival counters (zero between calls)
+  uint64_t wait_ns;    // limit of every bounded wait (kWaitLimitNs outside the failure test)
+  int drop_request;    // failure test: this request's first exchange is withheld (-1: none)
 };
 
 // A node's tree context, staged in shared memory by load_tree().
@@ -447,7 +449,7 @@ int verify_entry(const float *target_logits, const float *draft_logits, const in
                  float temperature, float top_p, uint64_t seed, int32_t *accept_len,
                  int32_t *path_nodes, int32_t *out_tokens, int32_t *near_ties, int max_depth_plus1,
                  void *workspace, size_t workspace_bytes, int32_t *status, void *stream,
-                 bool clear_workspace);
+                 bool clear_workspace, uint64_t wait_ns = kWaitLimitNs, int drop_request = -1);
 
 // greedy per-node kernel (verify_node.cu)
 int launch_verify_greedy(const VerifyArgs &args, cudaStream_t stream);

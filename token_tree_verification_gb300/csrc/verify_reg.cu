@@ -308,10 +308,12 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     }
     sl = warp_sum(sl);
     sd = warp_sum(sd);
-    if (lane < CS)
+    // (the failure test withholds the last CTA's share for one request, so
+    // that every CTA's wait on this exchange runs out)
+    if (lane < CS && !(c.b == a.drop_request && rank == CS - 1))
       st_async_v4_f32(peer_addr(&ex.stat[rank][w_id], lane), make_float4(ml, sl, md, sd),
                       peer_addr(&xbar[0], lane));
-    if (!mbar_wait(&xbar[0], 0)) ok = false;
+    if (!mbar_wait_for(&xbar[0], 0, a.wait_ns)) ok = false;
     // group maxima and sums, added in the same order by every warp
     const int nslot = CS * kRWarps;
     const float4 *flat = &ex.stat[0][0];
@@ -407,13 +409,13 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         }
         fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 && ok) {   // (no arrival after a wait ran out, as in the rounds below)
           mbar_arrive_expect_tx(&tp.bar[par], static_cast<uint32_t>(CS) * kHistBytes);
           for (int r = 0; r < CS; ++r)
             bulk_copy_s2s(peer_addr(&tp.recv[par][rank][0][0], r), smem_addr(&tp.cta[par][0][0]),
                           kHistBytes, peer_addr(&tp.bar[par], r));
         }
-        if (ok && !mbar_wait(&tp.bar[par], (pass >> 1) & 1)) ok = false;
+        if (ok && !mbar_wait_for(&tp.bar[par], (pass >> 1) & 1, a.wait_ns)) ok = false;
         {
           const int row = tid >> 8, bin = tid & 255;
           unsigned long long h = 0ull;
@@ -509,7 +511,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       if (lane < CS)
         st_async_v2_f32(peer_addr(&tp.statp[rank][w_id].x, lane), sf, nflags,
                         peer_addr(&tp.sbar, lane));
-      if (ok && !mbar_wait(&tp.sbar, 0)) ok = false;
+      if (ok && !mbar_wait_for(&tp.sbar, 0, a.wait_ns)) ok = false;
     }
     // the children's p and q from their raw logits (scalar warp), published
     // with the uniforms through an mbarrier (release / acquire)
@@ -552,7 +554,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&nbar);
     }
-    if (ok && !mbar_wait(&nbar, 0)) ok = false;
+    if (ok && !mbar_wait_for(&nbar, 0, a.wait_ns)) ok = false;
     if (TOPP) near = ns.near;
 
     // ---- V2: the children's accept tests in index order, stopping at the
@@ -583,6 +585,13 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         break;
       }
       if (frozen) continue;
+      // After a wait ran out this thread takes part in no further exchange:
+      // an arrival on a barrier whose previous phase never completed is not
+      // allowed.  (Its request is reported and its walk not run.)
+      if (!ok) {
+        frozen = true;
+        continue;
+      }
       // rejected: r becomes max(0, p - c q) / W(c) with c = c_prev + W_prev
       const float c_new = c_prev + W_prev;
       float wsum = resid_sum_pos(xp, xq, c_new);   // c_new > 0
@@ -591,7 +600,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       if (tid == 0) mbar_arrive_expect_tx(&xbar[1 + p], static_cast<uint32_t>(CS * kRWarps * 4));
       if (lane < CS)
         st_async_f32(peer_addr(&ex.part[p][rank][w_id], lane), wsum, peer_addr(&xbar[1 + p], lane));
-      if (ok && !mbar_wait(&xbar[1 + p], (rounds >> 1) & 1)) ok = false;
+      if (ok && !mbar_wait_for(&xbar[1 + p], (rounds >> 1) & 1, a.wait_ns)) ok = false;
       ++rounds;
       const float *fl = &ex.part[p][0][0];
       float acc = 0.f;
