@@ -245,6 +245,8 @@ class Step:
         self.max_prefix = int(w.prefix_lens.max())
         self.seed = seed
         self.side = torch.cuda.Stream()
+        self.attn_ctas = attn_cta_budget(w, torch.cuda.get_device_properties(
+            torch.cuda.current_device()).multi_processor_count)
 
     def run(self, i: int, stream=None):
         """Enqueue step i on ``stream`` (default: the current stream) over
@@ -264,11 +266,33 @@ class Step:
         self.side.wait_stream(cur)
         ttv.build_tree_mask(par, off, self.status, mask=self.mask, depth=self.depth, stream=cur)
         ttv.tree_attn(q, k, v, pl, off, self.mask, self.max_prefix, self.status, o=self.o,
-                      workspace=self.ws_attn, stream=cur)
+                      workspace=self.ws_attn, stream=cur, max_ctas=self.attn_ctas)
         with torch.cuda.stream(self.side):
             ttv.tree_verify(tl, dl, tok, par, off, w.temperature, seed, self.W, self.status, self.ws,
                             outputs=outs, stream=self.side)
         cur.wait_stream(self.side)
+
+
+def verify_resident_ctas(w) -> int:
+    """CTAs stochastic verification keeps resident while it works: two (one
+    per 16384 vocabulary entries) for every internal node; leaves leave at
+    once (their draw is taken by the walker when the walk reaches them).
+    Greedy verification's CTAs are short and many; it gets no reservation."""
+    if w.temperature <= 0 or w.V > 131072:
+        return 0
+    internal = 0
+    for b in range(w.B):
+        lo, hi = w.offsets[b], w.offsets[b + 1]
+        internal += len(set(w.parents[lo + 1:hi].tolist()))
+    return internal * ((w.V + 16383) // 16384)
+
+
+def attn_cta_budget(w, sms: int) -> int:
+    """The CTAs the step's attention may keep resident while verification
+    runs beside it: the SMs verification's internal nodes do not hold, when
+    they hold less than half of them (0: the whole GPU)."""
+    need = verify_resident_ctas(w)
+    return sms - need if 0 < need < sms // 2 else 0
 
 
 def run_native(args, rank, world, local_rank):

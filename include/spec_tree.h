@@ -143,6 +143,21 @@ int spec_tree_attn(const void *q, const void *k_cache, const void *v_cache, void
                    void *stream);
 
 /*
+ * spec_tree_attn_ex — spec_tree_attn for a caller that runs other kernels
+ * beside it (another stream, another graph branch): the bf16 path plans its
+ * key splits (the CTAs of one query block) for at most max_ctas CTAs resident
+ * at once instead of the whole GPU, so that the other work keeps the SMs it
+ * needs.  max_ctas == 0 means the device's SM count (spec_tree_attn);
+ * negative max_ctas is SPEC_ERR_SHAPE.  The result is the same; only the
+ * launch shape changes.  The fp32 path ignores max_ctas.
+ */
+int spec_tree_attn_ex(const void *q, const void *k_cache, const void *v_cache, void *o, int dtype,
+                      int B, int T, int Hq, int Hkv, int D, int S_cap, int max_prefix,
+                      const int32_t *prefix_lens, const int32_t *tree_offsets,
+                      const uint32_t *mask, float softmax_scale, void *workspace,
+                      size_t workspace_bytes, int max_ctas, int32_t *status, void *stream);
+
+/*
  * Bytes of scratch spec_tree_verify needs: per-node acceptance flags and
  * fallback tokens plus one arrival counter per request.  The workspace must
  * be zero-filled before its FIRST use; every call leaves the counters at zero

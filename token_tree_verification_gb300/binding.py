@@ -56,6 +56,8 @@ def load():
     lib.spec_tree_attn_workspace_size.restype = SZ
     lib.spec_tree_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, F, P, SZ, P, P]
     lib.spec_tree_attn.restype = I
+    lib.spec_tree_attn_ex.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, F, P, SZ, I, P, P]
+    lib.spec_tree_attn_ex.restype = I
     lib.spec_tree_verify_workspace_size.argtypes = [I, I, I]
     lib.spec_tree_verify_workspace_size.restype = SZ
     lib.spec_tree_verify.argtypes = [P, P, P, P, P, I, I, I, F, U64, P, P, P, P, I, P, SZ, P, P]
@@ -129,8 +131,10 @@ def tree_attn_workspace_size(B, T, Hq, Hkv, D, max_prefix) -> int:
 
 
 def tree_attn(q, k_cache, v_cache, prefix_lens, offsets, mask, max_prefix, status, o=None,
-              softmax_scale: float = 0.0, workspace=None, stream=None):
-    """Steps A2-A3.  q [T, Hq, D]; k_cache, v_cache [B, Hkv, S_cap, D]; bf16 or fp32."""
+              softmax_scale: float = 0.0, workspace=None, stream=None, max_ctas: int = 0):
+    """Steps A2-A3.  q [T, Hq, D]; k_cache, v_cache [B, Hkv, S_cap, D]; bf16 or fp32.
+    ``max_ctas`` > 0 plans the launch for that many resident CTAs
+    (spec_tree_attn_ex), leaving the other SMs to concurrent work."""
     lib = load()
     dt = q.dtype
     if dt not in (torch.bfloat16, torch.float32):
@@ -151,12 +155,12 @@ def tree_attn(q, k_cache, v_cache, prefix_lens, offsets, mask, max_prefix, statu
     ws_need = tree_attn_workspace_size(B, T, Hq, Hkv, D, max_prefix)
     if ws_need and workspace is None:
         workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
-    _check(lib.spec_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
-                              SPEC_BF16 if dt == torch.bfloat16 else SPEC_F32, B, T, Hq, Hkv, D,
-                              S_cap, int(max_prefix), _ptr(prefix_lens), _ptr(offsets), _ptr(mask),
-                              float(softmax_scale), _ptr(workspace),
-                              0 if workspace is None else workspace.numel(), _ptr(status),
-                              _stream(stream)), "spec_tree_attn")
+    _check(lib.spec_tree_attn_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+                                 SPEC_BF16 if dt == torch.bfloat16 else SPEC_F32, B, T, Hq, Hkv, D,
+                                 S_cap, int(max_prefix), _ptr(prefix_lens), _ptr(offsets),
+                                 _ptr(mask), float(softmax_scale), _ptr(workspace),
+                                 0 if workspace is None else workspace.numel(), int(max_ctas),
+                                 _ptr(status), _stream(stream)), "spec_tree_attn_ex")
     return o
 
 

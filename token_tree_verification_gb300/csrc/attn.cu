@@ -590,6 +590,18 @@ extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_
                               const int32_t *tree_offsets, const uint32_t *mask,
                               float softmax_scale, void *workspace, size_t workspace_bytes,
                               int32_t *status, void *stream) {
+  return spec_tree_attn_ex(q, k_cache, v_cache, o, dtype, B, T, Hq, Hkv, D, S_cap, max_prefix,
+                           prefix_lens, tree_offsets, mask, softmax_scale, workspace,
+                           workspace_bytes, 0, status, stream);
+}
+
+extern "C" int spec_tree_attn_ex(const void *q, const void *k_cache, const void *v_cache, void *o,
+                                 int dtype, int B, int T, int Hq, int Hkv, int D, int S_cap,
+                                 int max_prefix, const int32_t *prefix_lens,
+                                 const int32_t *tree_offsets, const uint32_t *mask,
+                                 float softmax_scale, void *workspace, size_t workspace_bytes,
+                                 int max_ctas, int32_t *status, void *stream) {
+  if (max_ctas < 0) return SPEC_ERR_SHAPE;
   if (!q || !k_cache || !v_cache || !o || !prefix_lens || !tree_offsets || !mask || !status)
     return SPEC_ERR_NULL;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
@@ -639,5 +651,8 @@ extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_
       !encode_kv_map(&tmv, v_cache, B, Hkv, S_cap, D))
     return SPEC_ERR_CUDA;
   (void)workspace; (void)workspace_bytes;
-  return spec::launch_attn_tc(args, max_prefix, T, tmq, tmk, tmv, packed, sm_count(), st);
+  // the key splits are planned for the SMs the caller leaves to this launch
+  const int sms = sm_count();
+  return spec::launch_attn_tc(args, max_prefix, T, tmq, tmk, tmv, packed,
+                              max_ctas > 0 && max_ctas < sms ? max_ctas : sms, st);
 }

@@ -748,7 +748,7 @@ void plan_attn_tc(int B, int T, int Hkv, int G, int max_prefix, int num_sms, int
   const long long units = static_cast<long long>(rowblocks) * B * Hkv;
   int cs = 1;
   long long best = -1;
-  for (int c = 1; c <= kTcMaxSplits; c *= 2) {
+  for (int c = 1; c <= kTcMaxSplits; ++c) {
     if (c > 1 && tiles_max < 2 * c) break;
     const long long waves = (units * c + num_sms - 1) / num_sms;
     const long long cost = waves * ((tiles_max + c - 1) / c + 4 + (c > 1 ? 3 : 0));

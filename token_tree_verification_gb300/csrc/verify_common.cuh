@@ -59,6 +59,10 @@ struct TreeSmem {
   int walk;
   int stop_fb;                        // the node's fallback token | tie << 31, in the writer CTA
   int timeout;                        // a bounded wait of this CTA ran out
+  float dm[32], ds[32];               // per warp: (max, sum) of a leaf's row (draw at a leaf)
+  int leaf[5];                        // walk ended at a leaf: node, request-local; accepted
+                                      // tokens; near-ties so far; the draw's selected range;
+                                      // the draw's token | tie << 31
 };
 
 struct NodeCtx {
@@ -173,8 +177,12 @@ static __device__ void write_root_stop(const VerifyArgs &a, int b, int token, in
 // One warp walks request b from the root (step V4).  Node i's data sits in
 // lane i % 32, slot i / 32.
 // spar / stok: the request's parents and tokens, staged in shared memory.
-static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, const int *spar,
-                             const int *stok) {
+// With `lazy_leaves` the leaves computed no fallback: when the walk stops at
+// a leaf, the walk records it in ts.leaf (node, accepted count, near-ties)
+// and leaves the emitted token and the near-tie count to the caller's draw;
+// returns whether it did.
+static __device__ bool walk_request(const VerifyArgs &a, int b, int lo, int n, const int *spar,
+                                    const int *stok, bool lazy_leaves, TreeSmem &ts) {
   const int lane = threadIdx.x & 31;
   // the request's flags and fallbacks, all in one round trip
   int par[4], flg[4], fbk[4];
@@ -185,7 +193,7 @@ static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, c
     flg[s] = i < n ? __ldcg(a.flags + lo + i) : 0;
     fbk[s] = i < n ? __ldcg(a.fallback + lo + i) : 0;
   }
-  if (!path_fits(a, b, n, spar)) return;
+  if (!path_fits(a, b, n, spar)) return false;
   int32_t *pn = a.path_nodes + static_cast<size_t>(b) * a.W;
   int32_t *ot = a.out_tokens + static_cast<size_t>(b) * a.W;
   int cur = 0, acc = 0, ties = 0;
@@ -208,6 +216,26 @@ static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, c
         m = lim < 0 ? 0u : (lim >= 31 ? m : (m & ((2u << lim) - 1u)));
       }
       ties += __popc(m);
+    }
+    if (next < 0 && lazy_leaves) {
+      bool has_child = false;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) has_child |= __any_sync(0xffffffffu, par[s] == cur);
+      if (!has_child) {
+        // a leaf: its draw is computed now, by the whole CTA
+        if (lane == 0) {
+          pn[0] = 0;
+          for (int j = acc + 1; j < a.W; ++j) {
+            pn[j] = -1;
+            ot[j] = -1;
+          }
+          a.accept_len[b] = acc;
+          ts.leaf[0] = cur;
+          ts.leaf[1] = acc;
+          ts.leaf[2] = ties;
+        }
+        return true;
+      }
     }
     if (next < 0) {
       // the fallback of node `cur` sits in lane cur % 32, slot cur / 32
@@ -237,6 +265,114 @@ static __device__ void walk_request(const VerifyArgs &a, int b, int lo, int n, c
     a.accept_len[b] = acc;
     a.near_ties[b] = ties;
   }
+  return false;
+}
+
+// The token drawn at a leaf u (the bonus token when the walk accepts the
+// path down to it): the inverse-CDF draw from p_u = softmax(row / T) at the
+// uniform `u`, taken by the whole CTA (blockDim.x threads, a multiple of 32,
+// at most 1024).  Warp w owns the contiguous range [w R, (w + 1) R) of the
+// row: one pass gives each warp's (max, sum), the CTA adds the warps'
+// masses in index order and finds the range where the running mass passes
+// u * S; that range's warp splits it over its lanes, finds the lane's
+// stretch, and that lane walks its entries.  Returns token | tie << 31, tie
+// when u * S lies within 1e-6 * S of the chosen entry's interval ends; when
+// rounding keeps the running sum below u * S, the last entry of positive
+// weight (a tie).  Called by every thread; the result is valid in thread 0.
+static __device__ int cta_leaf_draw(const float *row, int V, float l2s, float u, TreeSmem &ts) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  const int R = (V + nw - 1) / nw;
+  const int r0 = min(V, w * R), r1 = min(V, r0 + R);
+  // pass 1: the warp's online (max, sum), lanes strided for coalescing
+  float m = -INFINITY, sum = 0.f;
+  for (int x = r0 + lane; x < r1; x += 32) {
+    const float v = __ldcg(row + x) * l2s;
+    if (v > m) {
+      sum = sum * fast_exp2(m - v) + 1.f;
+      m = v;
+    } else if (v != -INFINITY) {
+      sum += fast_exp2(v - m);
+    }
+  }
+  const float wm = warp_max(m);
+  sum = (m == -INFINITY) ? 0.f : sum * fast_exp2(m - wm);
+  sum = warp_sum(sum);
+  if (lane == 0) {
+    ts.dm[w] = wm;
+    ts.ds[w] = sum;
+  }
+  __syncthreads();
+  // the warps' masses relative to the row's max, and where u * S falls
+  if (w == 0) {
+    const float mw = lane < nw ? ts.dm[lane] : -INFINITY;
+    const float M = warp_max(mw);
+    const float mass = (lane < nw && ts.ds[lane] > 0.f) ? ts.ds[lane] * fast_exp2(mw - M) : 0.f;
+    float inc = mass;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const float S = __shfl_sync(0xffffffffu, inc, 31);
+    const float target = u * S;
+    const uint32_t hit = __ballot_sync(0xffffffffu, lane < nw && inc > target);
+    const uint32_t pos = __ballot_sync(0xffffffffu, mass > 0.f);
+    const int ws = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const float before = __shfl_sync(0xffffffffu, inc - mass, ws);   // mass before warp ws
+    if (lane == 0) {
+      ts.leaf[3] = ws | (hit ? 0 : (1 << 30));       // bit 30: rounding, no crossing
+      ts.dm[0] = M;
+      ts.ds[0] = S;
+      ts.ds[1] = before;
+    }
+  }
+  __syncthreads();
+  const int sel = ts.leaf[3];
+  const int ws = sel & 0xffff;
+  const bool rounding = (sel >> 30) & 1;
+  const float M = ts.dm[0], S = ts.ds[0], before = ts.ds[1];
+  const float target = u * S;
+  int result = 0;
+  if (w == ws) {
+    // pass 2: the selected range split into one stretch per lane
+    const int a0 = min(V, ws * R), a1 = min(V, a0 + R);
+    const int per = (a1 - a0 + 31) / 32;
+    const int s0 = min(a1, a0 + lane * per), s1 = min(a1, s0 + per);
+    float ls = 0.f;
+    for (int x = s0; x < s1; ++x) ls += fast_exp2(__ldcg(row + x) * l2s - M);
+    float inc = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const uint32_t hit = rounding ? 0u : __ballot_sync(0xffffffffu, before + inc > target);
+    const uint32_t pos = __ballot_sync(0xffffffffu, ls > 0.f);
+    const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    if (lane == L) {
+      float cum = before + inc - ls;
+      int pick = -1, last = s0;
+      bool tie = !hit;
+      for (int x = s0; x < s1; ++x) {
+        const float wv = fast_exp2(__ldcg(row + x) * l2s - M);
+        if (wv > 0.f) last = x;
+        if (pick < 0 && hit && cum + wv > target) {
+          pick = x;
+          tie = fabsf(target - cum) < kTieBand * S || fabsf(target - (cum + wv)) < kTieBand * S;
+        }
+        cum += wv;
+      }
+      if (pick < 0) {   // rounding: the last entry of positive weight, on the boundary
+        pick = last;
+        tie = true;
+      }
+      ts.leaf[4] = pick | (tie ? (1 << 31) : 0);
+    }
+  }
+  __syncthreads();
+  result = ts.leaf[4];
+  return result;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -388,6 +524,19 @@ static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, co
   return load_tree_b(a, t, ts, load_tree_a(a, t, ts, ld));
 }
 
+// The request's parents and tokens from node t's staged window into ts.par /
+// ts.tok, without validation (a node whose CTAs skip load_tree_b: the root,
+// which validates, arrives with the error bit if the tree is malformed, and
+// then no walk reads them).  Ends with a barrier.
+static __device__ void stage_request(const NodeCtx &c, int t, TreeSmem &ts) {
+  for (int i = threadIdx.x; i < c.n; i += blockDim.x) {
+    const int wi = c.lo + i - (t - (SPEC_MAX_TREE_NODES - 1));   // in [0, 254]
+    ts.par[i] = ts.wpar[wi];
+    ts.tok[i] = ts.wtok[wi];
+  }
+  __syncthreads();
+}
+
 // Called by every thread of the one CTA per node that publishes the node's
 // results, once they are written (flags of its children, its fallback).
 // `root_stop_token` >= 0 at the root when no child of the root was accepted:
@@ -399,7 +548,8 @@ static __device__ NodeCtx load_tree(const VerifyArgs &a, int t, TreeSmem &ts, co
 // clears the request's counter for the next call (with valid offsets every
 // node of the request arrives exactly once).
 static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts,
-                                       int root_stop_token, int root_stop_ties, bool timed_out) {
+                                       int root_stop_token, int root_stop_ties, bool timed_out,
+                                       bool lazy_leaves = false) {
   const int tid = threadIdx.x;
   bool root_done = false;
   if (tid < 32 && c.count && !c.err && !timed_out && c.u == 0 && root_stop_token >= 0 &&
@@ -410,7 +560,10 @@ static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, Tr
   if (tid == 0) {
     int walk = 0;
     if (c.count) {
-      const uint32_t add = 1u | (timed_out ? kArriveErr : 0u) | (root_done ? kArriveRootDone : 0u);
+      // a node that found an error arrives with the error bit, so that no
+      // walk (which trusts the validated tree) runs for the request
+      const uint32_t add = 1u | ((timed_out || c.err) ? kArriveErr : 0u) |
+                           (root_done ? kArriveRootDone : 0u);
       uint32_t prev;
       if (root_done) {
         // nothing this node wrote is read by another node: no ordering needed
@@ -437,7 +590,21 @@ static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, Tr
   __syncthreads();
   // The walker's loads are ordered after thread 0's acquire by the barrier
   // and read L2 (ld.global.cg), where the other nodes' released results sit.
-  if (ts.walk && tid < 32) walk_request(a, c.b, c.lo, c.n, ts.par, ts.tok);
+  if (!ts.walk) return;
+  if (tid == 0) ts.leaf[0] = -1;
+  __syncthreads();
+  if (tid < 32) walk_request(a, c.b, c.lo, c.n, ts.par, ts.tok, lazy_leaves, ts);
+  __syncthreads();
+  const int leaf = ts.leaf[0];
+  if (leaf < 0) return;
+  // the walk accepted the path down to a leaf: the bonus token is its draw
+  const float *row = a.target + static_cast<size_t>(c.lo + leaf) * a.V;
+  const int r = cta_leaf_draw(row, a.V, a.inv_temp * 1.4426950408889634f,
+                              spec_uniform(a.seed, leaf, c.b, 1), ts);
+  if (tid == 0) {
+    a.out_tokens[static_cast<size_t>(c.b) * a.W + ts.leaf[1]] = r & 0x7fffffff;
+    a.near_ties[c.b] = ts.leaf[2] + ((r >> 31) & 1);
+  }
 }
 
 // Host entry of spec_tree_verify / spec_tree_verify_top_p (verify.cu): checks

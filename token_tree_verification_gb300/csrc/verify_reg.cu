@@ -216,15 +216,38 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     fence_barrier_init();
   }
   pdl_wait();
-  // the tree first, then the target row, straight into registers
+  // the tree first, then the target row
   const TreeLoads tl = tree_loads(a, t);
   float4 xp[kRVec], xq[kRVec];
-  load_row(trow, base, end, vec, xp);
+  if constexpr (TOPP) {
+    load_row(trow, base, end, vec, xp);
+  } else if (tid == 0 && vec && end > v0) {
+    // the slice goes to L2 at once, before the node knows whether it is a
+    // leaf (whose row is read only if the walk ends there)
+    const uint32_t bytes = (static_cast<uint32_t>(end - v0) * 4u) & ~15u;
+    if (bytes > 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       reinterpret_cast<uint64_t>(trow + v0)),
+                   "r"(bytes)
+                   : "memory");
+  }
   if (CS > 1) cluster_arrive_relaxed();   // waited for before the first remote store
   const NodeCtx ca = load_tree_a(a, t, ts, tl);
   // Internal nodes only: the draft row is requested as soon as the staged
   // window shows a child, before the tree is validated.
   const bool early_draft = has_children(ca, t, ts);
+  if constexpr (!TOPP) {
+    if (!early_draft && !ca.err && ca.u != 0) {
+      // A leaf other than a lone root: its only result is the token drawn if
+      // the walk accepts the path down to it, which the walker then draws
+      // itself.  The leaf arrives and frees its SMs.
+      stage_request(ca, t, ts);
+      if (CS > 1) cluster_wait();
+      if (rank == 0) arrive_and_walk(a, ca, ts, -1, 0, false, true);
+      return;
+    }
+    load_row(trow, base, end, vec, xp);
+  }
   if (early_draft) {
     load_row(drow, base, end, vec, xq);
   } else {
@@ -787,7 +810,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         __syncthreads_count(!c.err && tid < k && tid <= stop && (my_flag & kFlagTie) != 0);
     const int fb = ts.stop_fb;
     arrive_and_walk(a, c, ts, (!c.err && stop == k) ? (fb & 0x7fffffff) : -1,
-                    child_ties + ((fb >> 31) & 1), ts.timeout != 0);
+                    child_ties + ((fb >> 31) & 1), ts.timeout != 0, !TOPP);
   }
   if (CS > 1) cluster_wait();
 }
