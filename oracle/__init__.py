@@ -66,6 +66,8 @@ def _load():
     lib.oracle_tree_expand.restype = i32
     lib.oracle_tree_prune.argtypes = [P, P, P, P, i32, i32, P, P, P, P, P]
     lib.oracle_tree_prune.restype = i32
+    lib.oracle_tree_merge.argtypes = [P, P, P, P, P, P, i32, i32, P, P, P, P, P]
+    lib.oracle_tree_merge.restype = i32
     lib.oracle_verify_nodes.argtypes = [P, P, P, P, P, i32, i32, i32, ctypes.c_float,
                                         ctypes.c_double, u64, i32, ctypes.c_double, P, P, P, P, P, P]
     lib.oracle_verify_nodes.restype = i32
@@ -291,4 +293,22 @@ def tree_prune(parents, tokens, scores, cand_offsets, keep: int):
                                _ptr(out["tokens"]), _ptr(out["kept"]), _ptr(out["n_out"]), _ptr(out["status"]))
     if rc != 0:
         raise ValueError(f"oracle_tree_prune: {rc}")
+    return out
+
+
+def tree_merge(parents_a, tokens_a, off_a, parents_b, tokens_b, off_b, cap: int = 128):
+    """Merge two speculators' token trees per request (oracle_tree_merge).
+    Returns dict(parents, tokens, map_b [B][cap], n_out [B], status [B])."""
+    lib = _load()
+    oa, ob = _c(off_a, np.int32), _c(off_b, np.int32)
+    B = oa.size - 1
+    out = {k: np.zeros((B, cap), np.int32) for k in ("parents", "tokens", "map_b")}
+    out["n_out"] = np.zeros(B, np.int32)
+    out["status"] = np.zeros(B, np.int32)
+    rc = lib.oracle_tree_merge(_ptr(_c(parents_a, np.int32)), _ptr(_c(tokens_a, np.int32)), _ptr(oa),
+                               _ptr(_c(parents_b, np.int32)), _ptr(_c(tokens_b, np.int32)), _ptr(ob),
+                               B, cap, _ptr(out["parents"]), _ptr(out["tokens"]), _ptr(out["map_b"]),
+                               _ptr(out["n_out"]), _ptr(out["status"]))
+    if rc != 0:
+        raise ValueError(f"oracle_tree_merge: {rc}")
     return out

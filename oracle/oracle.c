@@ -891,3 +891,68 @@ int oracle_tree_prune(const int32_t *parents, const int32_t *tokens, const doubl
   }
   return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Merging two speculators' token trees (developer article, §7.2 混合推测策略: */
+/* an LLM speculator's tree merged with an n-gram speculator's,             */
+/* tree.merge(other)).  Both trees of request b share the root (the last     */
+/* committed token; the root tokens are ignored).  The merged tree holds A's  */
+/* nodes unchanged (indices 0 .. n_a - 1), then every node of B whose token  */
+/* path from the root is not the path of a node already in the merged tree, */
+/* in B's index order; a B node whose path is already present maps to the   */
+/* present node of lowest merged index.  Outputs per request at stride cap:  */
+/* out_parents (-2 past n_out), out_tokens (-1 past n_out), map_b[b][i] =    */
+/* the merged index of B's node i (-1 past n_b, stride cap), n_out[b].       */
+/* Errors: OR_ERR_TREE (a tree with no node or more than cap nodes, or a      */
+/* merged tree larger than cap), OR_ERR_PARENT; outputs untouched then.      */
+/* ------------------------------------------------------------------------ */
+int oracle_tree_merge(const int32_t *parents_a, const int32_t *tokens_a, const int32_t *off_a,
+                      const int32_t *parents_b, const int32_t *tokens_b, const int32_t *off_b,
+                      int B, int cap, int32_t *out_parents, int32_t *out_tokens, int32_t *map_b,
+                      int32_t *n_out, int32_t *status) {
+  if (B < 1 || cap < 1) return OR_ERR_SHAPE;
+  int32_t *mp = (int32_t *)malloc(sizeof(int32_t) * (size_t)cap * 2);
+  int32_t *mt = (int32_t *)malloc(sizeof(int32_t) * (size_t)cap * 2);
+  int32_t *mb = (int32_t *)malloc(sizeof(int32_t) * (size_t)cap);
+  if (!mp || !mt || !mb) { free(mp); free(mt); free(mb); return OR_ERR_SHAPE; }
+  for (int b = 0; b < B; ++b) {
+    const int na = off_a[b + 1] - off_a[b], nb = off_b[b + 1] - off_b[b];
+    const int32_t *pa = parents_a + off_a[b], *ta = tokens_a + off_a[b];
+    const int32_t *pb = parents_b + off_b[b], *tb = tokens_b + off_b[b];
+    int st = OR_OK;
+    if (na < 1 || na > cap || nb < 1 || nb > cap) st = OR_ERR_TREE;
+    if (st == OR_OK && (check_parents(pa, na) != OR_OK || check_parents(pb, nb) != OR_OK))
+      st = OR_ERR_PARENT;
+    int n = 0;
+    if (st == OR_OK) {
+      /* A unchanged */
+      for (int j = 0; j < na; ++j) { mp[n] = pa[j]; mt[n] = ta[j]; ++n; }
+      mb[0] = 0; /* the roots coincide */
+      for (int i = 1; i < nb && st == OR_OK; ++i) {
+        const int parent = mb[pb[i]];
+        int found = -1;
+        for (int j = 1; j < n && found < 0; ++j)
+          if (mp[j] == parent && mt[j] == tb[i]) found = j;
+        if (found >= 0) {
+          mb[i] = found;
+        } else if (n == cap) {
+          st = OR_ERR_TREE;
+        } else {
+          mp[n] = parent;
+          mt[n] = tb[i];
+          mb[i] = n++;
+        }
+      }
+    }
+    status[b] = st;
+    if (st != OR_OK) continue;
+    for (int j = 0; j < cap; ++j) {
+      out_parents[(size_t)b * cap + j] = j < n ? mp[j] : -2;
+      out_tokens[(size_t)b * cap + j] = j < n ? mt[j] : -1;
+      map_b[(size_t)b * cap + j] = j < nb ? mb[j] : -1;
+    }
+    n_out[b] = n;
+  }
+  free(mp); free(mt); free(mb);
+  return OR_OK;
+}
