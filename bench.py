@@ -455,7 +455,8 @@ def run_native(args, rank, world, local_rank):
         # the rows after the hot path, on the headline workload's shapes
         result["next_rows"] = {"kv_compact": time_kv_compact(st, stream, chunk),
                                "tree_build": time_tree_build(w, stream, chunk),
-                               "top_p": time_verify_top_p(st, stream, chunk)}
+                               "top_p": time_verify_top_p(st, stream, chunk),
+                               "tree_merge": time_tree_merge(st, stream, chunk)}
     if not args.no_e2e:
         result["e2e"] = run_e2e(st, w, stream, args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -531,6 +532,49 @@ def time_kv_compact(st, stream, n, reps=3):
     moved = int(acc_h.sum()) * w.Hkv * w.D * w.k_cache.element_size() * 2 * 2
     return {"us": best * 1e3, "accept_len": acc_h.tolist(), "bytes": moved,
             "gbs": moved / (best * 1e-3) / 1e9,
+            "timing": f"CUDA graph of {n} launches, events on the launching stream"}
+
+
+def time_tree_merge(st, stream, n, reps=3):
+    """Merging an n-gram speculator's chain into the step's draft tree (the
+    mixed speculation of the developer article's deployment notes), timed
+    alone: a graph of n launches.  The chain follows the tree's first path
+    for two tokens, then leaves it for three new ones."""
+    import torch
+    ttv, w = st.ttv, st.w
+    par_a, tok_a = st.par, st.tok
+    path = [0]
+    for i in range(1, w.T):
+        if w.parents[i] == path[-1]:
+            path.append(i)
+    chain_tok = [0] + [int(w.tokens[i]) for i in path[1:3]] + [int(w.V) - 1 - j for j in range(3)]
+    par_b = torch.tensor([-1] + list(range(len(chain_tok) - 1)), dtype=torch.int32, device="cuda")
+    tok_b = torch.tensor(chain_tok, dtype=torch.int32, device="cuda")
+    off_b = torch.tensor([0, len(chain_tok)], dtype=torch.int32, device="cuda")
+    mst = torch.zeros(w.B, dtype=torch.int32, device="cuda")
+    if w.B != 1:
+        return None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n):
+            out = ttv.tree_merge(par_a, tok_a, st.off, par_b, tok_b, off_b, mst)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        best = ms if best is None else min(best, ms)
+    if (mst.cpu().numpy() != 0).any():
+        raise RuntimeError(f"tree_merge status {mst.cpu().tolist()}")
+    return {"us": best * 1e3, "nodes": int(out["n_out"][0].item()),
+            "shape": f"{w.T}-node draft tree + a {len(chain_tok)}-node n-gram chain",
             "timing": f"CUDA graph of {n} launches, events on the launching stream"}
 
 

@@ -333,6 +333,36 @@ int spec_tree_prune(const int32_t *parents, const int32_t *tokens, const float *
                     void *stream);
 
 /*
+ * spec_tree_merge — merging two speculators' token trees into one tree.
+ *
+ * Source: SpecInfer developer article, §7.2 混合推测策略 (mixed speculation:
+ * an LLM speculator's token tree merged with an n-gram speculator's,
+ * tree.merge(other), to widen coverage); the merged tree is then verified
+ * in one pass like any token tree.
+ *
+ * For request b, trees A (nodes [offsets_a[b], offsets_a[b+1])) and B share
+ * the root (the last committed token; root tokens are ignored).  The merged
+ * tree keeps A's nodes at indices 0 .. n_a - 1 unchanged; every node of B
+ * whose token path from the root is already present maps to the present
+ * node of lowest merged index, and the others are appended in B's order
+ * (so parent < index holds).  Outputs per request at stride
+ * SPEC_MAX_TREE_NODES:
+ *   out_parents [B][128]  merged parents (-2 past n_out[b])
+ *   out_tokens  [B][128]  merged tokens (-1 past n_out[b])
+ *   map_b       [B][128]  merged index of B's node i (-1 past n_b), e.g. to
+ *                         gather a speculator's draft rows for the merged tree
+ *   n_out       [B]
+ *   Ta, Tb: total nodes of A and of B (offsets_a[B], offsets_b[B]).
+ * Errors on the device (outputs untouched): SPEC_ERR_TREE_TOO_LARGE (a tree
+ * with no node or more than SPEC_MAX_TREE_NODES, or a merged tree larger
+ * than that), SPEC_ERR_BAD_PARENT.
+ */
+int spec_tree_merge(const int32_t *parents_a, const int32_t *tokens_a, const int32_t *offsets_a,
+                    const int32_t *parents_b, const int32_t *tokens_b, const int32_t *offsets_b,
+                    int B, int Ta, int Tb, int32_t *out_parents, int32_t *out_tokens,
+                    int32_t *map_b, int32_t *n_out, int32_t *status, void *stream);
+
+/*
  * spec_tree_verify_static — spec_tree_verify without a caller workspace.
  *
  * No counterpart in the paper: this is a library convenience.  It serves

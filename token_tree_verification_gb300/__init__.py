@@ -9,5 +9,5 @@ calls raise.
 from .binding import (  # noqa: F401
     SpecError, load, lib_path, build_tree_mask, tree_attn, tree_attn_workspace_size,
     tree_verify, tree_verify_workspace_size, make_verify_workspace, kv_compact, tree_expand, tree_prune, status_string,
-    philox_uniforms, STATUS,
+    philox_uniforms, tree_merge, STATUS,
 )

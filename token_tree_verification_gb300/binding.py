@@ -70,6 +70,8 @@ def load():
     lib.spec_tree_expand.restype = I
     lib.spec_tree_prune.argtypes = [P, P, P, P, I, I, P, P, P, P, P, P]
     lib.spec_tree_prune.restype = I
+    lib.spec_tree_merge.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.spec_tree_merge.restype = I
     lib.spec_philox_uniforms.argtypes = [U64, P, I, P, P]
     lib.spec_philox_uniforms.restype = I
     lib.spec_status_string.argtypes = [I]
@@ -293,4 +295,28 @@ def philox_uniforms(seed: int, counters, out=None, stream=None):
         out = torch.empty(n, dtype=torch.float32, device=counters.device)
     _check(lib.spec_philox_uniforms(int(seed) & (2**64 - 1), _ptr(counters), n, _ptr(out),
                                     _stream(stream)), "spec_philox_uniforms")
+    return out
+
+
+def tree_merge(parents_a, tokens_a, offsets_a, parents_b, tokens_b, offsets_b, status,
+               stream=None):
+    """Merge two speculators' token trees per request.  Returns dict(parents,
+    tokens, map_b [B][128], n_out [B]) of device tensors."""
+    lib = load()
+    for t, name in ((parents_a, "parents_a"), (tokens_a, "tokens_a"), (offsets_a, "offsets_a"),
+                    (parents_b, "parents_b"), (tokens_b, "tokens_b"), (offsets_b, "offsets_b"),
+                    (status, "status")):
+        _dev(t, torch.int32, name)
+    B = offsets_a.numel() - 1
+    if offsets_b.numel() - 1 != B:
+        raise ValueError("both trees need the same number of requests")
+    dev_ = parents_a.device
+    out = {k: torch.empty((B, MAX_TREE_NODES), dtype=torch.int32, device=dev_)
+           for k in ("parents", "tokens", "map_b")}
+    out["n_out"] = torch.empty(B, dtype=torch.int32, device=dev_)
+    _check(lib.spec_tree_merge(_ptr(parents_a), _ptr(tokens_a), _ptr(offsets_a), _ptr(parents_b),
+                               _ptr(tokens_b), _ptr(offsets_b), B, parents_a.numel(),
+                               parents_b.numel(), _ptr(out["parents"]), _ptr(out["tokens"]),
+                               _ptr(out["map_b"]), _ptr(out["n_out"]), _ptr(status),
+                               _stream(stream)), "spec_tree_merge")
     return out
