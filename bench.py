@@ -385,8 +385,8 @@ def run_native(args, rank, world, local_rank):
 
     # per-kernel durations: each kernel alone, back to back in a graph, on the
     # same stream and over the same rotating inputs
-    d_mask, d_attn, d_ver = per_kernel_graph_times(st, stream, chunk)
-    _, w_attn, w_ver = per_kernel_graph_times(st, stream, chunk, rotate=False)
+    d_mask, d_attn, d_ver, d_attn_step = per_kernel_graph_times(st, stream, chunk)
+    _, w_attn, w_ver, _ = per_kernel_graph_times(st, stream, chunk, rotate=False)
     kernel_timing = ("each kernel kind timed alone: a CUDA graph of %d launches over the rotating "
                      "inputs, CUDA events on the launching stream" % chunk)
 
@@ -438,7 +438,9 @@ def run_native(args, rank, world, local_rank):
         "roofline": roof,
         "kernels": {
             "mask": {"ms": mask_ms, "bytes": mb},
-            "attn": {"ms": attn_ms, "bytes": ab, "gbs": achieved},
+            "attn": {"ms": attn_ms, "bytes": ab, "gbs": achieved, "plan": "whole GPU"},
+            "attn_in_step": {"ms": float(d_attn_step.mean()), "max_ctas": st.attn_ctas,
+                             "note": "the step's launch, planned for the SMs verification leaves"},
             "verify": {"ms": ver_ms, "bytes": vb, "gbs": vb / (ver_ms * 1e-3) / 1e9},
             "step_gbs": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9,
             "step_frac": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9 / peak,
@@ -674,16 +676,21 @@ def per_kernel_graph_times(st, stream, n, reps=3, rotate=True):
     import torch
     ttv, w = st.ttv, st.w
     out = []
-    for kind in range(3):
+    for kind in range(4):
+        if kind == 3 and not st.attn_ctas:
+            out.append(out[1])
+            continue
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
                 c = st.copies[i % len(st.copies) if rotate else 0]
                 if kind == 0:
                     ttv.build_tree_mask(st.par, st.off, st.status, mask=st.mask, depth=st.depth)
-                elif kind == 1:
+                elif kind in (1, 3):
+                    # kind 1: planned for the whole GPU; kind 3: as the step plans it
                     ttv.tree_attn(c["q"], c["k"], c["v"], st.pl, st.off, st.mask, st.max_prefix,
-                                  st.status, o=st.o, workspace=st.ws_attn)
+                                  st.status, o=st.o, workspace=st.ws_attn,
+                                  max_ctas=st.attn_ctas if kind == 3 else 0)
                 else:
                     ttv.tree_verify(c["tl"], c["dl"], st.tok, st.par, st.off, w.temperature,
                                     st.seed + i, st.W, st.status, st.ws, outputs=st.outs)

@@ -82,21 +82,33 @@ tree_merge_kernel(const int32_t *parents_a, const int32_t *tokens_a, const int32
   }
   __syncthreads();
   const int maxd = sm.maxd;
+  const int lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kMergeThreads / 32;
   for (int d = 1; d <= maxd; ++d) {
-    for (int i = tid; i < nb; i += kMergeThreads) {
+    // one warp per node of this level; its lanes search A's nodes, then B's
+    // earlier nodes, four at a time (the lowest index wins)
+    for (int i = warp; i < nb; i += kWarps) {
       if (sm.db[i] != d) continue;
       const int pr = sm.rep[sm.pb[i]];   // resolved at level d - 1
       const int tk = sm.tb[i];
       int r = -1;
-      if (pr < na)
-        for (int j = 1; j < na && r < 0; ++j)
-          if (sm.pa[j] == pr && sm.ta[j] == tk) r = j;
-      if (r < 0) {
-        // the first node of this level of B with the same parent and token
-        for (int i2 = 1; i2 <= i && r < 0; ++i2)
-          if (sm.db[i2] == d && sm.tb[i2] == tk && sm.rep[sm.pb[i2]] == pr) r = na + i2;
+#pragma unroll
+      for (int s = 0; s < kMergeCap / 32 && r < 0; ++s) {
+        const int j = s * 32 + lane;
+        const bool hit = pr < na && j >= 1 && j < na && sm.pa[j] == pr && sm.ta[j] == tk;
+        const uint32_t m = __ballot_sync(0xffffffffu, hit);
+        if (m) r = s * 32 + __ffs(m) - 1;
       }
-      sm.rep[i] = r;
+#pragma unroll
+      for (int s = 0; s < kMergeCap / 32 && r < 0; ++s) {
+        // the first node of this level of B with the same parent and token
+        const int i2 = s * 32 + lane;
+        const bool hit = i2 >= 1 && i2 <= i && sm.db[i2] == d && sm.tb[i2] == tk &&
+                         sm.rep[sm.pb[i2]] == pr;
+        const uint32_t m = __ballot_sync(0xffffffffu, hit);
+        if (m) r = na + s * 32 + __ffs(m) - 1;
+      }
+      if (lane == 0) sm.rep[i] = r;
     }
     __syncthreads();
   }
