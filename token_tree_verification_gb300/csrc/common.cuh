@@ -51,6 +51,21 @@ inline int current_device() {
   return (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) ? dev : -1;
 }
 
+// SMs of the current device (launch plans size grids by it); 152 (GB300)
+// when no device can be queried.
+inline int sm_count() {
+  static std::atomic<int> n[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 152;
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return 152;
+    n[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 // A kernel needs its dynamic shared-memory limit raised before a launch with
 // more than 48 KB, on each device it runs on.  `granted[dev]` holds the
 // largest limit set on device dev; the limit only ever grows, and changes

@@ -263,9 +263,13 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
     ts.timeout = 1;
     if (tid == 0) report(a.status, c.b, SPEC_ERR_TIMEOUT);
   }
+  // A wait that ran out anywhere in the CTA: its threads may hold different
+  // decisions, so the CTA takes one path from here on (no draw, no published
+  // decision; rank 0 arrives with the error bit).
+  const bool cta_timeout = __syncthreads_or(!ok);
 
   int writer = 0;  // the CTA of the group that publishes the node's results
-  if (!c.err) {
+  if (!c.err && !cta_timeout) {
     // ---- V3: when every child is rejected (or u is a leaf), the token
     //      emitted on stopping here: inverse CDF of r ∝ max(0, p - c q)
     if (stop == k) {
@@ -366,16 +370,17 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
     }
     // every CTA computed the same decisions; the writer publishes them
     if (rank == writer && tid < k) a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
-  } else if (rank == 0 && tid == 0 && c.b >= 0) {
+  } else if (c.err && rank == 0 && tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }
   if (rank == writer) {
     // the node's flags and fallback are written; near-ties among the tested children
+    const bool decided = !c.err && !cta_timeout;
     const int child_ties =
-        __syncthreads_count(!c.err && tid < k && tid <= stop && (my_flag & kFlagTie) != 0);
+        __syncthreads_count(decided && tid < k && tid <= stop && (my_flag & kFlagTie) != 0);
     const int fb = ts.stop_fb;
-    arrive_and_walk(a, c, ts, (!c.err && stop == k) ? (fb & 0x7fffffff) : -1,
-                    child_ties + ((fb >> 31) & 1), ts.timeout != 0);
+    arrive_and_walk(a, c, ts, (decided && stop == k) ? (fb & 0x7fffffff) : -1,
+                    child_ties + ((fb >> 31) & 1), cta_timeout);
   }
   if (CS > 1) cluster_wait();
 }
@@ -438,6 +443,7 @@ int verify_entry(const float *target_logits, const float *draft_logits, const in
   args.seed = seed;
   args.wait_ns = wait_ns;
   args.drop_request = drop_request;
+  args.prefetch_rows = 0;
   args.accept_len = accept_len;
   args.path_nodes = path_nodes;
   args.out_tokens = out_tokens;

@@ -40,6 +40,8 @@ struct VerifyArgs {
   uint32_t *done;      // [B] arrival counters (zero between calls)
   uint64_t wait_ns;    // limit of every bounded wait (kWaitLimitNs outside the failure test)
   int drop_request;    // failure test: this request's first exchange is withheld (-1: none)
+  int prefetch_rows;   // stochastic kernel: every node prefetches its target slice into L2
+                       // at once (set when all the launch's CTAs are resident together)
 };
 
 // A node's tree context, staged in shared memory by load_tree().
@@ -537,6 +539,31 @@ static __device__ void stage_request(const NodeCtx &c, int t, TreeSmem &ts) {
   __syncthreads();
 }
 
+// The root's arrival when its walk is known to end at the root (every child
+// of the root rejected, a valid tree, no wait of the CTA ran out, the path
+// fits the output rows): it needs no other node's results, so the CTA that
+// will draw the emitted token arrives before drawing it, and the atomic's
+// round trip overlaps the draw.  Called by every thread of that CTA;
+// `done` holds in warp 0, `prev` (the arrival word before) in thread 0.
+struct RootArrival {
+  bool done;
+  uint32_t prev;
+};
+
+static __device__ RootArrival root_arrive_early(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts) {
+  RootArrival r{false, 0u};
+  const int tid = threadIdx.x;
+  if (tid < 32) r.done = path_fits(a, c.b, c.n, ts.par);
+  if (tid == 0 && r.done) {
+    // nothing this node wrote is read by another node: no ordering needed
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(r.prev)
+                 : "l"(a.done + c.b), "r"(1u | kArriveRootDone)
+                 : "memory");
+  }
+  return r;
+}
+
 // Called by every thread of the one CTA per node that publishes the node's
 // results, once they are written (flags of its children, its fallback).
 // `root_stop_token` >= 0 at the root when no child of the root was accepted:
@@ -549,11 +576,16 @@ static __device__ void stage_request(const NodeCtx &c, int t, TreeSmem &ts) {
 // node of the request arrives exactly once).
 static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts,
                                        int root_stop_token, int root_stop_ties, bool timed_out,
-                                       bool lazy_leaves = false) {
+                                       bool lazy_leaves = false,
+                                       const RootArrival &early = RootArrival{false, 0u}) {
   const int tid = threadIdx.x;
   bool root_done = false;
-  if (tid < 32 && c.count && !c.err && !timed_out && c.u == 0 && root_stop_token >= 0 &&
-      path_fits(a, c.b, c.n, ts.par)) {
+  if (tid < 32 && early.done) {
+    // the root arrived early (root_arrive_early): its outputs alone remain
+    write_root_stop(a, c.b, root_stop_token, root_stop_ties);
+    root_done = true;
+  } else if (tid < 32 && c.count && !c.err && !timed_out && c.u == 0 && root_stop_token >= 0 &&
+             path_fits(a, c.b, c.n, ts.par)) {
     write_root_stop(a, c.b, root_stop_token, root_stop_ties);
     root_done = true;
   }
@@ -565,7 +597,9 @@ static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, Tr
       const uint32_t add = 1u | ((timed_out || c.err) ? kArriveErr : 0u) |
                            (root_done ? kArriveRootDone : 0u);
       uint32_t prev;
-      if (root_done) {
+      if (early.done) {
+        prev = early.prev;
+      } else if (root_done) {
         // nothing this node wrote is read by another node: no ordering needed
         asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;"
                      : "=r"(prev)

@@ -170,6 +170,32 @@ __device__ __forceinline__ float pick4(const float4 v, int c) {
   return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
 }
 
+// The warp totals of the eight steps' values ls[0..7] at once: a transposed
+// butterfly (each exchange halves the values a lane carries) leaves step m's
+// total in lanes 4m .. 4m+3 and returns it there.  Every total adds the same
+// pairs in the same order as warp_sum, so it is bit-identical to it.
+__device__ __forceinline__ float step_totals(const float (&ls)[kRVec], int lane) {
+  static_assert(kRVec == 8, "three halving exchanges");
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float v4[4], v2[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? ls[4 + i] : ls[i];
+    const float give = b4 ? ls[i] : ls[4 + i];
+    v4[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? v4[2 + i] : v4[i];
+    const float give = b3 ? v4[i] : v4[2 + i];
+    v2[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+  }
+  float v = (b2 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? v2[0] : v2[1], 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v;
+}
+
 __device__ __forceinline__ float warp_scan(float v, int lane) {  // inclusive
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -221,9 +247,11 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   float4 xp[kRVec], xq[kRVec];
   if constexpr (TOPP) {
     load_row(trow, base, end, vec, xp);
-  } else if (tid == 0 && vec && end > v0) {
+  } else if (a.prefetch_rows && tid == 0 && vec && end > v0) {
     // the slice goes to L2 at once, before the node knows whether it is a
-    // leaf (whose row is read only if the walk ends there)
+    // leaf (whose row is read only if the walk ends there); only when every
+    // CTA of the launch is resident, since a leaf's prefetch otherwise takes
+    // bandwidth from the nodes still running
     const uint32_t bytes = (static_cast<uint32_t>(end - v0) * 4u) & ~15u;
     if (bytes > 0)
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
@@ -649,9 +677,17 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     ts.timeout = 1;
     if (tid == 0) report(a.status, c.b, SPEC_ERR_TIMEOUT);
   }
+  // A wait that ran out anywhere in the CTA: its threads may have taken
+  // different decisions (a thread whose wait ran out skips the later waits
+  // and may read the node's scalars before they are written), so the CTA
+  // takes one path from here on: no draw, no published decision, and rank 0
+  // arrives with the error bit.  Without a timeout every thread holds the
+  // same decisions and the draw's barriers are met by all of them.
+  const bool cta_timeout = __syncthreads_or(!ok);
 
   int writer = 0;  // the CTA of the group that publishes the node's results
-  if (!c.err) {
+  RootArrival early{false, 0u};
+  if (!c.err && !cta_timeout) {
     // ---- V3: when every child is rejected (or u is a leaf), the token
     //      emitted on stopping here: inverse CDF of r ∝ max(0, p - c q)
     if (stop == k) {
@@ -693,6 +729,8 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         if (owner < 0) owner = 0;
       }
       writer = owner;
+      // the root whose walk ends here arrives before its draw
+      if (rank == owner && c.u == 0 && c.count) early = root_arrive_early(a, c, ts);
       if (rank == owner) {
         // level 1: the slice's 16 warp ranges
         const float v1 = lane < kRWarps ? mass(rank, lane) : 0.f;
@@ -705,11 +743,15 @@ tree_verify_reg_kernel(const VerifyArgs a) {
           float ls[kRVec];
 #pragma unroll
           for (int m = 0; m < kRVec; ++m) ls[m] = sum4_resid(xp[m], xq[m], c_prev);
+          const float own = step_totals(ls, lane);
+          float cs_all[kRVec];
+#pragma unroll
+          for (int m = 0; m < kRVec; ++m) cs_all[m] = __shfl_sync(0xffffffffu, own, 4 * m);
           int ms = -1;
           float before = run2;
 #pragma unroll
           for (int m = 0; m < kRVec; ++m) {
-            const float cs_ = warp_sum(ls[m]);
+            const float cs_ = cs_all[m];
             if (ms < 0 && run2 + cs_ > target) {
               ms = m;
               before = run2;
@@ -801,21 +843,24 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     }
     // every CTA computed the same decisions; the writer publishes them
     if (rank == writer && tid < k) a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
-  } else if (rank == 0 && tid == 0 && c.b >= 0) {
+  } else if (c.err && rank == 0 && tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }
   if (rank == writer) {
     // the node's flags and fallback are written; near-ties among the tested children
+    const bool decided = !c.err && !cta_timeout;
     const int child_ties =
-        __syncthreads_count(!c.err && tid < k && tid <= stop && (my_flag & kFlagTie) != 0);
+        __syncthreads_count(decided && tid < k && tid <= stop && (my_flag & kFlagTie) != 0);
     const int fb = ts.stop_fb;
-    arrive_and_walk(a, c, ts, (!c.err && stop == k) ? (fb & 0x7fffffff) : -1,
-                    child_ties + ((fb >> 31) & 1), ts.timeout != 0, !TOPP);
+    arrive_and_walk(a, c, ts, (decided && stop == k) ? (fb & 0x7fffffff) : -1,
+                    child_ties + ((fb >> 31) & 1), cta_timeout, !TOPP, early);
   }
   if (CS > 1) cluster_wait();
 }
 
-int launch_verify_reg(const VerifyArgs &args, int cs, bool top_p, cudaStream_t stream) {
+int launch_verify_reg(const VerifyArgs &args_in, int cs, bool top_p, cudaStream_t stream) {
+  VerifyArgs args = args_in;
+  args.prefetch_rows = static_cast<long long>(args.T) * cs <= sm_count() ? 1 : 0;   // one CTA per SM
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(args.T) * cs, 1, 1);
   cfg.blockDim = dim3(kRThreads, 1, 1);
