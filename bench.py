@@ -256,18 +256,21 @@ class Step:
                     self.seed + i, self.outs, stream)
 
     def launch(self, q, k, v, tl, dl, par, off, tok, pl, seed, outs, stream=None):
-        """One step: the mask then tree attention on ``stream``, and
-        verification on a second stream forked from it and joined back.
-        Verification reads only the logits and the tree, attention only Q, the
-        caches and the mask, so the two run side by side (under graph capture
-        the fork and join become two branches of the graph)."""
+        """One step: tree attention on ``stream``, building its rows' ancestor
+        sets from the parent array itself, and on a second stream forked from
+        it and joined back the mask kernel (its mask and depths, for the
+        consumers after attention) then verification.  Verification reads only
+        the logits and the tree, attention only Q, the caches and the
+        parents, so the branches run side by side (under graph capture the
+        fork and join become two branches of the graph)."""
         torch, ttv, w = self.torch, self.ttv, self.w
         cur = torch.cuda.current_stream() if stream is None else stream
         self.side.wait_stream(cur)
-        ttv.build_tree_mask(par, off, self.status, mask=self.mask, depth=self.depth, stream=cur)
-        ttv.tree_attn(q, k, v, pl, off, self.mask, self.max_prefix, self.status, o=self.o,
-                      workspace=self.ws_attn, stream=cur, max_ctas=self.attn_ctas)
+        ttv.tree_attn(q, k, v, pl, off, None, self.max_prefix, self.status, o=self.o,
+                      workspace=self.ws_attn, stream=cur, max_ctas=self.attn_ctas, parents=par)
         with torch.cuda.stream(self.side):
+            ttv.build_tree_mask(par, off, self.status, mask=self.mask, depth=self.depth,
+                                stream=self.side)
             ttv.tree_verify(tl, dl, tok, par, off, w.temperature, seed, self.W, self.status, self.ws,
                             outputs=outs, stream=self.side)
         cur.wait_stream(self.side)
@@ -440,7 +443,8 @@ def run_native(args, rank, world, local_rank):
             "mask": {"ms": mask_ms, "bytes": mb},
             "attn": {"ms": attn_ms, "bytes": ab, "gbs": achieved, "plan": "whole GPU"},
             "attn_in_step": {"ms": float(d_attn_step.mean()), "max_ctas": st.attn_ctas,
-                             "note": "the step's launch, planned for the SMs verification leaves"},
+                             "note": "the step's launch: ancestor sets from the parents, "
+                                     "planned for the SMs verification leaves"},
             "verify": {"ms": ver_ms, "bytes": vb, "gbs": vb / (ver_ms * 1e-3) / 1e9},
             "step_gbs": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9,
             "step_frac": (ab + vb + mb) / (ms_per_step * 1e-3) / 1e9 / peak,
@@ -677,20 +681,21 @@ def per_kernel_graph_times(st, stream, n, reps=3, rotate=True):
     ttv, w = st.ttv, st.w
     out = []
     for kind in range(4):
-        if kind == 3 and not st.attn_ctas:
-            out.append(out[1])
-            continue
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
                 c = st.copies[i % len(st.copies) if rotate else 0]
                 if kind == 0:
                     ttv.build_tree_mask(st.par, st.off, st.status, mask=st.mask, depth=st.depth)
-                elif kind in (1, 3):
-                    # kind 1: planned for the whole GPU; kind 3: as the step plans it
+                elif kind == 1:
+                    # planned for the whole GPU, from the mask array
                     ttv.tree_attn(c["q"], c["k"], c["v"], st.pl, st.off, st.mask, st.max_prefix,
-                                  st.status, o=st.o, workspace=st.ws_attn,
-                                  max_ctas=st.attn_ctas if kind == 3 else 0)
+                                  st.status, o=st.o, workspace=st.ws_attn)
+                elif kind == 3:
+                    # as the step launches it: from the parents, for the SMs verification leaves
+                    ttv.tree_attn(c["q"], c["k"], c["v"], st.pl, st.off, None, st.max_prefix,
+                                  st.status, o=st.o, workspace=st.ws_attn, max_ctas=st.attn_ctas,
+                                  parents=st.par)
                 else:
                     ttv.tree_verify(c["tl"], c["dl"], st.tok, st.par, st.off, w.temperature,
                                     st.seed + i, st.W, st.status, st.ws, outputs=st.outs)

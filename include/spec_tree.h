@@ -31,7 +31,10 @@
  *    call leaves the outputs of a request untouched when it finds an error
  *    for that request itself; codes that other calls wrote into `status`
  *    (which may run concurrently on other streams) do not affect it.  After
- *    SPEC_ERR_TIMEOUT (never expected) the request's outputs are unspecified.
+ *    SPEC_ERR_TIMEOUT (never expected) the request's outputs are unspecified,
+ *    and a verification workspace used by that call must be zero-filled
+ *    again before its next use (a node whose CTAs disagree on the timeout
+ *    may leave its request's arrival counter off zero).
  *  - A batch is packed ragged: request b owns global nodes
  *    [tree_offsets[b], tree_offsets[b+1]) with tree_offsets[0] = 0 and
  *    tree_offsets[B] = T.  Node indices inside a request (parents, path
@@ -143,19 +146,32 @@ int spec_tree_attn(const void *q, const void *k_cache, const void *v_cache, void
                    void *stream);
 
 /*
- * spec_tree_attn_ex — spec_tree_attn for a caller that runs other kernels
- * beside it (another stream, another graph branch): the bf16 path plans its
- * key splits (the CTAs of one query block) for at most max_ctas CTAs resident
- * at once instead of the whole GPU, so that the other work keeps the SMs it
- * needs.  max_ctas == 0 means the device's SM count (spec_tree_attn);
- * negative max_ctas is SPEC_ERR_SHAPE.  The result is the same; only the
- * launch shape changes.  The fp32 path ignores max_ctas.
+ * spec_tree_attn_ex — spec_tree_attn with two options for a caller that runs
+ * other kernels beside it (another stream, another graph branch).
+ *
+ *   max_ctas  the bf16 path plans its key splits (the CTAs of one query
+ *             block) for at most max_ctas CTAs resident at once instead of
+ *             the whole GPU, so that the other work keeps the SMs it needs.
+ *             0 means the device's SM count (spec_tree_attn); negative is
+ *             SPEC_ERR_SHAPE.  The result is the same; only the launch shape
+ *             changes.  The fp32 path ignores it.
+ *   parents   [T] int32, the request-local parent array of spec_build_tree_mask
+ *             (device).  Read only when mask is NULL: then every row's
+ *             ancestor set is built inside the kernel from the parents (the
+ *             SpecInfer developer article's topology mask, §2.1), so the mask
+ *             kernel need not run before this one.  The result equals the
+ *             call with the mask spec_build_tree_mask writes for the same
+ *             parents.  A parent that is not below its node, or a root whose
+ *             parent is not -1, reports SPEC_ERR_BAD_PARENT for its request
+ *             (the walk stops there; the request's outputs are then
+ *             unspecified).  mask and parents both NULL is SPEC_ERR_NULL.
  */
 int spec_tree_attn_ex(const void *q, const void *k_cache, const void *v_cache, void *o, int dtype,
                       int B, int T, int Hq, int Hkv, int D, int S_cap, int max_prefix,
                       const int32_t *prefix_lens, const int32_t *tree_offsets,
-                      const uint32_t *mask, float softmax_scale, void *workspace,
-                      size_t workspace_bytes, int max_ctas, int32_t *status, void *stream);
+                      const uint32_t *mask, const int32_t *parents, float softmax_scale,
+                      void *workspace, size_t workspace_bytes, int max_ctas, int32_t *status,
+                      void *stream);
 
 /*
  * Bytes of scratch spec_tree_verify needs: per-node acceptance flags and

@@ -136,3 +136,75 @@ def test_device_errors(gpu_lib):
     lo, hi = w.offsets[1], w.offsets[2]
     assert (o[lo:hi].float() == 7.0).all()        # untouched
     assert not (o[: w.offsets[1]].float() == 7.0).all()
+
+
+def gpu_attn_parents(w, status=None, max_ctas=0):
+    """spec_tree_attn_ex with no mask array: the kernel builds every row's
+    ancestor set from the parent array."""
+    import token_tree_verification_gb300 as ttv
+    from parity import dev
+    if status is None:
+        status = torch.zeros(w.B, dtype=torch.int32, device="cuda")
+    o = ttv.tree_attn(w.q.cuda(), w.k_cache.cuda(), w.v_cache.cuda(), dev(w.prefix_lens, torch.int32),
+                      dev(w.offsets, torch.int32), None, int(w.prefix_lens.max()), status,
+                      max_ctas=max_ctas, parents=dev(w.parents, torch.int32))
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy().astype(np.float64), status.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", dict(B=3, L=77, N=20, depth=4, width=4, Hq=8, Hkv=2, D=128)),        # fp32 kernel
+    ("llama70b_gqa", dict(B=1, Hq=4, Hkv=4, D=128, L=0, N=8, depth=5, width=4, V=64)),
+    ("llama70b_gqa", dict(B=3, Hq=8, Hkv=2, D=64, L=200, N=33, depth=5, width=4, V=64)),
+    ("llama70b_gqa", dict(B=2, Hq=16, Hkv=2, D=128, L=129, N=40, depth=5, width=8, V=64)),
+    ("llama70b_gqa", dict(B=1, Hq=4, Hkv=2, D=128, L=300, N=128, depth=5, width=8, V=64)),
+])
+def test_parents_path(gpu_lib, kernel, name, kw):
+    """Masks built in the kernel from the parents: outputs bit-identical to
+    the mask-array path (the same ancestor bits) and within tolerance of the
+    oracle."""
+    if name == "tiny" and kernel == "mma":
+        pytest.skip("fp32 inputs take the fp32 kernel either way")
+    w = synthetic.make_workload(name, seed=11, **kw)
+    got_m, st_m = gpu_attn(w)
+    got_p, st_p = gpu_attn_parents(w)
+    assert (st_m == 0).all() and (st_p == 0).all()
+    assert np.array_equal(got_m, got_p)
+    assert_attn_close(got_p, full_oracle(w), f"parents {name} {kw}")
+
+
+def test_parents_path_llama7b_step_launch(gpu_lib):
+    """The 7B workload as the timed step launches it: parents, no mask array,
+    the split plan for the SMs verification leaves.  Bit-identical to the
+    mask-array launch with the same plan (another split count rounds the
+    merge differently), and within tolerance of the oracle on every row."""
+    import token_tree_verification_gb300 as ttv
+    from parity import dev
+    w = synthetic.make_workload("llama7b", seed=0, device="cuda")
+    status = torch.zeros(w.B, dtype=torch.int32, device="cuda")
+    mask, _ = ttv.build_tree_mask(dev(w.parents, torch.int32), dev(w.offsets, torch.int32), status)
+    o_m = ttv.tree_attn(w.q.cuda(), w.k_cache.cuda(), w.v_cache.cuda(), dev(w.prefix_lens, torch.int32),
+                        dev(w.offsets, torch.int32), mask, int(w.prefix_lens.max()), status, max_ctas=118)
+    torch.cuda.synchronize()
+    got_p, st = gpu_attn_parents(w, max_ctas=118)
+    assert (st == 0).all() and (status.cpu().numpy() == 0).all()
+    assert np.array_equal(o_m.float().cpu().numpy().astype(np.float64), got_p)
+    ref = oracle_attn_rows(w, np.arange(w.T * w.Hq))
+    assert_attn_close(got_p.reshape(-1, w.D), ref, "llama7b, step launch")
+
+
+def test_parents_path_bad_parent(gpu_lib, kernel):
+    """A parent that is not below its node is reported for its request only;
+    the other requests' rows are unaffected."""
+    w = synthetic.make_workload("llama70b_gqa", seed=12, B=3, Hq=4, Hkv=2, D=128, L=90, N=12,
+                                depth=3, width=4, V=64)
+    ref_good, _ = gpu_attn_parents(w)
+    par = w.parents.copy()
+    lo = w.offsets[1]
+    par[lo + 5] = 7          # forward parent in request 1
+    w.parents = par
+    got, st = gpu_attn_parents(w)
+    assert st.tolist() == [0, -5, 0]   # SPEC_ERR_BAD_PARENT
+    for b in (0, 2):
+        a, z = w.offsets[b], w.offsets[b + 1]
+        assert np.array_equal(got[a:z], ref_good[a:z])

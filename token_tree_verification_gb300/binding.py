@@ -56,7 +56,7 @@ def load():
     lib.spec_tree_attn_workspace_size.restype = SZ
     lib.spec_tree_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, F, P, SZ, P, P]
     lib.spec_tree_attn.restype = I
-    lib.spec_tree_attn_ex.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, F, P, SZ, I, P, P]
+    lib.spec_tree_attn_ex.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, F, P, SZ, I, P, P]
     lib.spec_tree_attn_ex.restype = I
     lib.spec_tree_verify_workspace_size.argtypes = [I, I, I]
     lib.spec_tree_verify_workspace_size.restype = SZ
@@ -133,10 +133,12 @@ def tree_attn_workspace_size(B, T, Hq, Hkv, D, max_prefix) -> int:
 
 
 def tree_attn(q, k_cache, v_cache, prefix_lens, offsets, mask, max_prefix, status, o=None,
-              softmax_scale: float = 0.0, workspace=None, stream=None, max_ctas: int = 0):
+              softmax_scale: float = 0.0, workspace=None, stream=None, max_ctas: int = 0,
+              parents=None):
     """Steps A2-A3.  q [T, Hq, D]; k_cache, v_cache [B, Hkv, S_cap, D]; bf16 or fp32.
-    ``max_ctas`` > 0 plans the launch for that many resident CTAs
-    (spec_tree_attn_ex), leaving the other SMs to concurrent work."""
+    ``max_ctas`` > 0 plans the launch for that many resident CTAs, leaving
+    the other SMs to concurrent work; with ``mask=None`` the kernel builds
+    every row's ancestor set from ``parents`` (both spec_tree_attn_ex)."""
     lib = load()
     dt = q.dtype
     if dt not in (torch.bfloat16, torch.float32):
@@ -146,7 +148,12 @@ def tree_attn(q, k_cache, v_cache, prefix_lens, offsets, mask, max_prefix, statu
     _dev(v_cache, dt, "v_cache")
     _dev(prefix_lens, torch.int32, "prefix_lens")
     _dev(offsets, torch.int32, "offsets")
-    _dev(mask, torch.int32, "mask")
+    if mask is None:
+        if parents is None:
+            raise ValueError("tree_attn needs a mask or the parent array")
+        _dev(parents, torch.int32, "parents")
+    else:
+        _dev(mask, torch.int32, "mask")
     _dev(status, torch.int32, "status")
     T, Hq, D = q.shape
     B, Hkv, S_cap, D2 = k_cache.shape
@@ -160,7 +167,8 @@ def tree_attn(q, k_cache, v_cache, prefix_lens, offsets, mask, max_prefix, statu
     _check(lib.spec_tree_attn_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
                                  SPEC_BF16 if dt == torch.bfloat16 else SPEC_F32, B, T, Hq, Hkv, D,
                                  S_cap, int(max_prefix), _ptr(prefix_lens), _ptr(offsets),
-                                 _ptr(mask), float(softmax_scale), _ptr(workspace),
+                                 _ptr(mask), _ptr(parents) if mask is None else None,
+                                 float(softmax_scale), _ptr(workspace),
                                  0 if workspace is None else workspace.numel(), int(max_ctas),
                                  _ptr(status), _stream(stream)), "spec_tree_attn_ex")
     return o

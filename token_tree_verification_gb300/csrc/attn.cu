@@ -172,7 +172,7 @@ tree_attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
     for (int h2 = 0; h2 < 2; ++h2) {
       const int r = row0 + r_local[h2];
       msk[h2] = make_uint4(0, 0, 0, 0);
-      if (r < rows_total) msk[h2] = clip_mask(__ldg(a.mask + R.lo + r / a.G), R.n);
+      if (r < rows_total) msk[h2] = node_mask(a, R, b, R.lo + r / a.G);
     }
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
@@ -401,7 +401,7 @@ tree_attn_f32_kernel(const AttnArgs a) {
     return;
   }
   const int g = h / a.G;
-  const uint4 m = clip_mask(__ldg(a.mask + t), R.n);
+  const uint4 m = node_mask(a, R, b, t);
   const float *q = static_cast<const float *>(a.q) + (static_cast<size_t>(t) * a.Hq + h) * D;
   const size_t kv_off = (static_cast<size_t>(b) * a.Hkv + g) * a.S_cap * D;
   const float *kc = static_cast<const float *>(a.k) + kv_off;
@@ -514,21 +514,6 @@ bool use_mma_kernel() {
   return e != nullptr && strcmp(e, "mma") == 0;
 }
 
-// SMs of the current device (the split plan sizes grids by it); 152 (GB300)
-// when no device can be queried.
-int sm_count() {
-  static std::atomic<int> n[spec::kMaxDevices];
-  const int dev = spec::current_device();
-  if (dev < 0) return 152;
-  int v = n[dev].load(std::memory_order_relaxed);
-  if (v == 0) {
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      return 152;
-    n[dev].store(v, std::memory_order_relaxed);
-  }
-  return v;
-}
-
 template <int D>
 int launch_mma(const spec::AttnArgs &args, int max_prefix, int T, cudaStream_t stream) {
   using C = spec::MmaCfg<D>;
@@ -554,7 +539,7 @@ int launch_mma(const spec::AttnArgs &args, int max_prefix, int T, cudaStream_t s
   const long long max_keys = static_cast<long long>(max_prefix) + max_nodes;
   const int tiles_max = static_cast<int>((max_keys + spec::kKeyTile - 1) / spec::kKeyTile);
   const long long units = static_cast<long long>(rowblocks) * args.B * args.Hkv;
-  const long long slots = static_cast<long long>(per_sm) * sm_count();
+  const long long slots = static_cast<long long>(per_sm) * spec::sm_count();
   // splits: enough that no CTA streams more than ~16 tiles, then more while
   // the grid still fits in one wave
   int cs = 1;
@@ -591,7 +576,7 @@ extern "C" int spec_tree_attn(const void *q, const void *k_cache, const void *v_
                               float softmax_scale, void *workspace, size_t workspace_bytes,
                               int32_t *status, void *stream) {
   return spec_tree_attn_ex(q, k_cache, v_cache, o, dtype, B, T, Hq, Hkv, D, S_cap, max_prefix,
-                           prefix_lens, tree_offsets, mask, softmax_scale, workspace,
+                           prefix_lens, tree_offsets, mask, nullptr, softmax_scale, workspace,
                            workspace_bytes, 0, status, stream);
 }
 
@@ -599,10 +584,12 @@ extern "C" int spec_tree_attn_ex(const void *q, const void *k_cache, const void 
                                  int dtype, int B, int T, int Hq, int Hkv, int D, int S_cap,
                                  int max_prefix, const int32_t *prefix_lens,
                                  const int32_t *tree_offsets, const uint32_t *mask,
-                                 float softmax_scale, void *workspace, size_t workspace_bytes,
-                                 int max_ctas, int32_t *status, void *stream) {
+                                 const int32_t *parents, float softmax_scale, void *workspace,
+                                 size_t workspace_bytes, int max_ctas, int32_t *status,
+                                 void *stream) {
   if (max_ctas < 0) return SPEC_ERR_SHAPE;
-  if (!q || !k_cache || !v_cache || !o || !prefix_lens || !tree_offsets || !mask || !status)
+  if (!q || !k_cache || !v_cache || !o || !prefix_lens || !tree_offsets || (!mask && !parents) ||
+      !status)
     return SPEC_ERR_NULL;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   if (B < 1 || T < 1 || T > B * SPEC_MAX_TREE_NODES || Hq < 1 || Hkv < 1 || Hq % Hkv ||
@@ -623,6 +610,7 @@ extern "C" int spec_tree_attn_ex(const void *q, const void *k_cache, const void 
   args.prefix_lens = prefix_lens;
   args.offsets = tree_offsets;
   args.mask = reinterpret_cast<const uint4 *>(mask);
+  args.parents = mask ? nullptr : parents;
   args.status = status;
   args.B = B;
   args.T = T;
@@ -652,7 +640,7 @@ extern "C" int spec_tree_attn_ex(const void *q, const void *k_cache, const void 
     return SPEC_ERR_CUDA;
   (void)workspace; (void)workspace_bytes;
   // the key splits are planned for the SMs the caller leaves to this launch
-  const int sms = sm_count();
+  const int sms = spec::sm_count();
   return spec::launch_attn_tc(args, max_prefix, T, tmq, tmk, tmv, packed,
                               max_ctas > 0 && max_ctas < sms ? max_ctas : sms, st);
 }

@@ -18,7 +18,8 @@ struct AttnArgs {
   void *o;
   const int32_t *prefix_lens;
   const int32_t *offsets;
-  const uint4 *mask;
+  const uint4 *mask;       // per node ancestor-or-self bits, or null: built from `parents`
+  const int32_t *parents;  // [T] request-local parent of every node (read when mask is null)
   int32_t *status;
   int B, T, Hq, Hkv, G, D, S_cap;
   float scale_log2;        // softmax scale * log2(e)
@@ -66,6 +67,49 @@ __device__ __forceinline__ uint4 clip_mask(uint4 m, int n) {
     if (n <= lo) w[i] = 0;
     else if (n < lo + 32) w[i] &= (1u << (n - lo)) - 1u;
   }
+  return m;
+}
+
+// Ancestor-or-self set of request-local node u (u < n <= 128), from the
+// request's parent array read through par(i): the walk follows u's parent
+// chain to the root.  Every step must go to a lower index and end at a root
+// whose parent is -1; a parent that breaks this ends the walk (so a malformed
+// array can never loop) and sets *bad.
+template <typename Par>
+__device__ __forceinline__ uint4 ancestor_mask(Par par, int u, bool *bad) {
+  uint4 m = make_uint4(0u, 0u, 0u, 0u);
+  int x = u;
+  for (;;) {
+    const uint32_t bit = 1u << (x & 31);
+    const int q = x >> 5;
+    m.x |= q == 0 ? bit : 0u;
+    m.y |= q == 1 ? bit : 0u;
+    m.z |= q == 2 ? bit : 0u;
+    m.w |= q == 3 ? bit : 0u;
+    const int p = par(x);
+    if (x == 0) {
+      if (p != -1) *bad = true;
+      break;
+    }
+    if (p < 0 || p >= x) {
+      *bad = true;
+      break;
+    }
+    x = p;
+  }
+  return m;
+}
+
+// The mask of row node t (global index) of request R, for the kernels that
+// do not stage the parent array: from the mask array when there is one,
+// else by walking the parents in global memory.  A malformed parent array
+// reports SPEC_ERR_BAD_PARENT for the request.
+__device__ __forceinline__ uint4 node_mask(const AttnArgs &a, const ReqGeom &R, int b, int t) {
+  if (a.mask) return clip_mask(__ldg(a.mask + t), R.n);
+  bool bad = false;
+  const int32_t *par = a.parents + R.lo;
+  const uint4 m = ancestor_mask([&](int i) { return __ldg(par + i); }, t - R.lo, &bad);
+  if (bad) report(a.status, b, SPEC_ERR_BAD_PARENT);
   return m;
 }
 

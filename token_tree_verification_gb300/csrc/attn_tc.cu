@@ -206,6 +206,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   __shared__ __align__(8) uint64_t bar_m;          // key splits: the peers' rows have arrived
   __shared__ int s_timeout;
   __shared__ int s_pv_issued;                        // P V products issued so far (warp 2)
+  __shared__ int s_par[SPEC_MAX_TREE_NODES];         // the request's parents (no mask array)
 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -425,7 +426,19 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
   } else {
     // ------------------------------------------------------------ softmax warps
     uint4 msk = make_uint4(0, 0, 0, 0);
-    if (lanes_live && row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + srow) / a.G), R.n);
+    if (a.mask) {
+      if (lanes_live && row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + srow) / a.G), R.n);
+    } else {
+      // no mask array: the softmax warps stage the request's parents, and
+      // each thread walks its row's node to the root (the first S tile is
+      // still on its way)
+      for (int i = tid - 96; i < R.n; i += 32 * C::kSoftmaxWarps) s_par[i] = __ldg(a.parents + R.lo + i);
+      named_bar_sync(2, 32 * C::kSoftmaxWarps);
+      bool bad = false;
+      if (lanes_live && row_ok)
+        msk = ancestor_mask([&](int i) { return s_par[i]; }, (row0 + srow) / a.G, &bad);
+      if (bad) report(a.status, b, SPEC_ERR_BAD_PARENT);
+    }
     const float sl2 = a.scale_log2;
     bool ok = true;
     // A timed-out wait clears `ok` and later waits are skipped, but the loop
