@@ -96,6 +96,7 @@ struct TcCfg {
 };
 
 constexpr int kTcMaxSplits = 8;
+constexpr int kEarlyTiles = 2;   // K/V tiles requested with Q, before tile 0 lands
 
 
 
@@ -326,6 +327,13 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       }
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
+        // Q and the first two tiles go first: every CTA's first tile then
+        // lands ahead of the rest of the ring's initial fill, so the first S
+        // starts earlier; the other stages are requested once tile 0 is in.
+        if (i == kEarlyTiles && !mbar_wait(&bar_full[0], 0)) {
+          s_timeout = 1;
+          break;
+        }
         if (i >= NS && !mbar_wait(&bar_empty[st], ((i / NS) - 1) & 1)) {
           s_timeout = 1;
           break;
