@@ -61,6 +61,7 @@ struct TreeSmem {
   int walk;
   int stop_fb;                        // the node's fallback token | tie << 31, in the writer CTA
   int timeout;                        // a bounded wait of this CTA ran out
+  int fits;                           // the root: the deepest path fits the output rows
   float dm[32], ds[32];               // per warp: (max, sum) of a leaf's row (draw at a leaf)
   int leaf[5];                        // walk ended at a leaf: node, request-local; accepted
                                       // tokens; near-ties so far; the draw's selected range;
@@ -138,8 +139,9 @@ constexpr uint32_t kArriveRootDone = 1u << 24;
 
 // Whether request b's output rows hold its deepest path (one warp; spar:
 // the request's parents, staged in shared memory, already validated).
-// Reports SPEC_ERR_TREE_TOO_LARGE and returns false when they do not.
-static __device__ bool path_fits(const VerifyArgs &a, int b, int n, const int *spar) {
+// path_fits_quiet only answers; path_fits also reports
+// SPEC_ERR_TREE_TOO_LARGE when they do not.
+static __device__ bool path_fits_quiet(const VerifyArgs &a, int n, const int *spar) {
   const int lane = threadIdx.x & 31;
   int maxd = 0;
 #pragma unroll
@@ -153,11 +155,13 @@ static __device__ bool path_fits(const VerifyArgs &a, int b, int n, const int *s
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) maxd = max(maxd, __shfl_xor_sync(0xffffffffu, maxd, o));
-  if (maxd + 1 > a.W) {
-    if (lane == 0) report(a.status, b, SPEC_ERR_TREE_TOO_LARGE);
-    return false;
-  }
-  return true;
+  return maxd + 1 <= a.W;
+}
+
+static __device__ bool path_fits(const VerifyArgs &a, int b, int n, const int *spar) {
+  const bool fits = path_fits_quiet(a, n, spar);
+  if (!fits && (threadIdx.x & 31) == 0) report(a.status, b, SPEC_ERR_TREE_TOO_LARGE);
+  return fits;
 }
 
 // Outputs of request b when the walk ends at the root without accepting a
@@ -543,7 +547,8 @@ static __device__ void stage_request(const NodeCtx &c, int t, TreeSmem &ts) {
 // of the root rejected, a valid tree, no wait of the CTA ran out, the path
 // fits the output rows): it needs no other node's results, so the CTA that
 // will draw the emitted token arrives before drawing it, and the atomic's
-// round trip overlaps the draw.  Called by every thread of that CTA;
+// round trip overlaps the draw.  Called by every thread of that CTA, after
+// warp 0 stored path_fits_quiet() in ts.fits;
 // `done` holds in warp 0, `prev` (the arrival word before) in thread 0.
 struct RootArrival {
   bool done;
@@ -553,7 +558,7 @@ struct RootArrival {
 static __device__ RootArrival root_arrive_early(const VerifyArgs &a, const NodeCtx &c, TreeSmem &ts) {
   RootArrival r{false, 0u};
   const int tid = threadIdx.x;
-  if (tid < 32) r.done = path_fits(a, c.b, c.n, ts.par);
+  if (tid < 32) r.done = ts.fits != 0;   // path_fits_quiet, taken while the rows loaded
   if (tid == 0 && r.done) {
     // nothing this node wrote is read by another node: no ordering needed
     asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;"

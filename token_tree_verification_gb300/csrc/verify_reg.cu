@@ -285,6 +285,12 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   const NodeCtx c = load_tree_b(a, t, ts, ca);
   const int k = c.k;
   const bool need_draft = !c.err && k > 0;   // leaves never read their draft row
+  // the root: whether the request's deepest path fits the output rows, while
+  // the rows are in flight (its early arrival needs it)
+  if (!c.err && c.u == 0 && w_id == 0) {
+    const bool f = path_fits_quiet(a, c.n, ts.par);
+    if (lane == 0) ts.fits = f ? 1 : 0;
+  }
   if (need_draft && !early_draft) load_row(drow, base, end, vec, xq);   // not expected
   // The scalar warp draws the node's uniforms (children's accept tests, the
   // fallback draw) and reads the children's raw logits while the rows are in
@@ -314,6 +320,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
   int stop = k;        // first accepted child, k when every child is rejected
   int my_flag = 0;     // thread j < k: the flag of child j
   int p_ok = -1;       // parity of the last reduction round that moved the residual
+  float slice_lo = 0.f, slice_hi = 0.f;   // that round's two slice totals (two CTAs)
   int near = 0;            // top-p: ns.near
   uint32_t tau_kept[2] = {0u, 0u};   // top-p: tau of p and q after renormalisation
   float c_prev = 0.f, Ml = 0.f, Sp = 1.f;
@@ -395,6 +402,54 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     const float inv_sq = need_draft ? 1.f / Sq : 0.f;
     const float sc_l = ml == -INFINITY ? 0.f : fast_exp2((ml - Ml) * l2s) * inv_sp;
     const float sc_d = (need_draft && md != -INFINITY) ? fast_exp2((md - Md) * l2s) * inv_sq : 0.f;
+    // The children's p and q from their raw logits (scalar warp), published
+    // with the uniforms through an mbarrier (release / acquire).  Without a
+    // nucleus this needs only the group statistics, so the scalar warp does it
+    // before scaling its own entries, and the accept tests wait less.
+    uint32_t tau_bits[2] = {0u, 0u};
+    float inv_nuc[2] = {1.f, 1.f};
+    auto publish_children = [&]() {
+      int nb = 0;
+      if constexpr (TOPP) {
+        const TopPSmem &tp = *reinterpret_cast<const TopPSmem *>(dyn_smem);
+        for (int i = lane; i < CS * kRWarps; i += 32) nb |= static_cast<int>((&tp.statp[0][0])[i].y);
+        nb = __reduce_or_sync(0xffffffffu, static_cast<unsigned>(nb));
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int j = lane + 32 * s;
+        if (j < k) {
+          float P = precise_prob(rawP[s], Ml, a.temp, a.inv_temp, 1.f) * inv_sp;
+          float Q = precise_prob(rawQ[s], Md, a.temp, a.inv_temp, 1.f) * inv_sq;
+          if constexpr (TOPP) {
+            // Membership follows the child's own entry of the filtered rows:
+            // the same operations on the same operands as its owner thread
+            // (warp maximum from the exchanged statistics, the same exp path).
+            const int x = ts.tok[ts.child[j]];
+            const int r = x / kRegChunk, off = x - r * kRegChunk;
+            const int wo = off / kRSpan, mo = (off % kRSpan) >> 7;
+            const float4 st = ex.stat[r][wo];
+            const float zp = fmaf(rawP[s], l2s, -st.x * l2s), zq = fmaf(rawQ[s], l2s, -st.z * l2s);
+            const float eP = (mo < kRVec / 2 ? fast_exp2(zp) : exp2_taylor(zp)) *
+                             (fast_exp2((st.x - Ml) * l2s) * inv_sp);
+            const float eQ = (mo < kRVec / 2 ? fast_exp2(zq) : exp2_taylor(zq)) *
+                             (fast_exp2((st.z - Md) * l2s) * inv_sq);
+            P = __float_as_uint(eP) >= tau_bits[0] ? P * inv_nuc[0] : 0.f;
+            Q = __float_as_uint(eQ) >= tau_bits[1] ? Q * inv_nuc[1] : 0.f;
+            ns.ctie[j] = ((nb & 1) && near_bits(__float_as_uint(eP), tau_bits[0])) ||
+                         ((nb & 2) && near_bits(__float_as_uint(eQ), tau_bits[1]));
+          }
+          ns.P[j] = P;
+          ns.Q[j] = Q;
+        }
+      }
+      if (lane == 0) ns.near = nb;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&nbar);
+    };
+    if constexpr (!TOPP) {
+      if (scalar_warp) publish_children();
+    }
 #pragma unroll
     for (int m = 0; m < kRVec; ++m) {
       xp[m].x *= sc_l; xp[m].y *= sc_l; xp[m].z *= sc_l; xp[m].w *= sc_l;
@@ -409,8 +464,6 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     //      (per-warp histograms, a CTA histogram, the group's by bulk copy)
     //      and keeps the digit where the running mass from the top reaches
     //      top_p.
-    uint32_t tau_bits[2] = {0u, 0u};
-    float inv_nuc[2] = {1.f, 1.f};
     if constexpr (TOPP) {
       TopPSmem &tp = *reinterpret_cast<TopPSmem *>(dyn_smem);
       // state[r] = {prefix bits of tau, mass above the prefix's digit range,
@@ -564,46 +617,9 @@ tree_verify_reg_kernel(const VerifyArgs a) {
                         peer_addr(&tp.sbar, lane));
       if (ok && !mbar_wait_for(&tp.sbar, 0, a.wait_ns)) ok = false;
     }
-    // the children's p and q from their raw logits (scalar warp), published
-    // with the uniforms through an mbarrier (release / acquire)
-    if (scalar_warp) {
-      int nb = 0;
-      if constexpr (TOPP) {
-        const TopPSmem &tp = *reinterpret_cast<const TopPSmem *>(dyn_smem);
-        for (int i = lane; i < CS * kRWarps; i += 32) nb |= static_cast<int>((&tp.statp[0][0])[i].y);
-        nb = __reduce_or_sync(0xffffffffu, static_cast<unsigned>(nb));
-      }
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int j = lane + 32 * s;
-        if (j < k) {
-          float P = precise_prob(rawP[s], Ml, a.temp, a.inv_temp, 1.f) * inv_sp;
-          float Q = precise_prob(rawQ[s], Md, a.temp, a.inv_temp, 1.f) * inv_sq;
-          if constexpr (TOPP) {
-            // Membership follows the child's own entry of the filtered rows:
-            // the same operations on the same operands as its owner thread
-            // (warp maximum from the exchanged statistics, the same exp path).
-            const int x = ts.tok[ts.child[j]];
-            const int r = x / kRegChunk, off = x - r * kRegChunk;
-            const int wo = off / kRSpan, mo = (off % kRSpan) >> 7;
-            const float4 st = ex.stat[r][wo];
-            const float zp = fmaf(rawP[s], l2s, -st.x * l2s), zq = fmaf(rawQ[s], l2s, -st.z * l2s);
-            const float eP = (mo < kRVec / 2 ? fast_exp2(zp) : exp2_taylor(zp)) *
-                             (fast_exp2((st.x - Ml) * l2s) * inv_sp);
-            const float eQ = (mo < kRVec / 2 ? fast_exp2(zq) : exp2_taylor(zq)) *
-                             (fast_exp2((st.z - Md) * l2s) * inv_sq);
-            P = __float_as_uint(eP) >= tau_bits[0] ? P * inv_nuc[0] : 0.f;
-            Q = __float_as_uint(eQ) >= tau_bits[1] ? Q * inv_nuc[1] : 0.f;
-            ns.ctie[j] = ((nb & 1) && near_bits(__float_as_uint(eP), tau_bits[0])) ||
-                         ((nb & 2) && near_bits(__float_as_uint(eQ), tau_bits[1]));
-          }
-          ns.P[j] = P;
-          ns.Q[j] = Q;
-        }
-      }
-      if (lane == 0) ns.near = nb;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&nbar);
+    // top-p: the children's p and q need the nuclei
+    if constexpr (TOPP) {
+      if (scalar_warp) publish_children();
     }
     if (ok && !mbar_wait_for(&nbar, 0, a.wait_ns)) ok = false;
     if (TOPP) near = ns.near;
@@ -614,6 +630,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     float W_prev = 1.f;
     bool frozen = false;   // a residual that summed to zero stays as it is
     int rounds = 0;
+    // (slice_lo, slice_hi: the two CTAs' totals of the last round that moved the residual)
     for (int j = 0; j < k; ++j) {
       const float P = ns.P[j];
       const float Q = ns.Q[j];
@@ -660,11 +677,17 @@ tree_verify_reg_kernel(const VerifyArgs a) {
         const int i = lane + 32 * s;
         if (i < nslot) acc += fl[i];
       }
-      const float Wn = warp_sum(acc);
+      // the group total, each 16-lane half summed first: with two CTAs the
+      // halves are the CTAs' slice totals, which the draw then reuses
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      const float Wn = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
       if (Wn > 0.f) {
         c_prev = c_new;
         W_prev = Wn;
         p_ok = p;
+        slice_lo = __shfl_sync(0xffffffffu, acc, 0);
+        slice_hi = __shfl_sync(0xffffffffu, acc, 16);
       } else {
         frozen = true;
       }
@@ -700,10 +723,17 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       };
       float slice[kMaxCS];
       float total = 0.f;
+      if (CS == 2 && p_ok >= 0) {
+        // the last round's halves: the same sums as the loop below
 #pragma unroll
-      for (int r = 0; r < kMaxCS; ++r) {
-        slice[r] = r < CS ? warp_sum(lane < kRWarps ? mass(r, lane) : 0.f) : 0.f;
-        total += slice[r];
+        for (int r = 0; r < kMaxCS; ++r) slice[r] = r == 0 ? slice_lo : (r == 1 ? slice_hi : 0.f);
+        total = (0.f + slice_lo) + slice_hi;
+      } else {
+#pragma unroll
+        for (int r = 0; r < kMaxCS; ++r) {
+          slice[r] = r < CS ? warp_sum(lane < kRWarps ? mass(r, lane) : 0.f) : 0.f;
+          total += slice[r];
+        }
       }
       const float target = ns.u_fb * total;
       int owner = -1;
