@@ -51,20 +51,31 @@ struct NodeScalars {
   int ctie[SPEC_MAX_TREE_NODES];     // top-p: child j's entry is near tau at such a node
 };
 
+// One CTA's candidates for tau after the first radix pass: the bits of its
+// entries (p row, q row) whose top 8 bits equal tau's; n counts them all,
+// also beyond the capacity (then the radix passes continue instead).
+constexpr int kCandCap = 512;
+struct __align__(16) TopPCands {
+  uint32_t n[4];
+  uint32_t v[2][kCandCap];
+};
+
 // Top-p working storage (dynamic shared memory).  Masses are fixed point,
 // value * 2^40 rounded to u64, so histogram sums are exact and independent
 // of the order of the atomic adds, and the rounding of a whole row stays
 // below V * 2^-41 of its mass.
 struct TopPSmem {
-  // per warp: [row (p, q)][high, low 20 bits of the mass][8-bit digit]; a
-  // warp adds at most 1024 entries of a row, so each half stays below 2^30
+  // per warp: [row (p, q)][high, low 20 bits of the mass][digit]; a warp
+  // adds at most 1024 entries of a row, so each half stays below 2^30
   uint32_t warp_hist[kRWarps][2][2][256];
   unsigned long long cta[2][2][256];               // the CTA's histogram, by pass parity
   unsigned long long recv[2][kMaxCS][2][256];      // every CTA's histogram, by pass parity
   unsigned long long hsum[2][256];                 // the group's histogram
   unsigned long long state[2][4];   // per row: prefix bits, mass above, digit mass, target
   float2 statp[kMaxCS][kRWarps];    // per warp: its mass of the filtered p, near flags
-  uint64_t bar[2], sbar;
+  TopPCands cand_local;             // this CTA's candidates
+  TopPCands cand_recv[kMaxCS];      // every CTA's candidates
+  uint64_t bar[2], sbar, gbar;
 };
 constexpr uint32_t kHistBytes = 2 * 256 * 8;  // one CTA histogram
 constexpr float kFixedScale = 1099511627776.f;  // 2^40
@@ -76,26 +87,34 @@ __device__ __forceinline__ unsigned long long fixed_mass(float v) {
   return __float2ull_rn(v * kFixedScale);
 }
 // hist[bin] += fixed_mass(v), split into its bits 20 and up (at saddr) and
-// its low 20 bits (at saddr + 1 KB), two 32-bit shared-memory adds, as one
-// unit: the scaling, the conversion and the adds stay together, so that an
-// unrolled loop over a thread's entries does not hold all their conversions
-// in registers at once.
+// its low 20 bits (at saddr + 1 KB), 32-bit shared-memory adds (a 64-bit
+// shared add measured about twice as slow; an add of zero is skipped, as
+// the first is for most entries: p < 2^-20), as one unit: the scaling, the
+// conversion and the adds stay together, so that an unrolled loop over a
+// thread's entries does not hold all their conversions in registers at once.
 __device__ __forceinline__ void hist_add(uint32_t saddr, float v) {
   asm volatile(
-      "{\n\t.reg .f32 s;\n\t.reg .u64 m;\n\t.reg .u32 hi, lo;\n\t"
+      "{\n\t.reg .f32 s;\n\t.reg .u64 m;\n\t.reg .u32 hi, lo;\n\t.reg .pred big;\n\t"
       "mul.rn.f32 s, %1, 0f53800000;\n\t"   // v * 2^40 (exact)
       "cvt.rni.u64.f32 m, s;\n\t"
+      "cvt.u32.u64 lo, m;\n\t"
       "shr.u64 m, m, 20;\n\t"
       "cvt.u32.u64 hi, m;\n\t"
-      "cvt.rni.u64.f32 m, s;\n\t"
-      "cvt.u32.u64 lo, m;\n\t"
       "and.b32 lo, lo, 1048575;\n\t"
-      "red.shared.add.u32 [%0], hi;\n\t"
-      "red.shared.add.u32 [%0+1024], lo;\n\t}"
+      "setp.ne.u32 big, hi, 0;\n\t"
+      "@big red.shared.add.u32 [%0], hi;\n\t"
+      "setp.ne.u32 big, lo, 0;\n\t"
+      "@big red.shared.add.u32 [%0+1024], lo;\n\t}"
       :
       : "r"(saddr), "f"(v)
       : "memory");
 }
+
+// The radix digits of tau's bits (non-negative floats: bit 31 is 0): the
+// exponent, then 8, 8 and 7 bits of the mantissa.
+__device__ __forceinline__ int radix_shift(int pass) { return pass == 0 ? 23 : (pass == 1 ? 15 : (pass == 2 ? 7 : 0)); }
+__device__ __forceinline__ uint32_t radix_mask(int pass) { return pass == 3 ? 127u : 255u; }
+__device__ __forceinline__ int radix_top(int pass) { return pass == 0 ? 31 : radix_shift(pass - 1); }
 __device__ __forceinline__ bool near_bits(uint32_t x, uint32_t t) {
   const int d = static_cast<int>(x - t);
   return d >= -kTauUlps && d <= kTauUlps;
@@ -238,6 +257,7 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       mbar_init(&tp.bar[0], 1);
       mbar_init(&tp.bar[1], 1);
       mbar_init(&tp.sbar, 1);
+      mbar_init(&tp.gbar, 1);
     }
     fence_barrier_init();
   }
@@ -459,74 +479,24 @@ tree_verify_reg_kernel(const VerifyArgs a) {
     //      upper tail {x >= tau} holds at least top_p of the mass; entries of
     //      that tail keep their mass, renormalised, the rest drop to 0.  The
     //      float bits of non-negative entries order like the values, so tau
-    //      is found by 4 radix passes of 8 bits over them: each pass sums the
-    //      fixed-point mass of the entries still in play per 8-bit digit
-    //      (per-warp histograms, a CTA histogram, the group's by bulk copy)
-    //      and keeps the digit where the running mass from the top reaches
-    //      top_p.
+    //      is found by radix passes over them (the exponent, then 8, 8 and 7
+    //      mantissa bits): each pass sums the fixed-point mass of the entries
+    //      still in play per digit and keeps the digit where the running mass
+    //      from the top reaches top_p.  The first pass takes per-warp
+    //      histograms, a CTA histogram and the group's by bulk copy; the
+    //      entries sharing tau's exponent are then gathered from the group,
+    //      and the other passes run on them in every CTA.
     if constexpr (TOPP) {
       TopPSmem &tp = *reinterpret_cast<TopPSmem *>(dyn_smem);
       // state[r] = {prefix bits of tau, mass above the prefix's digit range,
       // mass of the kept digit, target}; rows p (0) and q (1)
       if (tid < 8) (&tp.state[0][0])[tid] = 0ull;
+      if (tid < 4) tp.cand_local.n[tid] = 0u;
       __syncthreads();
-      for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        const int par = pass & 1;
-        const uint32_t hi_p = static_cast<uint32_t>(tp.state[0][0]) >> (shift + 8);
-        const uint32_t hi_q = static_cast<uint32_t>(tp.state[1][0]) >> (shift + 8);
-        uint32_t *wh = &tp.warp_hist[w_id][0][0][0];
-        const uint32_t wh_addr = smem_addr(wh);
-        for (int i = lane; i < 1024; i += 32) wh[i] = 0u;
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < kRVec; ++m) {
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const float v = pick4(xp[m], cc);
-            const uint32_t bits = __float_as_uint(v);
-            if (bits != 0u && (pass == 0 || (bits >> (shift + 8)) == hi_p))
-              hist_add(wh_addr + 4u * ((bits >> shift) & 255u), v);
-          }
-        }
-        if (need_draft) {
-#pragma unroll
-          for (int m = 0; m < kRVec; ++m) {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const float v = pick4(xq[m], cc);
-              const uint32_t bits = __float_as_uint(v);
-              if (bits != 0u && (pass == 0 || (bits >> (shift + 8)) == hi_q))
-                hist_add(wh_addr + 2048u + 4u * ((bits >> shift) & 255u), v);
-            }
-          }
-        }
-        __syncthreads();
-        {
-          const int row = tid >> 8, bin = tid & 255;   // 512 threads: 2 rows x 256 digits
-          unsigned long long h = 0ull;
-#pragma unroll
-          for (int ww = 0; ww < kRWarps; ++ww)
-            h += (static_cast<unsigned long long>(tp.warp_hist[ww][row][0][bin]) << 20) +
-                 tp.warp_hist[ww][row][1][bin];
-          tp.cta[par][row][bin] = h;
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0 && ok) {   // (no arrival after a wait ran out, as in the rounds below)
-          mbar_arrive_expect_tx(&tp.bar[par], static_cast<uint32_t>(CS) * kHistBytes);
-          for (int r = 0; r < CS; ++r)
-            bulk_copy_s2s(peer_addr(&tp.recv[par][rank][0][0], r), smem_addr(&tp.cta[par][0][0]),
-                          kHistBytes, peer_addr(&tp.bar[par], r));
-        }
-        if (ok && !mbar_wait_for(&tp.bar[par], (pass >> 1) & 1, a.wait_ns)) ok = false;
-        {
-          const int row = tid >> 8, bin = tid & 255;
-          unsigned long long h = 0ull;
-          for (int r = 0; r < CS; ++r) h += tp.recv[par][r][row][bin];
-          tp.hsum[row][bin] = h;
-        }
-        __syncthreads();
+      // Warp r (rows p, q) finds the digit of row r, at bits [shift, shift + width)
+      // of tau, where the running mass of tp.hsum from the top reaches the
+      // target, and extends tp.state[r].
+      auto find_digit = [&](int pass, int shift) {
         if (w_id < (need_draft ? 2 : 1)) {
           // warp r: the digit of row r where the running mass from the top
           // reaches the target (lane l holds digits 255 - 8l .. 248 - 8l)
@@ -572,6 +542,155 @@ tree_verify_reg_kernel(const VerifyArgs a) {
             tp.state[r][3] = target;
           }
         }
+      };
+      auto gather_candidates = [&]() -> bool {
+        TopPCands &cl = tp.cand_local;
+        const uint32_t d0p = static_cast<uint32_t>(tp.state[0][0]) >> 23;
+        const uint32_t d0q = need_draft ? static_cast<uint32_t>(tp.state[1][0]) >> 23 : 0xffffffffu;
+        // this thread's entries in the digit, as bit masks over its 32 slots
+        uint32_t mp = 0u, mq = 0u;
+#pragma unroll
+        for (int m = 0; m < kRVec; ++m)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t bp = __float_as_uint(pick4(xp[m], cc));
+            const uint32_t bq = __float_as_uint(pick4(xq[m], cc));
+            mp |= (bp != 0u && (bp >> 23) == d0p) ? (1u << (4 * m + cc)) : 0u;
+            mq |= (bq != 0u && (bq >> 23) == d0q) ? (1u << (4 * m + cc)) : 0u;
+          }
+        // a warp prefix of the counts, one atomic per warp and row
+        auto slot_base = [&](int cnt, uint32_t *counter) -> int {
+          int inc = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          int base = 0;
+          if (lane == 31 && inc > 0) base = static_cast<int>(atomicAdd(counter, static_cast<uint32_t>(inc)));
+          return __shfl_sync(0xffffffffu, base, 31) + inc - cnt;
+        };
+        int atp = slot_base(__popc(mp), &cl.n[0]);
+        int atq = slot_base(__popc(mq), &cl.n[1]);
+#pragma unroll
+        for (int m = 0; m < kRVec; ++m)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            if ((mp >> (4 * m + cc)) & 1u) {
+              if (atp < kCandCap) cl.v[0][atp] = __float_as_uint(pick4(xp[m], cc));
+              ++atp;
+            }
+            if ((mq >> (4 * m + cc)) & 1u) {
+              if (atq < kCandCap) cl.v[1][atq] = __float_as_uint(pick4(xq[m], cc));
+              ++atq;
+            }
+          }
+        // (generic writes, read by the bulk copies)
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && ok) {   // (no arrival after a wait ran out)
+          mbar_arrive_expect_tx(&tp.gbar, static_cast<uint32_t>(CS * sizeof(TopPCands)));
+          for (int r = 0; r < CS; ++r)
+            bulk_copy_s2s(peer_addr(&tp.cand_recv[rank], r), smem_addr(&cl),
+                          static_cast<uint32_t>(sizeof(TopPCands)), peer_addr(&tp.gbar, r));
+        }
+        if (ok && !mbar_wait_for(&tp.gbar, 0, a.wait_ns)) ok = false;
+        // every CTA sees the same counts, so every CTA takes the same path
+        // (and a CTA whose wait ran out takes one path, by the barrier)
+        bool fits = ok;
+        for (int r = 0; r < CS; ++r) fits = fits && tp.cand_recv[r].n[0] <= kCandCap &&
+                                        tp.cand_recv[r].n[1] <= kCandCap;
+        if (!__syncthreads_and(fits)) return false;
+        // passes 1-3 on the candidates: the group histogram of the entries
+        // still in play, from the candidates alone
+        for (int lp = 1; lp < 4; ++lp) {
+          const int shift = radix_shift(lp), top = radix_top(lp);
+          const uint32_t dmask = radix_mask(lp);
+          (&tp.hsum[0][0])[tid] = 0ull;   // 512 threads: 2 rows x 256 digits
+          __syncthreads();
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            if (r == 1 && !need_draft) break;
+            const uint32_t hi = static_cast<uint32_t>(tp.state[r][0]) >> top;
+            for (int r2 = 0; r2 < CS; ++r2) {
+              const int n = static_cast<int>(tp.cand_recv[r2].n[r]);
+              for (int i = tid; i < n; i += kRThreads) {
+                const uint32_t bits = tp.cand_recv[r2].v[r][i];
+                if ((bits >> top) == hi)
+                  atomicAdd(&tp.hsum[r][(bits >> shift) & dmask], fixed_mass(__uint_as_float(bits)));
+              }
+            }
+          }
+          __syncthreads();
+          find_digit(lp, shift);
+          __syncthreads();
+        }
+        return true;
+      };
+      for (int pass = 0; pass < 4; ++pass) {
+        // After pass 0, tau's exponent is known, and few entries share it:
+        // they are gathered from every CTA of the group in one exchange, and
+        // passes 1-3 run on them locally (the same sums over the same
+        // entries, so the same tau); too many, and the passes below run.
+        if (pass == 1 && gather_candidates()) break;
+        const int shift = radix_shift(pass), top = radix_top(pass);
+        const uint32_t dmask = radix_mask(pass);
+        const int par = pass & 1;
+        const uint32_t hi_p = static_cast<uint32_t>(tp.state[0][0]) >> top;
+        const uint32_t hi_q = static_cast<uint32_t>(tp.state[1][0]) >> top;
+        uint32_t *wh = &tp.warp_hist[w_id][0][0][0];
+        const uint32_t wh_addr = smem_addr(wh);
+        for (int i = lane; i < 1024; i += 32) wh[i] = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < kRVec; ++m) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const float v = pick4(xp[m], cc);
+            const uint32_t bits = __float_as_uint(v);
+            if (bits != 0u && (pass == 0 || (bits >> top) == hi_p))
+              hist_add(wh_addr + 4u * ((bits >> shift) & dmask), v);
+          }
+        }
+        if (need_draft) {
+#pragma unroll
+          for (int m = 0; m < kRVec; ++m) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const float v = pick4(xq[m], cc);
+              const uint32_t bits = __float_as_uint(v);
+              if (bits != 0u && (pass == 0 || (bits >> top) == hi_q))
+                hist_add(wh_addr + 2048u + 4u * ((bits >> shift) & dmask), v);
+            }
+          }
+        }
+        __syncthreads();
+        {
+          const int row = tid >> 8, bin = tid & 255;   // 512 threads: 2 rows x 256 digits
+          unsigned long long h = 0ull;
+#pragma unroll
+          for (int ww = 0; ww < kRWarps; ++ww)
+            h += (static_cast<unsigned long long>(tp.warp_hist[ww][row][0][bin]) << 20) +
+                 tp.warp_hist[ww][row][1][bin];
+          tp.cta[par][row][bin] = h;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && ok) {   // (no arrival after a wait ran out, as in the rounds below)
+          mbar_arrive_expect_tx(&tp.bar[par], static_cast<uint32_t>(CS) * kHistBytes);
+          for (int r = 0; r < CS; ++r)
+            bulk_copy_s2s(peer_addr(&tp.recv[par][rank][0][0], r), smem_addr(&tp.cta[par][0][0]),
+                          kHistBytes, peer_addr(&tp.bar[par], r));
+        }
+        if (ok && !mbar_wait_for(&tp.bar[par], (pass >> 1) & 1, a.wait_ns)) ok = false;
+        {
+          const int row = tid >> 8, bin = tid & 255;
+          unsigned long long h = 0ull;
+          for (int r = 0; r < CS; ++r) h += tp.recv[par][r][row][bin];
+          tp.hsum[row][bin] = h;
+        }
+        __syncthreads();
+        find_digit(pass, shift);
         __syncthreads();
       }
       // the nucleus: entries whose bits are >= tau's, renormalised.  An
