@@ -104,13 +104,19 @@ __device__ __forceinline__ uint4 ancestor_mask(Par par, int u, bool *bad) {
 // do not stage the parent array: from the mask array when there is one,
 // else by walking the parents in global memory.  A malformed parent array
 // reports SPEC_ERR_BAD_PARENT for the request.
-__device__ __forceinline__ uint4 node_mask(const AttnArgs &a, const ReqGeom &R, int b, int t) {
-  if (a.mask) return clip_mask(__ldg(a.mask + t), R.n);
+// (the walk is kept out of line, so that the kernels' mask-array path is
+// compiled as without it)
+static __device__ __noinline__ uint4 node_mask_walk(const AttnArgs &a, const ReqGeom &R, int b, int t) {
   bool bad = false;
   const int32_t *par = a.parents + R.lo;
   const uint4 m = ancestor_mask([&](int i) { return __ldg(par + i); }, t - R.lo, &bad);
   if (bad) report(a.status, b, SPEC_ERR_BAD_PARENT);
   return m;
+}
+
+__device__ __forceinline__ uint4 node_mask(const AttnArgs &a, const ReqGeom &R, int b, int t) {
+  if (a.mask) return clip_mask(__ldg(a.mask + t), R.n);
+  return node_mask_walk(a, R, b, t);
 }
 
 // Byte offset of 16-byte chunk `c16` (0..7) of row `row` inside one SW128
