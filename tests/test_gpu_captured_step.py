@@ -1,6 +1,6 @@
-"""The step bench.py times, as it times it: mask, tree attention and
-verification captured in one CUDA graph (with programmatic dependent launch
-between the kernels) and replayed, compared with the oracle.
+"""The step bench.py times, as it times it: tree attention (its masks built
+from the parents) on one branch and the mask kernel then verification on the
+other, captured in one CUDA graph and replayed, compared with the oracle.
 
 Source: speculative-decoding explainer (intelliparadigm.com) §3.2
 并行验证的CUDA优化 (capture the whole verification flow in a CUDA graph).
