@@ -751,32 +751,35 @@ def derived_rates(st, stream, ms_per_step, mask_ms, attn_ms, ver_ms, samples=64,
 def run_e2e(st, w, stream, steps):
     """Same metric through the public API with host buffers: every step copies
     all of its inputs (Q, K/V caches, target and draft logits, tree arrays)
-    from pinned host memory and reads the verified tokens back.  The copies of
-    step i + 1 go on two copy streams into the other of two device input sets
-    while step i's kernels run, as a serving loop would overlap them; the
-    timed region spans every copy and every step.  The four small tree arrays
-    travel as one packed buffer and the four outputs come back as one, since
-    every copy pays a fixed start-up cost on the host-device link."""
+    from pinned host memory and reads the verified tokens back.  The inputs sit
+    in one pinned buffer (each at a 256-byte aligned offset), copied in two
+    halves on two copy streams into the other of two device input buffers while
+    step i's kernels run, as a serving loop would overlap them; the timed region
+    spans every copy and every step.  The four outputs come back as one copy,
+    since every copy pays a fixed start-up cost on the host-device link."""
     import torch
     ttv = st.ttv
     names = [k for k, v in st.copies[0].items() if v is not None]
-    host = {k: st.copies[0][k].cpu().pin_memory() for k in names}
     tree_parts = [("par", st.par), ("off", st.off), ("tok", st.tok), ("pl", st.pl)]
-    tree_host = torch.cat([v.cpu() for _, v in tree_parts]).pin_memory()
+    parts = [(k, st.copies[0][k]) for k in names] + tree_parts
+    # every input of a step at a 256-byte aligned offset of one byte buffer:
+    # one pinned host buffer, two device buffers (double-buffered inputs)
+    layout, at = [], 0
+    for k, t in parts:
+        nb = t.numel() * t.element_size()
+        layout.append((k, at, nb, t.dtype, tuple(t.shape)))
+        at = (at + nb + 255) // 256 * 256
+    total = at
 
-    def tree_views(buf):
-        out, at = {}, 0
-        for k, v in tree_parts:
-            out[k] = buf[at:at + v.numel()]
-            at += v.numel()
-        return out
+    def views(buf):
+        return {k: buf[off:off + nb].view(dt).view(sh) for k, off, nb, dt, sh in layout}
 
-    sets = []
-    for j in range(2):
-        d = {k: st.copies[j][k] for k in names}
-        d["tree"] = tree_host.cuda()
-        d.update(tree_views(d["tree"]))
-        sets.append(d)
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    hv = views(host_buf)
+    for k, t in parts:
+        hv[k].copy_(t.cpu())
+    dev_bufs = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    sets = [views(b) for b in dev_bufs]
     # the outputs as views of one device buffer, read back with one copy
     shapes = [(k, tuple(v.shape)) for k, v in st.outs.items()]
     n_out = sum(int(np.prod(sh)) for _, sh in shapes)
@@ -787,28 +790,22 @@ def run_e2e(st, w, stream, steps):
         outs[k] = out_dev[at:at + n].view(sh)
         at += n
     out_host = [torch.empty(n_out, dtype=torch.int32).pin_memory() for _ in range(2)]
-    src = dict(host, tree=tree_host)
-    h2d = sum(v.numel() * v.element_size() for v in src.values())
+    h2d = total
     d2h = out_dev.numel() * out_dev.element_size()
     cs = [torch.cuda.Stream(), torch.cuda.Stream()]
-    # inputs by size, each to the copy stream with fewer bytes so far
-    order = sorted(src, key=lambda k: -src[k].nbytes)
-    lanes, load = {}, [0, 0]
-    for k in order:
-        lane = 0 if load[0] <= load[1] else 1
-        lanes[k] = lane
-        load[lane] += src[k].nbytes
+    # the buffer in two halves, one per copy stream (split on a 256-byte boundary)
+    half = (total // 2 + 255) // 256 * 256
+    ranges = [(0, half), (half, total)]
     free = [torch.cuda.Event() for _ in range(2)]
 
     def copy_in(i):
-        d = sets[i % 2]
+        dst = dev_bufs[i % 2]
         done = [torch.cuda.Event(), torch.cuda.Event()]
         for lane in range(2):
             cs[lane].wait_event(free[i % 2])
+            a, b = ranges[lane]
             with torch.cuda.stream(cs[lane]):
-                for k in order:
-                    if lanes[k] == lane:
-                        d[k].copy_(src[k], non_blocking=True)
+                dst[a:b].copy_(host_buf[a:b], non_blocking=True)
             done[lane].record(cs[lane])
         stream.wait_event(done[0])
         stream.wait_event(done[1])
@@ -852,8 +849,9 @@ def run_e2e(st, w, stream, steps):
         raise RuntimeError("end-to-end outputs differ from the device path")
     return {"value": w.T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipeline": ("two copy streams into double-buffered inputs, overlapping the previous step; "
-                         "tree arrays packed into one copy, outputs read back in one")}
+            "pipeline": ("every input of a step in one pinned buffer, copied in two halves on two "
+                         "copy streams into double-buffered device inputs, overlapping the previous "
+                         "step; outputs read back in one copy")}
 
 
 # --------------------------------------------------------------------------
