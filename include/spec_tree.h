@@ -42,6 +42,16 @@
  *  - A parent array satisfies parent[0] = -1 and 0 <= parent[i] < i, so node
  *    order is topological and siblings are ordered by index.
  *  - A return value of SPEC_OK means the work was enqueued.
+ *  - Bounds-checked build (libspec_tree_checked.so, compiled with
+ *    -DSPEC_CHECKED): every global access whose index is computed from the
+ *    inputs (a tree offset, a parent, a token, a path node, a prefix length)
+ *    is first tested against the extent of its buffer as the call's size
+ *    arguments define it.  A failed test writes SPEC_ERR_INDEX to the
+ *    request's status word (request 0's when the request is not known) and
+ *    skips the access: a load yields 0, a store is dropped.  It never traps
+ *    or asserts.  The host-side checks and the results are those of the
+ *    normal build; only speed differs.  spec_build_checked() says which
+ *    build is loaded.
  */
 #ifndef SPEC_TREE_H
 #define SPEC_TREE_H
@@ -66,7 +76,9 @@ typedef enum {
   SPEC_ERR_CUDA = -8,            /* a CUDA runtime call or launch failed */
   SPEC_ERR_TIMEOUT = -9,         /* a bounded device-side wait ran out (never expected) */
   SPEC_ERR_PREFIX_RANGE = -10,   /* prefix_lens[b] < 0 or L_b + N_b > S_cap */
-  SPEC_ERR_ALIGNMENT = -11       /* a pointer is not 16-byte aligned */
+  SPEC_ERR_ALIGNMENT = -11,      /* a pointer is not 16-byte aligned */
+  SPEC_ERR_INDEX = -12           /* bounds-checked build only: a computed global index fell
+                                    outside its buffer; the access was skipped */
 } spec_status;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
@@ -460,6 +472,9 @@ int spec_philox_uniforms(uint64_t seed, const int64_t *counters, int n, float *u
 
 /* Human-readable name of a spec_status value (static storage). */
 const char *spec_status_string(int code);
+
+/* 1 in the bounds-checked build (-DSPEC_CHECKED), 0 otherwise. */
+int spec_build_checked(void);
 
 #ifdef __cplusplus
 }

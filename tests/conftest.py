@@ -21,5 +21,8 @@ def gpu_lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import token_tree_verification_gb300 as ttv
-    ttv.load()
+    lib = ttv.load()
+    # SPEC_TREE_CHECKED=1 runs the suites against the bounds-checked build
+    want = 1 if os.environ.get("SPEC_TREE_CHECKED", "0") == "1" else 0
+    assert lib.spec_build_checked() == want, ttv.lib_path()
     return ttv

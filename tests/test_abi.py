@@ -34,10 +34,27 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-11, 1):
+    for code in range(-12, 1):
         s = lib.spec_status_string(code).decode()
         assert s.startswith("SPEC_")
     assert b"unknown" in lib.spec_status_string(42)
+
+
+def test_bounds_checked_build_exports_the_same_entry_points(lib):
+    """The -DSPEC_CHECKED debug build compiles from the same sources, exports
+    every declared entry point and says which build it is."""
+    from token_tree_verification_gb300 import build
+    path = build.build(checked=True)
+    assert os.path.basename(path) == "libspec_tree_checked.so"
+    chk = ctypes.CDLL(path)
+    for n in declared_symbols():
+        assert hasattr(chk, n), n
+    chk.spec_build_checked.restype = ctypes.c_int
+    lib.spec_build_checked.restype = ctypes.c_int
+    assert chk.spec_build_checked() == 1
+    assert lib.spec_build_checked() == 0
+    chk.spec_status_string.restype = ctypes.c_char_p
+    assert chk.spec_status_string(-12).decode().startswith("SPEC_ERR_INDEX")
 
 
 def test_workspace_sizes(lib):

@@ -24,7 +24,7 @@ STATUS = {
     0: "SPEC_OK", -1: "SPEC_ERR_NULL", -2: "SPEC_ERR_SHAPE", -3: "SPEC_ERR_DTYPE",
     -4: "SPEC_ERR_TREE_TOO_LARGE", -5: "SPEC_ERR_BAD_PARENT", -6: "SPEC_ERR_TOKEN_RANGE",
     -7: "SPEC_ERR_WORKSPACE", -8: "SPEC_ERR_CUDA", -9: "SPEC_ERR_TIMEOUT",
-    -10: "SPEC_ERR_PREFIX_RANGE", -11: "SPEC_ERR_ALIGNMENT",
+    -10: "SPEC_ERR_PREFIX_RANGE", -11: "SPEC_ERR_ALIGNMENT", -12: "SPEC_ERR_INDEX",
 }
 SPEC_F32, SPEC_BF16 = 0, 1
 MAX_TREE_NODES = 128
@@ -37,6 +37,11 @@ class SpecError(RuntimeError):
 
 
 def lib_path() -> str:
+    """The library ``load()`` opens: the bounds-checked build when the
+    environment sets ``SPEC_TREE_CHECKED=1`` (built by ``build(checked=True)``),
+    the normal one otherwise."""
+    if os.environ.get("SPEC_TREE_CHECKED", "0") == "1":
+        return os.path.join(_HERE, "libspec_tree_checked.so")
     return os.path.join(_HERE, "libspec_tree.so")
 
 
@@ -76,6 +81,8 @@ def load():
     lib.spec_philox_uniforms.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
+    lib.spec_build_checked.argtypes = []
+    lib.spec_build_checked.restype = I
     _lib = lib
     return lib
 

@@ -183,8 +183,9 @@ tree_attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
         uint32_t v = 0;
         if (r < rows_total) {
           const int node = r / a.G, head = g * a.G + r % a.G;
-          v = __ldg(reinterpret_cast<const uint32_t *>(
-              q + (static_cast<size_t>(R.lo + node) * a.Hq + head) * D + col));
+          if (in_bounds(R.lo + node, a.T, a.status, b))
+            v = __ldg(reinterpret_cast<const uint32_t *>(
+                q + (static_cast<size_t>(R.lo + node) * a.Hq + head) * D + col));
         }
         qa[ks][j] = v;
       }
@@ -320,6 +321,7 @@ tree_attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
         const int r = row0 + r_local[h2];
         if (r >= rows_total) continue;
         const int node = r / a.G, head = g * a.G + r % a.G;
+        if (!in_bounds(R.lo + node, a.T, a.status, b)) continue;
         const float inv = 1.f / l_run[h2];
         __nv_bfloat16 *dst = out + (static_cast<size_t>(R.lo + node) * a.Hq + head) * D;
 #pragma unroll
@@ -373,6 +375,7 @@ tree_attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
     }
     const float inv = 1.f / L;
     const int node = r / a.G, head = g * a.G + r % a.G;
+    if (!in_bounds(R.lo + node, a.T, a.status, b)) continue;
     __nv_bfloat16 *dst = out + (static_cast<size_t>(R.lo + node) * a.Hq + head) * D + c4 * 4;
     uint2 pk;
     pk.x = pack_bf16(acc.x * inv, acc.y * inv);
@@ -413,7 +416,7 @@ tree_attn_f32_kernel(const AttnArgs a) {
     // scores of this chunk, one key per thread (log2 domain)
     const int key = c0 + tid;
     float sc = -INFINITY;
-    if (key < R.keys && key_visible(key, R.L, R.keys, m)) {
+    if (key < R.keys && key_visible(key, R.L, R.keys, m) && in_bounds(key, a.S_cap, a.status, b)) {
       const float *kr = kc + static_cast<size_t>(key) * D;
       float dot = 0.f;
       for (int d = 0; d < D; ++d) dot = fmaf(qs[d], kr[d], dot);
@@ -444,7 +447,8 @@ tree_attn_f32_kernel(const AttnArgs a) {
       float part = 0.f;
       const int nk = min(kF32Chunk, R.keys - c0);
       for (int j = 0; j < nk; ++j)
-        if (ps[j] != 0.f) part = fmaf(ps[j], vc[static_cast<size_t>(c0 + j) * D + tid], part);
+        if (ps[j] != 0.f && in_bounds(c0 + j, a.S_cap, a.status, b))
+          part = fmaf(ps[j], vc[static_cast<size_t>(c0 + j) * D + tid], part);
       acc = acc * alpha + part;
     }
     __syncthreads();

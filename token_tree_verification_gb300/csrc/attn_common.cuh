@@ -109,13 +109,18 @@ __device__ __forceinline__ uint4 ancestor_mask(Par par, int u, bool *bad) {
 static __device__ __noinline__ uint4 node_mask_walk(const AttnArgs &a, const ReqGeom &R, int b, int t) {
   bool bad = false;
   const int32_t *par = a.parents + R.lo;
-  const uint4 m = ancestor_mask([&](int i) { return __ldg(par + i); }, t - R.lo, &bad);
+  const uint4 m = ancestor_mask(
+      [&](int i) { return in_bounds(R.lo + i, a.T, a.status, b) ? __ldg(par + i) : -2; }, t - R.lo,
+      &bad);
   if (bad) report(a.status, b, SPEC_ERR_BAD_PARENT);
   return m;
 }
 
 __device__ __forceinline__ uint4 node_mask(const AttnArgs &a, const ReqGeom &R, int b, int t) {
-  if (a.mask) return clip_mask(__ldg(a.mask + t), R.n);
+  if (a.mask) {
+    if (!in_bounds(t, a.T, a.status, b)) return make_uint4(0u, 0u, 0u, 0u);
+    return clip_mask(__ldg(a.mask + t), R.n);
+  }
   return node_mask_walk(a, R, b, t);
 }
 

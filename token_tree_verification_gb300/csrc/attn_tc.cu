@@ -435,12 +435,14 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     // ------------------------------------------------------------ softmax warps
     uint4 msk = make_uint4(0, 0, 0, 0);
     if (a.mask) {
-      if (lanes_live && row_ok) msk = clip_mask(__ldg(a.mask + R.lo + (row0 + srow) / a.G), R.n);
+      if (lanes_live && row_ok && in_bounds(R.lo + (row0 + srow) / a.G, a.T, a.status, b))
+        msk = clip_mask(__ldg(a.mask + R.lo + (row0 + srow) / a.G), R.n);
     } else {
       // no mask array: the softmax warps stage the request's parents, and
       // each thread walks its row's node to the root (the first S tile is
       // still on its way)
-      for (int i = tid - 96; i < R.n; i += 32 * C::kSoftmaxWarps) s_par[i] = __ldg(a.parents + R.lo + i);
+      for (int i = tid - 96; i < R.n; i += 32 * C::kSoftmaxWarps)
+        s_par[i] = in_bounds(R.lo + i, a.T, a.status, b) ? __ldg(a.parents + R.lo + i) : -2;
       named_bar_sync(2, 32 * C::kSoftmaxWarps);
       bool bad = false;
       if (lanes_live && row_ok)
@@ -659,6 +661,7 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       pk.z = bf16x2_bits(__floats2bfloat162_rn(v1.x * inv, v1.y * inv));
       pk.w = bf16x2_bits(__floats2bfloat162_rn(v1.z * inv, v1.w * inv));
       const int rr = row0 + lr;
+      if (!in_bounds(R.lo + rr / a.G, a.T, a.status, b)) continue;
       *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) +
                                  (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D +
                                  c8 * 8) = pk;
@@ -742,8 +745,9 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
       const int rr = row0 + lr;
       __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.o) +
                            (static_cast<size_t>(R.lo + rr / a.G) * a.Hq + g * a.G + rr % a.G) * D + col0;
+      const bool store = in_bounds(R.lo + rr / a.G, a.T, a.status, b);
 #pragma unroll
-      for (int q8 = 0; q8 < kE / 8; ++q8) {
+      for (int q8 = 0; q8 < kE / 8 && store; ++q8) {
         uint4 pk;
         pk.x = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 0] * inv, acc[q8 * 8 + 1] * inv));
         pk.y = bf16x2_bits(__floats2bfloat162_rn(acc[q8 * 8 + 2] * inv, acc[q8 * 8 + 3] * inv));

@@ -90,6 +90,39 @@ __device__ __forceinline__ void report(int32_t *status, int b, int code) {
   if (status != nullptr && b >= 0) atomicCAS(status + b, 0, code);
 }
 
+// Bounds-checked debug build (-DSPEC_CHECKED): a global access whose index is
+// computed from the inputs first asks in_bounds(i, n, ...) whether 0 <= i < n
+// for its buffer's extent n.  A failed test records SPEC_ERR_INDEX for request
+// b (request 0 when b is not known) and the caller skips the access.  In the
+// normal build the test is the constant true and compiles away.
+#ifdef SPEC_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(long long i, long long n, int32_t *status, int b) {
+  if constexpr (!kChecked) {
+    return true;
+  } else {
+    if (i >= 0 && i < n) return true;
+    report(status, b < 0 ? 0 : b, SPEC_ERR_INDEX);
+    return false;
+  }
+}
+
+// The range [i, i + len) lies inside [0, n).
+__device__ __forceinline__ bool range_in_bounds(long long i, long long len, long long n,
+                                                int32_t *status, int b) {
+  if constexpr (!kChecked) {
+    return true;
+  } else {
+    if (i >= 0 && len >= 0 && i + len <= n) return true;
+    report(status, b < 0 ? 0 : b, SPEC_ERR_INDEX);
+    return false;
+  }
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -74,15 +74,17 @@ kv_compact_kernel(const KvArgs a) {
   for (int i = tid; i < total; i += kKvThreads) {
     const int kv = i / (acc * chunks), rem = i % (acc * chunks);
     const int j = rem / chunks, c = rem % chunks;
-    const uint8_t *src = (kv ? a.v : a.k) + (head + L + __ldg(pn + j + 1)) * row_bytes;
-    rows[i] = __ldcs(reinterpret_cast<const uint4 *>(src) + c);
+    const int x = __ldg(pn + j + 1);
+    const uint8_t *src = (kv ? a.v : a.k) + (head + L + x) * row_bytes;
+    rows[i] = in_bounds(L + x, a.S_cap, a.status, b) ? __ldcs(reinterpret_cast<const uint4 *>(src) + c)
+                                                      : make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   for (int i = tid; i < total; i += kKvThreads) {
     const int kv = i / (acc * chunks), rem = i % (acc * chunks);
     const int j = rem / chunks, c = rem % chunks;
     uint8_t *dst = (kv ? a.v : a.k) + (head + L + 1 + j) * row_bytes;
-    reinterpret_cast<uint4 *>(dst)[c] = rows[i];
+    if (in_bounds(L + 1 + j, a.S_cap, a.status, b)) reinterpret_cast<uint4 *>(dst)[c] = rows[i];
   }
 }
 

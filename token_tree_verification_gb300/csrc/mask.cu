@@ -35,7 +35,7 @@ build_tree_mask_kernel(const int32_t *__restrict__ parents, const int32_t *__res
   if (i == 0) bad = 0;
   __syncthreads();
   if (i < n) {
-    const int p = __ldg(parents + lo + i);
+    const int p = in_bounds(lo + i, T, status, b) ? __ldg(parents + lo + i) : -2;
     par[i] = p;
     const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
     if (!ok) bad = 1;
@@ -77,7 +77,7 @@ build_tree_mask_kernel(const int32_t *__restrict__ parents, const int32_t *__res
     __syncthreads();
     if (!any) break;
   }
-  if (i < n) {
+  if (i < n && in_bounds(lo + i, T, status, b)) {
     mask[lo + i] = anc[i];
     depth[lo + i] = dep[i];
   }

@@ -15,6 +15,15 @@ extern "C" const char *spec_status_string(int code) {
     case SPEC_ERR_TIMEOUT: return "SPEC_ERR_TIMEOUT: a bounded device wait ran out";
     case SPEC_ERR_PREFIX_RANGE: return "SPEC_ERR_PREFIX_RANGE: prefix does not fit the cache";
     case SPEC_ERR_ALIGNMENT: return "SPEC_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case SPEC_ERR_INDEX: return "SPEC_ERR_INDEX: a computed index fell outside its buffer";
     default: return "unknown spec_status";
   }
+}
+
+extern "C" int spec_build_checked(void) {
+#ifdef SPEC_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
 }

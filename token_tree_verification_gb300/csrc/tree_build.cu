@@ -378,9 +378,11 @@ tree_prune_kernel(const PruneArgs a) {
   if (tid == 0) s_bad = 0;
   __syncthreads();
   if (tid < n) {
-    const int p = __ldg(a.parents + lo + tid);
+    // (the candidate arrays hold cand_offsets[B] entries)
+    const bool in = in_bounds(lo + tid, kChecked ? __ldg(a.offsets + a.B) : 0, a.status, b);
+    const int p = in ? __ldg(a.parents + lo + tid) : -2;
     par[tid] = p;
-    sc[tid] = __ldg(a.scores + lo + tid);
+    sc[tid] = in ? __ldg(a.scores + lo + tid) : -INFINITY;
     if (tid == 0 ? p != -1 : (p < 0 || p >= tid)) s_bad = 1;
   }
   __syncthreads();
@@ -410,7 +412,7 @@ tree_prune_kernel(const PruneArgs a) {
   for (int k = 0; k < w; ++k) before += wsum[k];
   newid[tid] = keep_me ? before : -1;
   __syncthreads();
-  if (keep_me && tid < n) {
+  if (keep_me && tid < n && in_bounds(before, a.keep, a.status, b)) {
     op[before] = tid == 0 ? -1 : newid[par[tid]];
     ot[before] = __ldg(a.tokens + lo + tid);
     ok_[before] = tid;

@@ -51,12 +51,14 @@ tree_merge_kernel(const int32_t *parents_a, const int32_t *tokens_a, const int32
   }
   for (int i = tid; i < kMergeCap; i += kMergeThreads) {
     if (i < na) {
-      sm.pa[i] = __ldg(parents_a + lo_a + i);
-      sm.ta[i] = __ldg(tokens_a + lo_a + i);
+      const bool in = in_bounds(lo_a + i, Ta, status, b);
+      sm.pa[i] = in ? __ldg(parents_a + lo_a + i) : -2;
+      sm.ta[i] = in ? __ldg(tokens_a + lo_a + i) : -1;
     }
     if (i < nb) {
-      sm.pb[i] = __ldg(parents_b + lo_b + i);
-      sm.tb[i] = __ldg(tokens_b + lo_b + i);
+      const bool in = in_bounds(lo_b + i, Tb, status, b);
+      sm.pb[i] = in ? __ldg(parents_b + lo_b + i) : -2;
+      sm.tb[i] = in ? __ldg(tokens_b + lo_b + i) : -1;
     }
   }
   __syncthreads();
@@ -167,8 +169,10 @@ tree_merge_kernel(const int32_t *parents_a, const int32_t *tokens_a, const int32
   for (int i = tid; i < nb; i += kMergeThreads) {
     if (i > 0 && sm.rep[i] == na + i) {
       const int j = sm.idx[i];
-      op[j] = sm.scan[sm.pb[i]];
-      ot[j] = sm.tb[i];
+      if (in_bounds(j, kMergeCap, status, b)) {
+        op[j] = sm.scan[sm.pb[i]];
+        ot[j] = sm.tb[i];
+      }
     }
   }
   if (tid == 0) n_out[b] = n;

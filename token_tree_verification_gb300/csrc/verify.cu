@@ -369,7 +369,8 @@ tree_verify_cluster_kernel(const VerifyArgs a) {
       }
     }
     // every CTA computed the same decisions; the writer publishes them
-    if (rank == writer && tid < k) a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
+    if (rank == writer && tid < k && in_bounds(c.lo + ts.child[tid], a.T, a.status, c.b))
+      a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
   } else if (c.err && rank == 0 && tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }

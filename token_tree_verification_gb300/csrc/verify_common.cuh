@@ -196,8 +196,9 @@ static __device__ bool walk_request(const VerifyArgs &a, int b, int lo, int n, c
   for (int s = 0; s < 4; ++s) {
     const int i = lane + 32 * s;
     par[s] = i < n ? spar[i] : -2;
-    flg[s] = i < n ? __ldcg(a.flags + lo + i) : 0;
-    fbk[s] = i < n ? __ldcg(a.fallback + lo + i) : 0;
+    const bool in = i < n && in_bounds(lo + i, a.T, a.status, b);
+    flg[s] = in ? __ldcg(a.flags + lo + i) : 0;
+    fbk[s] = in ? __ldcg(a.fallback + lo + i) : 0;
   }
   if (!path_fits(a, b, n, spar)) return false;
   int32_t *pn = a.path_nodes + static_cast<size_t>(b) * a.W;
@@ -251,11 +252,11 @@ static __device__ bool walk_request(const VerifyArgs &a, int b, int lo, int n, c
       const int f3 = __shfl_sync(0xffffffffu, fbk[3], cur & 31);
       const int sl = cur >> 5;
       const int fb = sl == 0 ? f0 : (sl == 1 ? f1 : (sl == 2 ? f2 : f3));
-      if (lane == 0) ot[acc] = fb & 0x7fffffff;
+      if (lane == 0 && in_bounds(acc, a.W, a.status, b)) ot[acc] = fb & 0x7fffffff;
       ties += (fb >> 31) & 1;
       break;
     }
-    if (lane == 0) {
+    if (lane == 0 && in_bounds(acc + 1, a.W, a.status, b)) {
       ot[acc] = stok[next];
       pn[acc + 1] = next;
     }
@@ -637,10 +638,11 @@ static __device__ void arrive_and_walk(const VerifyArgs &a, const NodeCtx &c, Tr
   const int leaf = ts.leaf[0];
   if (leaf < 0) return;
   // the walk accepted the path down to a leaf: the bonus token is its draw
+  if (!in_bounds(c.lo + leaf, a.T, a.status, c.b)) return;   // CTA-uniform
   const float *row = a.target + static_cast<size_t>(c.lo + leaf) * a.V;
   const int r = cta_leaf_draw(row, a.V, a.inv_temp * 1.4426950408889634f,
                               spec_uniform(a.seed, leaf, c.b, 1), ts);
-  if (tid == 0) {
+  if (tid == 0 && in_bounds(ts.leaf[1], a.W, a.status, c.b)) {
     a.out_tokens[static_cast<size_t>(c.b) * a.W + ts.leaf[1]] = r & 0x7fffffff;
     a.near_ties[c.b] = ts.leaf[2] + ((r >> 31) & 1);
   }

@@ -78,7 +78,7 @@ tree_verify_greedy_node_kernel(const VerifyArgs a) {
       for (int j = 0; j < c.k; ++j) {
         const int ch = ts.child[j];
         const bool hit = ts.tok[ch] == g.i;
-        a.flags[c.lo + ch] = hit ? kFlagAccept : 0;
+        if (in_bounds(c.lo + ch, a.T, a.status, c.b)) a.flags[c.lo + ch] = hit ? kFlagAccept : 0;
         accepted |= hit;
       }
       ts.stop_fb = accepted ? -1 : g.i;   // -1: the walk goes on below this node

@@ -325,8 +325,10 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       if (j < k) {
         const int ch = ts.child[j];
         const int x = ts.tok[ch];
-        rawP[s] = __ldg(trow + x);
-        rawQ[s] = __ldg(drow + x);
+        if (in_bounds(x, a.V, a.status, c.b)) {
+          rawP[s] = __ldg(trow + x);
+          rawQ[s] = __ldg(drow + x);
+        }
         ns.U[j] = spec_uniform(a.seed, ch, c.b, 0);
       } else if (j == k) {
         ns.u_fb = spec_uniform(a.seed, c.u, c.b, 1);
@@ -991,7 +993,8 @@ tree_verify_reg_kernel(const VerifyArgs a) {
       }
     }
     // every CTA computed the same decisions; the writer publishes them
-    if (rank == writer && tid < k) a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
+    if (rank == writer && tid < k && in_bounds(c.lo + ts.child[tid], a.T, a.status, c.b))
+      a.flags[c.lo + ts.child[tid]] = tid <= stop ? my_flag : 0;
   } else if (c.err && rank == 0 && tid == 0 && c.b >= 0) {
     report(a.status, c.b, c.err);
   }
