@@ -174,6 +174,21 @@ def test_top_p_small_and_edge_vocabularies(gpu_lib):
             assert g["near_ties"].sum() <= 1
 
 
+def test_top_p_near_one(gpu_lib):
+    # Near top_p = 1 the nucleus holds nearly every entry, and at the largest
+    # float below 1 the rows' fixed-point totals fall short of top_p on many
+    # rows (rounding), where the kernel keeps every entry of positive mass.
+    w = synthetic.make_workload("llama7b", seed=2, L=64)
+    for top_p in (0.999, 0.99999994):
+        for seed in range(3):
+            g, o, ex = check(w, seed, top_p=top_p, max_exempt=2)
+            assert (g["status"] == 0).all()
+    w = synthetic.make_workload("tiny", seed=7, V=32003, B=3, N=12, depth=3, width=4)
+    for top_p in (0.999, 0.99999994):
+        g, o, ex = check(w, 11, temperature=0.9, top_p=top_p, max_exempt=1)
+        assert (g["status"] == 0).all()
+
+
 def test_top_p_leaves_greedy_unchanged(gpu_lib):
     w = synthetic.make_workload("tiny", seed=4, B=4, N=10, V=300)
     a = gpu_verify(w, 2, temperature=0.0)
