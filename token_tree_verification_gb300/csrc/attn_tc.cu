@@ -97,6 +97,10 @@ struct TcCfg {
 
 constexpr int kTcMaxSplits = 8;
 constexpr int kEarlyTiles = 2;   // K/V tiles requested with Q, before tile 0 lands
+// K/V tiles of a split prefetched into L2 before the PDL wait: one, so that
+// every split's first tile arrives ahead of the rest of the ring's initial
+// fill (a deeper prefetch queues all of them together in HBM).
+constexpr int kPrefetchTiles = 1;
 
 
 
@@ -243,14 +247,14 @@ tree_attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq,
     tma_prefetch_desc(&tmv);
     if (a.prefetch_keys > 0) {
       // One request whose key count the host knows: this split's first
-      // tiles, and its Q rows, are prefetched into L2 while the previous
+      // tile, and its Q rows, are prefetched into L2 while the previous
       // kernel still runs.  A prefetch only warms L2, which every write of
       // the previous kernel updates, so it can never serve stale data; if the
       // request's real key count differs, the prefetched lines are unused.
       const int tiles = (a.prefetch_keys + kKeyTile - 1) / kKeyTile;
       const int per = (tiles + CS - 1) / CS;
       const int t0 = split * per;
-      const int nt = min(NS, min(t0 + per, tiles) - t0);
+      const int nt = min(kPrefetchTiles, min(t0 + per, tiles) - t0);
       for (int i = 0; i < nt; ++i)
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx) {
